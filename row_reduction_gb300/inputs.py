@@ -1,0 +1,93 @@
+"""Seeded synthetic inputs for the six per-row operators.
+
+This module only draws random numbers; it holds none of the operators'
+arithmetic.  The tests, the benchmark and the smoke check use it to feed the
+same inputs to the CUDA library and to the CPU oracle.
+
+Recipe (NumPy ``default_rng(seed)``, PCG64, FP32 draws):
+
+* x ~ N(0, 1); with ``outliers=True`` a mask ``rng.random(shape) < 0.01``
+  selects about 1% of the entries, which are scaled by 100.
+* softmax and cross-entropy inputs are N(0, 2^2).
+* RMSNorm weight and LayerNorm gamma ~ 1 + 0.1 N(0, 1); beta ~ 0.1 N(0, 1).
+* residual ~ N(0, 1).
+* labels ~ uniform integers in [0, cols), int32.
+* eps: 1e-6 for RMSNorm, 1e-5 for LayerNorm and residual LayerNorm.
+
+The tuning seed is ``TUNE_SEED``; held-out validation uses ``HOLDOUT_SEED``.
+Workload ``k`` of a list uses ``seed + k``.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+TUNE_SEED = 20260905
+HOLDOUT_SEED = 20261202
+
+OPS = ("rmsnorm", "layernorm", "residual_layernorm", "softmax", "row_sum",
+       "cross_entropy")
+
+RMS_EPS = 1e-6
+LN_EPS = 1e-5
+
+# The published RMSNorm shapes: an odd single row (tail path), short odd rows
+# (row packing), few wide rows (cross-warp cooperation), then the bandwidth
+# sweep, whose shapes carry 1% outliers.
+RMSNORM_SHAPES = [(1, 127), (17, 257), (64, 4096)]
+RMSNORM_SWEEP = [(1024, 4096), (16384, 4096), (65536, 4096), (8192, 1024),
+                 (8192, 8192), (8192, 16384)]
+# The operator-family shapes.
+FAMILY_SHAPES = [(1, 127), (17, 257), (64, 4096), (1024, 4096)]
+
+
+def _normal(rng, shape, scale=1.0):
+    a = rng.standard_normal(shape, dtype=np.float32)
+    if scale != 1.0:
+        a *= np.float32(scale)
+    return a
+
+
+def make(op: str, rows: int, cols: int, seed: int, outliers: bool = False,
+         affine: bool = True) -> dict:
+    """Inputs for one call of ``op`` on a rows x cols FP32 matrix.
+
+    Returns a dict with NumPy arrays (``x`` and, per op, ``weight``,
+    ``gamma``, ``beta``, ``residual``, ``labels``) and the scalar ``eps``.
+    ``affine=False`` leaves the weight / gamma / beta out (identity).
+    """
+    rng = np.random.default_rng(seed)
+    shape = (rows, cols)
+    if op in ("softmax", "cross_entropy"):
+        x = _normal(rng, shape, 2.0)
+    else:
+        x = _normal(rng, shape)
+    if outliers:
+        mask = rng.random(shape, dtype=np.float32) < np.float32(0.01)
+        x[mask] *= np.float32(100.0)
+    d = {"x": x}
+    if op == "rmsnorm":
+        d["eps"] = RMS_EPS
+        if affine:
+            d["weight"] = np.float32(1.0) + _normal(rng, (cols,), 0.1)
+    elif op in ("layernorm", "residual_layernorm"):
+        d["eps"] = LN_EPS
+        if op == "residual_layernorm":
+            d["residual"] = _normal(rng, shape)
+        if affine:
+            d["gamma"] = np.float32(1.0) + _normal(rng, (cols,), 0.1)
+            d["beta"] = _normal(rng, (cols,), 0.1)
+    elif op == "cross_entropy":
+        d["labels"] = rng.integers(0, cols, rows, dtype=np.int32)
+    elif op in ("softmax", "row_sum"):
+        pass
+    else:
+        raise ValueError(f"unknown op {op!r}")
+    return d
+
+
+def integer_valued(rows: int, cols: int, seed: int, lo: int = -8,
+                   hi: int = 8) -> np.ndarray:
+    """Small integers stored as FP32: every partial sum of a row of up to
+    2^20 of them is an exact FP32 integer, whatever the addition order."""
+    rng = np.random.default_rng(seed)
+    return rng.integers(lo, hi + 1, (rows, cols)).astype(np.float32)
