@@ -1,0 +1,579 @@
+#!/usr/bin/env python3
+"""Benchmark of the per-row FP32 reduction library on GB300.
+
+One step = one call of the headline operator (RMSNorm, FP32) over one
+rows x cols matrix, through the C ABI.  Default workload: RMSNorm 1024x4096,
+x ~ N(0,1) with 1% outliers x100, weight ~ 1 + 0.1 N(0,1), eps = 1e-6.
+
+Device timing: the K timed steps run back to back on one stream, replayed
+from CUDA graphs of captured library calls (so host launch cost is not in the
+number), bracketed by CUDA events with a synchronize (and, for N > 1, a
+barrier) on both sides.  Consecutive steps cycle through a pool of input /
+output buffers at least 4x the L2 size, so no step finds its input in L2.
+`value` = algorithmic bytes moved per step x steps / time, in GB/s (the
+HBM-bandwidth form of the metric; `us_per_op` gives the time form).
+
+Also reported: `e2e` (same metric, each step copying x from pinned host
+memory and y back, around the library call), `roofline` (vs the measured HBM
+copy bandwidth), `cpu_baseline` (the CPU oracle on the host cores),
+`clocks` (nvidia-smi samples during the timed region), `plain_launch` (the
+same steps launched one by one from Python instead of replayed from graphs)
+and `sweep` (every published shape and operator, same method).
+
+`--impl reference` times the CPU oracle instead, on a bounded row sample of
+the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = ("RMSNorm FP32 µs/op and HBM GB/s (% of GB300 peak), "
+          "1×127 … 1024×4096")
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------- helpers
+def algorithmic_bytes(op, rows, cols, h_out=False, mean=False):
+    """Bytes an operator must move once: each input read once, each output
+    written once, parameter vectors counted once."""
+    rc = rows * cols
+    if op == "rmsnorm":
+        return 8 * rc + 4 * cols
+    if op == "layernorm":
+        return 8 * rc + 8 * cols
+    if op == "residual_layernorm":
+        return 12 * rc + 8 * cols + (4 * rc if h_out else 0)
+    if op == "softmax":
+        return 8 * rc
+    if op == "row_sum":
+        return 4 * rc + 4 * rows
+    if op == "cross_entropy":
+        return 4 * rc + 8 * rows + (4 if mean else 0)
+    raise ValueError(op)
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sources_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "row_reduction_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(workload_key):
+    """DRAM bytes per launch from the committed ncu summary of this
+    workload, if it was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"{workload_key}.ncu.txt")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    for line in open(path):
+        if ":" in line:
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip()
+    if fields.get("kernel_sources_sha256") != kernel_sources_sha():
+        return None
+    try:
+        return int(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,"
+             "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}",
+                 f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sms, maxs, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sms.append(float(f[1]))
+                maxs.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "samples": 0}
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxs),
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+# ------------------------------------------------------------ GPU harness
+class Workload:
+    """A pool of buffer sets for one (op, rows, cols) plus fast launchers."""
+
+    def __init__(self, op, rows, cols, seed, outliers, l2_bytes,
+                 max_pool_bytes=16 << 30):
+        import torch
+        import row_reduction_gb300 as mt
+        from row_reduction_gb300 import inputs
+        self.op, self.rows, self.cols = op, rows, cols
+        d = inputs.make(op, rows, cols, seed, outliers=outliers)
+        self.host = d
+        self.eps = float(d.get("eps", 0.0))
+        self.mean = op == "cross_entropy"
+        self.h_out = op == "residual_layernorm"
+        self.bytes = algorithmic_bytes(op, rows, cols, self.h_out, self.mean)
+        params = {k: torch.from_numpy(d[k]).cuda() for k in
+                  ("weight", "gamma", "beta") if k in d}
+        set_bytes = max(self.bytes, 1)
+        n = max(1, math.ceil(4 * l2_bytes / set_bytes))
+        n = max(1, min(n, max_pool_bytes // set_bytes, 256))
+        self.sets = []
+        for i in range(n):
+            s = dict(params)
+            s["x"] = torch.from_numpy(d["x"]).cuda()
+            if "residual" in d:
+                s["residual"] = torch.from_numpy(d["residual"]).cuda()
+            if "labels" in d:
+                s["labels"] = torch.from_numpy(d["labels"]).cuda()
+            if op in ("rmsnorm", "layernorm", "softmax",
+                      "residual_layernorm"):
+                s["y"] = torch.empty_like(s["x"])
+            if self.h_out:
+                s["h_out"] = torch.empty_like(s["x"])
+            if op == "row_sum":
+                s["out"] = torch.empty(rows, device="cuda")
+            if op == "cross_entropy":
+                s["loss"] = torch.empty(rows, device="cuda")
+                s["mean_loss"] = torch.empty(1, device="cuda")
+            self.sets.append(s)
+        self.pool_bytes = n * set_bytes
+        # Tiny shapes cannot fill 4x L2 with 256 sets; they are launch-bound
+        # and reported as "l2_resident".
+        self.l2_resident = self.pool_bytes < 4 * l2_bytes
+        self.launches_per_step = 2 if self.mean else 1
+        self.plan_text = mt.mt_describe_plan(mt.mt_plan_query(op, rows, cols))
+
+    def call_fn(self, i, stream_handle):
+        """A zero-argument callable issuing step i's library call (raw
+        ctypes entry point, arguments prepared once)."""
+        import ctypes
+        import row_reduction_gb300 as mt
+        L = mt.lib()
+        s = self.sets[i % len(self.sets)]
+        P = lambda k: s[k].data_ptr() if k in s else None  # noqa: E731
+        R, C, eps = self.rows, self.cols, ctypes.c_float(self.eps)
+        st = stream_handle
+        if self.op == "rmsnorm":
+            f, a = L.mt_rmsnorm_f32, (P("x"), P("weight"), P("y"), R, C, eps,
+                                      st)
+        elif self.op == "layernorm":
+            f, a = L.mt_layernorm_f32, (P("x"), P("gamma"), P("beta"),
+                                        P("y"), R, C, eps, st)
+        elif self.op == "residual_layernorm":
+            f, a = L.mt_residual_layernorm_f32, (
+                P("x"), P("residual"), P("gamma"), P("beta"), P("y"),
+                P("h_out"), R, C, eps, st)
+        elif self.op == "softmax":
+            f, a = L.mt_softmax_f32, (P("x"), P("y"), R, C, st)
+        elif self.op == "row_sum":
+            f, a = L.mt_row_sum_f32, (P("x"), P("out"), R, C, st)
+        else:
+            f, a = L.mt_cross_entropy_f32, (P("x"), P("labels"), P("loss"),
+                                            P("mean_loss"), R, C, st)
+
+        def go():
+            rc = f(*a)
+            if rc != 0:
+                raise RuntimeError(f"{self.op} failed with status {rc}")
+        return go
+
+
+def capture(work, first, count, stream):
+    """A CUDA graph of `count` consecutive steps starting at step `first`."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        h = torch.cuda.current_stream().cuda_stream
+        for i in range(first, first + count):
+            work.call_fn(i, h)()
+    return g
+
+
+def time_graph_steps(work, steps, warmup, per_graph=64, barrier=None,
+                     sampler=None):
+    """Times exactly `steps` steps (after `warmup`) replayed from graphs;
+    returns elapsed seconds on the device."""
+    import torch
+    stream = torch.cuda.Stream()
+    h = stream.cuda_stream
+    with torch.cuda.stream(stream):
+        for i in range(3):                       # fill the library's caches
+            work.call_fn(i, h)()
+    stream.synchronize()
+    # Graphs cycle through whole pools, so consecutive steps never reuse a
+    # buffer set before every other set has been used.
+    n = len(work.sets)
+    G = n * max(1, math.ceil(per_graph / n))
+    if steps < G:
+        G = steps
+    full = capture(work, 0, G, stream)
+    rem = steps % G
+    tail = capture(work, 0, rem, stream) if rem else None
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, math.ceil(warmup / G))):
+            full.replay()
+    stream.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    ctx = sampler if sampler is not None else _Null()
+    with ctx:
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for _ in range(steps // G):
+                full.replay()
+            if tail is not None:
+                tail.replay()
+            end.record(stream)
+        end.synchronize()
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    return start.elapsed_time(end) / 1e3
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+def time_plain_steps(work, steps, warmup):
+    """Same steps, each launched from Python (host launch cost included)."""
+    import torch
+    stream = torch.cuda.Stream()
+    h = stream.cuda_stream
+    fns = [work.call_fn(i, h) for i in range(len(work.sets))]
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            fns[i % len(fns)]()
+    stream.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for i in range(steps):
+            fns[i % len(fns)]()
+        end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / 1e3
+
+
+def time_e2e(work, steps, warmup):
+    """Each step: pinned host x -> device, library call, y -> pinned host."""
+    import torch
+    s0 = work.sets[0]
+    x_host = torch.from_numpy(work.host["x"]).pin_memory()
+    out_key = {"row_sum": "out", "cross_entropy": "loss"}.get(work.op, "y")
+    out_host = torch.empty(s0[out_key].shape, dtype=s0[out_key].dtype,
+                           pin_memory=True)
+    stream = torch.cuda.Stream()
+    h = stream.cuda_stream
+    fn = work.call_fn(0, h)
+
+    def step():
+        s0["x"].copy_(x_host, non_blocking=True)
+        fn()
+        out_host.copy_(s0[out_key], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step()
+    stream.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(steps):
+            step()
+        end.record(stream)
+    end.synchronize()
+    return (start.elapsed_time(end) / 1e3, x_host.numel() * 4,
+            out_host.numel() * 4)
+
+
+def cpu_baseline(op, d, rows, cols, budget_s=10.0):
+    """The CPU oracle as it stands, single-threaded, on the same inputs,
+    repeated for about `budget_s` seconds."""
+    import oracle
+    oracle.build()
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.run(op, d)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or (reps >= 1 and el * (reps + 1) / reps > 3 * budget_s):
+            break
+    b = algorithmic_bytes(op, rows, cols, op == "residual_layernorm",
+                          op == "cross_entropy")
+    return {"value": b * reps / el / 1e9, "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"{op} {rows}x{cols} (the full workload) x {reps} "
+                      f"repetitions, {el:.1f} s, one thread",
+            "us_per_op": el / reps * 1e6}
+
+
+# ---------------------------------------------------------------- arms
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    import oracle
+    from row_reduction_gb300 import inputs
+    oracle.build()
+    rows, cols = args.rows, args.cols
+    d = inputs.make(args.op, rows, cols, inputs.TUNE_SEED, outliers=True)
+    # Size the per-step row sample so the whole run stays near 60 s.
+    def rows_of(n):
+        return {k: (v[:n] if isinstance(v, np.ndarray) and
+                    k in ("x", "residual", "labels") else v)
+                for k, v in d.items()}
+    t0 = time.perf_counter()
+    oracle.run(args.op, rows_of(8))
+    per_row = max((time.perf_counter() - t0) / 8, 1e-7)
+    total_steps = args.steps + args.warmup
+    sample_rows = int(max(1, min(rows, 60.0 / total_steps / per_row)))
+    sub = rows_of(sample_rows)
+    for _ in range(args.warmup):
+        oracle.run(args.op, sub)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.run(args.op, sub)
+    el = time.perf_counter() - t0
+    b = algorithmic_bytes(args.op, sample_rows, cols)
+    value = b * args.steps / el / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"{args.op}_f32 {rows}x{cols}", "op": args.op,
+                   "rows": rows, "cols": cols,
+                   "sample_rows_per_step": sample_rows},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1,
+                         "kind": "oracle",
+                         "sample": f"first {sample_rows} of {rows} rows "
+                                   f"per step, one thread"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    import row_reduction_gb300 as mt
+    from row_reduction_gb300 import build as mt_build, inputs
+
+    mt_build.build()
+    mt.lib()
+    torch.cuda.set_device(local_rank)
+    props = torch.cuda.get_device_properties(local_rank)
+    l2 = int(getattr(props, "L2_cache_size", 126 << 20)) or (126 << 20)
+    barrier = (lambda: dist.barrier()) if world > 1 else None
+
+    work = Workload(args.op, args.rows, args.cols, inputs.TUNE_SEED,
+                    outliers=True, l2_bytes=l2)
+    sampler = ClockSampler(local_rank)
+    elapsed = time_graph_steps(work, args.steps, args.warmup,
+                               barrier=barrier, sampler=sampler)
+    if world > 1:
+        t = torch.tensor([elapsed], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+    per_step = elapsed / args.steps
+    value = world * work.bytes * args.steps / elapsed / 1e9
+    if rank != 0:
+        return 0
+
+    peak, peak_kind = measured_peak()
+    key = f"{args.op}_f32_{args.rows}x{args.cols}"
+    achieved = work.bytes / per_step / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak,
+                "unit": "GB/s", "frac": achieved / peak,
+                "traffic": profiled_traffic(key),
+                "peak_source": f"{peak_kind} HBM copy bandwidth "
+                               "(MEASURED_PEAKS.json hbm_gbs)"
+                if peak_kind == "measured" else "fallback 6.8 TB/s"}
+
+    plain = time_plain_steps(work, min(args.steps, 20000),
+                             min(args.warmup, 200))
+    plain_steps = min(args.steps, 20000)
+    e2e_steps = max(3, min(args.steps, 200))
+    e2e_el, bi, bo = time_e2e(work, e2e_steps, 3)
+    e2e = {"value": work.bytes * e2e_steps / e2e_el / 1e9, "unit": "GB/s",
+           "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+           "us_per_step": e2e_el / e2e_steps * 1e6}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": per_step * 1e3, "us_per_op": per_step * 1e6,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {
+            "workload": f"{args.op}_f32 rows={args.rows} cols={args.cols}, "
+                        "x~N(0,1) with 1% x100 outliers, "
+                        "weight~1+0.1N(0,1), eps=1e-6",
+            "op": args.op, "rows": args.rows, "cols": args.cols,
+            "plan": work.plan_text,
+            "l2": f"inputs larger than L2: rotating pool of "
+                  f"{len(work.sets)} buffer sets, "
+                  f"{work.pool_bytes / 2**20:.0f} MiB >= 4x L2 "
+                  f"({l2 / 2**20:.0f} MiB)",
+            "timing": "CUDA graphs of captured library calls, back to back "
+                      "on one stream, CUDA events",
+            "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": roofline,
+        "e2e": e2e,
+        "gpu_launches": args.steps * work.launches_per_step,
+        "clocks": sampler.summary(),
+        "plain_launch": {"value": work.bytes * plain_steps / plain / 1e9,
+                         "unit": "GB/s",
+                         "us_per_op": plain / plain_steps * 1e6,
+                         "steps": plain_steps,
+                         "note": "one Python ctypes call per step"},
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.op, work.host, args.rows,
+                                            args.cols, args.cpu_seconds)
+    if world == 1 and not args.no_sweep:
+        line["sweep"] = run_sweep(l2, peak)
+    print(json.dumps(line))
+    return 0
+
+
+def run_sweep(l2, peak):
+    """Every published shape: RMSNorm shapes and bandwidth sweep, then the
+    operator family, each timed like the headline."""
+    from row_reduction_gb300 import inputs
+    cases = [("rmsnorm", r, c, False) for r, c in inputs.RMSNORM_SHAPES]
+    cases += [("rmsnorm", r, c, True) for r, c in inputs.RMSNORM_SWEEP]
+    cases += [(op, r, c, False) for op in inputs.OPS if op != "rmsnorm"
+              for r, c in inputs.FAMILY_SHAPES]
+    out = []
+    import torch
+    for op, r, c, outl in cases:
+        work = Workload(op, r, c, inputs.TUNE_SEED, outliers=outl,
+                        l2_bytes=l2, max_pool_bytes=8 << 30)
+        # about 0.25 s of timed work, at least 64 steps
+        probe = time_graph_steps(work, 64, 16)
+        steps = int(max(64, min(200000, 0.25 / max(probe / 64, 1e-7))))
+        el = time_graph_steps(work, steps, max(16, steps // 20))
+        us = el / steps * 1e6
+        gbs = work.bytes / (el / steps) / 1e9
+        out.append({"op": op, "rows": r, "cols": c, "outliers": outl,
+                    "us_per_op": us, "gbs": gbs, "frac_of_peak": gbs / peak,
+                    "plan": work.plan_text, "pool_sets": len(work.sets),
+                    "l2_resident": work.l2_resident, "steps": steps})
+        del work
+        torch.cuda.empty_cache()
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100000)
+    ap.add_argument("--warmup", type=int, default=2000)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--op", default="rmsnorm")
+    ap.add_argument("--rows", type=int, default=1024)
+    ap.add_argument("--cols", type=int, default=4096)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        return run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

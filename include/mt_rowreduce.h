@@ -1,0 +1,219 @@
+/*
+ * mt_rowreduce.h -- C ABI of a GB300 (sm_103a) library of per-row FP32
+ * reductions: RMSNorm, LayerNorm, residual LayerNorm, softmax, row sum and
+ * cross-entropy.
+ *
+ * Operator family: "Consecutive-worker reduction layout checkpoint",
+ * §Evidence and what remains (generic V=4 operator coverage: sum, softmax,
+ * RMSNorm, LayerNorm, residual LayerNorm and cross-entropy).  RMSNorm
+ * semantics: "Thread Ownership and Software Staging", §Register-tiled
+ * reductions (the rmsnorm_register kernel: FP32 reduction and epilogue, one
+ * rounding at the output store).  Work mapping: "Consecutive-worker reduction
+ * layout checkpoint", §Implementation and semantics (W workers per row, V
+ * consecutive values per worker, full/tail split, private-slot bound).
+ *
+ * Conventions shared by every call below
+ * -------------------------------------
+ * Layout     every matrix is rows x cols, FP32, contiguous row-major (row r
+ *            starts at element r*cols); vectors (weight, gamma, beta) hold
+ *            cols FP32 values; per-row outputs hold rows FP32 values; labels
+ *            hold rows int32 values.
+ * Memory     every data pointer is a DEVICE pointer owned by the caller and
+ *            must be at least 4-byte aligned.  Calls allocate no device
+ *            memory and never synchronise the host; work is enqueued on
+ *            `stream` (NULL = the legacy default stream) on the current
+ *            device, and device-side faults surface at the caller's next
+ *            synchronisation.  16-byte aligned pointers and cols % 4 == 0 get
+ *            the fully vectorised path; other alignments are handled by a
+ *            per-row scalar head before the vector body.
+ * Aliasing   y == x (in place) is allowed; so are h_out == x and
+ *            h_out == residual.  Any other (partial) overlap between an
+ *            output and an input is undefined.
+ * Errors     arguments are checked before anything is enqueued: a NULL
+ *            required pointer, a pointer that is not 4-byte aligned,
+ *            rows < 0, cols < 1, cols > INT32_MAX or rows*cols overflowing
+ *            int64 give MT_ERR_INVALID_ARGUMENT and enqueue nothing.
+ *            rows == 0 returns MT_OK without a launch (outputs untouched).
+ *            A failed launch gives MT_ERR_CUDA (mt_last_cuda_error() has the
+ *            cudaError_t value).  A forced plan that is malformed gives
+ *            MT_ERR_INVALID_ARGUMENT; one that cannot hold the row or
+ *            exceeds the kernel's thread limit gives MT_ERR_OUT_OF_RESOURCES.
+ *            Plans are never silently remapped.
+ * Numerics   all arithmetic is FP32 with one rounding at each output store;
+ *            the addition order depends on the plan (W, V, chunks), and the
+ *            same inputs with the same plan give bit-identical outputs.  No
+ *            float atomics are used.
+ */
+#ifndef MT_ROWREDUCE_H
+#define MT_ROWREDUCE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MT_API __attribute__((visibility("default")))
+#else
+#define MT_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *mt_stream_t;
+
+typedef enum mt_status {
+    MT_OK = 0,
+    MT_ERR_INVALID_ARGUMENT = 1,
+    MT_ERR_UNSUPPORTED = 2,
+    MT_ERR_OUT_OF_RESOURCES = 3,
+    MT_ERR_CUDA = 4
+} mt_status;
+
+typedef enum mt_op {
+    MT_OP_RMSNORM = 0,
+    MT_OP_LAYERNORM = 1,
+    MT_OP_RESIDUAL_LAYERNORM = 2,
+    MT_OP_SOFTMAX = 3,
+    MT_OP_ROW_SUM = 4,
+    MT_OP_CROSS_ENTROPY = 5
+} mt_op;
+
+typedef enum mt_path {
+    /* The whole row is read once into registers (V*chunks values per
+     * thread) and written from them. */
+    MT_PATH_REGISTERS = 0,
+    /* Rows too wide for registers: a strided loop computes the statistics
+     * and a second (LayerNorm: third) loop re-reads x to write y.  Row sum
+     * and cross-entropy need only the first loop. */
+    MT_PATH_LOOP = 1
+} mt_path;
+
+/* One launch configuration ("plan").  In the pages' notation W =
+ * threads_per_row cooperating workers per row, V = values_per_thread
+ * consecutive values each worker owns per chunk; element i of a row (after
+ * its alignment head) belongs to worker (i / V) % W, chunk i / (W*V), slot
+ * (chunk*V + i % V).  ("Consecutive-worker reduction layout checkpoint",
+ * §Implementation and semantics.) */
+typedef struct mt_plan {
+    int32_t threads_per_row;   /* W: power of two, 1..1024 */
+    int32_t values_per_thread; /* V: 1, 2 or 4 (V=4: one 16-byte access) */
+    int32_t chunks;            /* register path: chunks held per thread, one
+                                  of 1, 2, 4, 8, 16; W*V*chunks >= cols.
+                                  Loop path: ignored (set 0). */
+    int32_t rows_per_block;    /* B >= 1 rows per CTA; W*B threads per CTA,
+                                  a multiple of 32 and <= 1024 */
+    int32_t path;              /* mt_path */
+    int32_t grid;              /* CTAs to launch; 0 = min(row groups, CTAs
+                                  resident on the device), the CTAs then loop
+                                  over row groups (grid-stride) */
+} mt_plan_t;
+
+/* ---- operators ---------------------------------------------------------
+ * Each takes its plan from the built-in, measured plan table
+ * (mt_plan_query).  The *_with_plan forms take an explicit plan; plan ==
+ * NULL means the table's plan. */
+
+/* RMSNorm per row: y = x / sqrt(mean(x^2) + eps) * weight.
+ * weight may be NULL (all ones).  ("Thread Ownership and Software Staging",
+ * §Register-tiled reductions, rmsnorm_register.) */
+MT_API mt_status mt_rmsnorm_f32(const float *x, const float *weight, float *y,
+                         int64_t rows, int64_t cols, float eps,
+                         mt_stream_t stream);
+MT_API mt_status mt_rmsnorm_f32_with_plan(const float *x, const float *weight,
+                                   float *y, int64_t rows, int64_t cols,
+                                   float eps, mt_stream_t stream,
+                                   const mt_plan_t *plan);
+
+/* LayerNorm per row: mu = mean(x), var = mean((x-mu)^2) (biased),
+ * y = (x - mu) / sqrt(var + eps) * gamma + beta.  gamma may be NULL (ones),
+ * beta may be NULL (zeros). */
+MT_API mt_status mt_layernorm_f32(const float *x, const float *gamma,
+                           const float *beta, float *y, int64_t rows,
+                           int64_t cols, float eps, mt_stream_t stream);
+MT_API mt_status mt_layernorm_f32_with_plan(const float *x, const float *gamma,
+                                     const float *beta, float *y,
+                                     int64_t rows, int64_t cols, float eps,
+                                     mt_stream_t stream,
+                                     const mt_plan_t *plan);
+
+/* Residual LayerNorm per row: h = x + residual (FP32 add);
+ * y = LayerNorm(h) as above; if h_out != NULL it receives h. */
+MT_API mt_status mt_residual_layernorm_f32(const float *x, const float *residual,
+                                    const float *gamma, const float *beta,
+                                    float *y, float *h_out, int64_t rows,
+                                    int64_t cols, float eps,
+                                    mt_stream_t stream);
+MT_API mt_status mt_residual_layernorm_f32_with_plan(
+    const float *x, const float *residual, const float *gamma,
+    const float *beta, float *y, float *h_out, int64_t rows, int64_t cols,
+    float eps, mt_stream_t stream, const mt_plan_t *plan);
+
+/* Softmax per row: y = exp(x - max(x)) / sum(exp(x - max(x))).  A row that
+ * holds a NaN gives an all-NaN output row. */
+MT_API mt_status mt_softmax_f32(const float *x, float *y, int64_t rows,
+                         int64_t cols, mt_stream_t stream);
+MT_API mt_status mt_softmax_f32_with_plan(const float *x, float *y, int64_t rows,
+                                   int64_t cols, mt_stream_t stream,
+                                   const mt_plan_t *plan);
+
+/* Row sum: out[r] = sum of row r (rows outputs).  Accumulated with
+ * compensated (two-sum) FP32 arithmetic, so sums of small integers are
+ * exact and near-zero sums keep their relative accuracy. */
+MT_API mt_status mt_row_sum_f32(const float *x, float *out, int64_t rows,
+                         int64_t cols, mt_stream_t stream);
+MT_API mt_status mt_row_sum_f32_with_plan(const float *x, float *out, int64_t rows,
+                                   int64_t cols, mt_stream_t stream,
+                                   const mt_plan_t *plan);
+
+/* Cross-entropy per row: loss[r] = log(sum(exp(x_r))) - x_r[labels[r]]
+ * (computed with the row max subtracted).  labels holds rows int32 class
+ * indices; a label outside [0, cols) gives loss NaN for that row.  If
+ * mean_loss != NULL it receives sum(loss) / rows, summed in a fixed order by
+ * a second one-CTA kernel on the same stream (deterministic). */
+MT_API mt_status mt_cross_entropy_f32(const float *logits, const int32_t *labels,
+                               float *loss, float *mean_loss, int64_t rows,
+                               int64_t cols, mt_stream_t stream);
+MT_API mt_status mt_cross_entropy_f32_with_plan(const float *logits,
+                                         const int32_t *labels, float *loss,
+                                         float *mean_loss, int64_t rows,
+                                         int64_t cols, mt_stream_t stream,
+                                         const mt_plan_t *plan);
+
+/* ---- planning and introspection (host only; no CUDA call) ------------- */
+
+/* The plan the operators use for (op, rows, cols): a lookup in the table of
+ * measured winners, else the built-in heuristic.  grid is left 0 (resolved
+ * at launch from the device's SM count and occupancy).  Returns
+ * MT_ERR_INVALID_ARGUMENT for an unknown op, rows < 0 or cols < 1. */
+MT_API mt_status mt_plan_query(int op, int64_t rows, int64_t cols, mt_plan_t *out);
+
+/* Legality of a plan for (op, cols) without launching anything: MT_OK, or
+ * the error the *_with_plan call would return. */
+MT_API mt_status mt_plan_check(int op, int64_t cols, const mt_plan_t *plan);
+
+/* Private-slot bound of the consecutive-worker map: the most values any one
+ * of W workers owns in a row of n elements with V consecutive values per
+ * worker, floor(n/(W*V))*V + min(n % (W*V), V).  ("Consecutive-worker
+ * reduction layout checkpoint", §Implementation and semantics.)  Returns
+ * -1 for n < 0, W < 1 or V < 1. */
+MT_API int64_t mt_private_slot_bound(int64_t n, int32_t W, int32_t V);
+
+/* Writes a one-line description of `plan` into buf (at most n bytes,
+ * NUL-terminated when n > 0).  Returns the length the full text needs,
+ * excluding the NUL (snprintf convention). */
+MT_API size_t mt_describe_plan(const mt_plan_t *plan, char *buf, size_t n);
+
+/* Static string naming a status. */
+MT_API const char *mt_status_string(mt_status status);
+
+/* The cudaError_t behind the calling thread's last MT_ERR_CUDA (0 if
+ * none). */
+MT_API int mt_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MT_ROWREDUCE_H */

@@ -1,0 +1,303 @@
+"""ctypes binding of ``libmt_rowreduce.so`` (argument marshalling only).
+
+Every function named ``mt_*`` here calls the C function of the same name in
+``include/mt_rowreduce.h``.  Pointer arguments accept a CUDA ``torch.Tensor``
+(FP32 / int32, contiguous), a raw integer device address, or ``None`` for
+NULL; ``stream`` accepts a ``torch.cuda.Stream``, a raw handle, or ``None``
+for torch's current stream.  A status other than ``MT_OK`` raises
+:class:`MTError`.  All computation happens in the library's CUDA kernels;
+there is no fallback of any kind: if the library is not built, every call
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libmt_rowreduce.so")
+
+MT_OK = 0
+MT_ERR_INVALID_ARGUMENT = 1
+MT_ERR_UNSUPPORTED = 2
+MT_ERR_OUT_OF_RESOURCES = 3
+MT_ERR_CUDA = 4
+
+MT_OP_RMSNORM = 0
+MT_OP_LAYERNORM = 1
+MT_OP_RESIDUAL_LAYERNORM = 2
+MT_OP_SOFTMAX = 3
+MT_OP_ROW_SUM = 4
+MT_OP_CROSS_ENTROPY = 5
+OP_IDS = {"rmsnorm": 0, "layernorm": 1, "residual_layernorm": 2,
+          "softmax": 3, "row_sum": 4, "cross_entropy": 5}
+
+MT_PATH_REGISTERS = 0
+MT_PATH_LOOP = 1
+
+# Symbols declared in include/mt_rowreduce.h.
+EXPORTS = (
+    "mt_rmsnorm_f32", "mt_rmsnorm_f32_with_plan",
+    "mt_layernorm_f32", "mt_layernorm_f32_with_plan",
+    "mt_residual_layernorm_f32", "mt_residual_layernorm_f32_with_plan",
+    "mt_softmax_f32", "mt_softmax_f32_with_plan",
+    "mt_row_sum_f32", "mt_row_sum_f32_with_plan",
+    "mt_cross_entropy_f32", "mt_cross_entropy_f32_with_plan",
+    "mt_plan_query", "mt_plan_check", "mt_private_slot_bound",
+    "mt_describe_plan", "mt_status_string", "mt_last_cuda_error",
+)
+
+
+class MtPlan(ctypes.Structure):
+    """``mt_plan_t``."""
+    _fields_ = [("threads_per_row", ctypes.c_int32),
+                ("values_per_thread", ctypes.c_int32),
+                ("chunks", ctypes.c_int32),
+                ("rows_per_block", ctypes.c_int32),
+                ("path", ctypes.c_int32),
+                ("grid", ctypes.c_int32)]
+
+    def as_dict(self) -> dict:
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+    def __repr__(self):
+        return f"MtPlan({self.as_dict()})"
+
+
+def make_plan(W, V, chunks=0, rows_per_block=1, path=MT_PATH_REGISTERS,
+              grid=0) -> MtPlan:
+    return MtPlan(W, V, chunks, rows_per_block, path, grid)
+
+
+class MTError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = f"{where}: {status_string(status)}"
+        if status == MT_ERR_CUDA:
+            msg += f" (cudaError {lib().mt_last_cuda_error()})"
+        super().__init__(msg)
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"CUDA library {LIB_PATH} is not built; run "
+                    "row_reduction_gb300.build.build() (or "
+                    "__graft_entry__.build()) first")
+            L = ctypes.CDLL(LIB_PATH)
+            P, I64, I32, F = (ctypes.c_void_p, ctypes.c_int64,
+                              ctypes.c_int32, ctypes.c_float)
+            PP = ctypes.POINTER(MtPlan)
+            st = ctypes.c_int
+            sig = {
+                "mt_rmsnorm_f32": [P, P, P, I64, I64, F, P],
+                "mt_rmsnorm_f32_with_plan": [P, P, P, I64, I64, F, P, PP],
+                "mt_layernorm_f32": [P, P, P, P, I64, I64, F, P],
+                "mt_layernorm_f32_with_plan": [P, P, P, P, I64, I64, F, P,
+                                               PP],
+                "mt_residual_layernorm_f32": [P, P, P, P, P, P, I64, I64, F,
+                                              P],
+                "mt_residual_layernorm_f32_with_plan": [P, P, P, P, P, P, I64,
+                                                        I64, F, P, PP],
+                "mt_softmax_f32": [P, P, I64, I64, P],
+                "mt_softmax_f32_with_plan": [P, P, I64, I64, P, PP],
+                "mt_row_sum_f32": [P, P, I64, I64, P],
+                "mt_row_sum_f32_with_plan": [P, P, I64, I64, P, PP],
+                "mt_cross_entropy_f32": [P, P, P, P, I64, I64, P],
+                "mt_cross_entropy_f32_with_plan": [P, P, P, P, I64, I64, P,
+                                                   PP],
+                "mt_plan_query": [ctypes.c_int, I64, I64, PP],
+                "mt_plan_check": [ctypes.c_int, I64, PP],
+            }
+            for name, args in sig.items():
+                fn = getattr(L, name)
+                fn.argtypes = args
+                fn.restype = st
+            L.mt_private_slot_bound.argtypes = [I64, I32, I32]
+            L.mt_private_slot_bound.restype = I64
+            L.mt_describe_plan.argtypes = [PP, ctypes.c_char_p,
+                                           ctypes.c_size_t]
+            L.mt_describe_plan.restype = ctypes.c_size_t
+            L.mt_status_string.argtypes = [ctypes.c_int]
+            L.mt_status_string.restype = ctypes.c_char_p
+            L.mt_last_cuda_error.argtypes = []
+            L.mt_last_cuda_error.restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+# ---- marshalling ------------------------------------------------------------
+def _ptr(t, name, dtype="float32"):
+    """Device address of a tensor (checked), a raw int, or None."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a CUDA tensor, int or None")
+    want = torch.float32 if dtype == "float32" else torch.int32
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != want:
+        raise TypeError(f"{name} must be {want}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _plan(p):
+    if p is None:
+        return None
+    if isinstance(p, MtPlan):
+        return ctypes.byref(p)
+    if isinstance(p, dict):
+        return ctypes.byref(MtPlan(**p))
+    raise TypeError("plan must be an MtPlan, a dict or None")
+
+
+def _check(st, where):
+    if st != MT_OK:
+        raise MTError(st, where)
+
+
+# ---- the C ABI, one function per entry point ---------------------------------
+def mt_rmsnorm_f32(x, weight, y, rows, cols, eps, stream=None):
+    _check(lib().mt_rmsnorm_f32(_ptr(x, "x"), _ptr(weight, "weight"),
+                                _ptr(y, "y"), rows, cols, eps,
+                                _stream(stream)), "mt_rmsnorm_f32")
+
+
+def mt_rmsnorm_f32_with_plan(x, weight, y, rows, cols, eps, stream=None,
+                             plan=None):
+    _check(lib().mt_rmsnorm_f32_with_plan(
+        _ptr(x, "x"), _ptr(weight, "weight"), _ptr(y, "y"), rows, cols, eps,
+        _stream(stream), _plan(plan)), "mt_rmsnorm_f32_with_plan")
+
+
+def mt_layernorm_f32(x, gamma, beta, y, rows, cols, eps, stream=None):
+    _check(lib().mt_layernorm_f32(_ptr(x, "x"), _ptr(gamma, "gamma"),
+                                  _ptr(beta, "beta"), _ptr(y, "y"), rows,
+                                  cols, eps, _stream(stream)),
+           "mt_layernorm_f32")
+
+
+def mt_layernorm_f32_with_plan(x, gamma, beta, y, rows, cols, eps,
+                               stream=None, plan=None):
+    _check(lib().mt_layernorm_f32_with_plan(
+        _ptr(x, "x"), _ptr(gamma, "gamma"), _ptr(beta, "beta"), _ptr(y, "y"),
+        rows, cols, eps, _stream(stream), _plan(plan)),
+        "mt_layernorm_f32_with_plan")
+
+
+def mt_residual_layernorm_f32(x, residual, gamma, beta, y, h_out, rows, cols,
+                              eps, stream=None):
+    _check(lib().mt_residual_layernorm_f32(
+        _ptr(x, "x"), _ptr(residual, "residual"), _ptr(gamma, "gamma"),
+        _ptr(beta, "beta"), _ptr(y, "y"), _ptr(h_out, "h_out"), rows, cols,
+        eps, _stream(stream)), "mt_residual_layernorm_f32")
+
+
+def mt_residual_layernorm_f32_with_plan(x, residual, gamma, beta, y, h_out,
+                                        rows, cols, eps, stream=None,
+                                        plan=None):
+    _check(lib().mt_residual_layernorm_f32_with_plan(
+        _ptr(x, "x"), _ptr(residual, "residual"), _ptr(gamma, "gamma"),
+        _ptr(beta, "beta"), _ptr(y, "y"), _ptr(h_out, "h_out"), rows, cols,
+        eps, _stream(stream), _plan(plan)),
+        "mt_residual_layernorm_f32_with_plan")
+
+
+def mt_softmax_f32(x, y, rows, cols, stream=None):
+    _check(lib().mt_softmax_f32(_ptr(x, "x"), _ptr(y, "y"), rows, cols,
+                                _stream(stream)), "mt_softmax_f32")
+
+
+def mt_softmax_f32_with_plan(x, y, rows, cols, stream=None, plan=None):
+    _check(lib().mt_softmax_f32_with_plan(_ptr(x, "x"), _ptr(y, "y"), rows,
+                                          cols, _stream(stream), _plan(plan)),
+           "mt_softmax_f32_with_plan")
+
+
+def mt_row_sum_f32(x, out, rows, cols, stream=None):
+    _check(lib().mt_row_sum_f32(_ptr(x, "x"), _ptr(out, "out"), rows, cols,
+                                _stream(stream)), "mt_row_sum_f32")
+
+
+def mt_row_sum_f32_with_plan(x, out, rows, cols, stream=None, plan=None):
+    _check(lib().mt_row_sum_f32_with_plan(_ptr(x, "x"), _ptr(out, "out"),
+                                          rows, cols, _stream(stream),
+                                          _plan(plan)),
+           "mt_row_sum_f32_with_plan")
+
+
+def mt_cross_entropy_f32(logits, labels, loss, mean_loss, rows, cols,
+                         stream=None):
+    _check(lib().mt_cross_entropy_f32(
+        _ptr(logits, "logits"), _ptr(labels, "labels", "int32"),
+        _ptr(loss, "loss"), _ptr(mean_loss, "mean_loss"), rows, cols,
+        _stream(stream)), "mt_cross_entropy_f32")
+
+
+def mt_cross_entropy_f32_with_plan(logits, labels, loss, mean_loss, rows,
+                                   cols, stream=None, plan=None):
+    _check(lib().mt_cross_entropy_f32_with_plan(
+        _ptr(logits, "logits"), _ptr(labels, "labels", "int32"),
+        _ptr(loss, "loss"), _ptr(mean_loss, "mean_loss"), rows, cols,
+        _stream(stream), _plan(plan)), "mt_cross_entropy_f32_with_plan")
+
+
+def mt_plan_query(op, rows, cols) -> MtPlan:
+    op = OP_IDS.get(op, op)
+    p = MtPlan()
+    _check(lib().mt_plan_query(op, rows, cols, ctypes.byref(p)),
+           "mt_plan_query")
+    return p
+
+
+def mt_plan_check(op, cols, plan) -> int:
+    """Status the *_with_plan call would return for this plan (no raise)."""
+    op = OP_IDS.get(op, op)
+    return lib().mt_plan_check(op, cols, _plan(plan))
+
+
+def mt_private_slot_bound(n, W, V) -> int:
+    return lib().mt_private_slot_bound(n, W, V)
+
+
+def mt_describe_plan(plan) -> str:
+    need = lib().mt_describe_plan(_plan(plan), None, 0)
+    buf = ctypes.create_string_buffer(need + 1)
+    lib().mt_describe_plan(_plan(plan), buf, need + 1)
+    return buf.value.decode()
+
+
+def status_string(st) -> str:
+    return lib().mt_status_string(st).decode()
+
+
+mt_status_string = status_string
+
+
+def mt_last_cuda_error() -> int:
+    return lib().mt_last_cuda_error()

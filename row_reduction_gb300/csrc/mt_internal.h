@@ -1,0 +1,79 @@
+// mt_internal.h -- types shared by the C-ABI layer, the planner and the
+// kernel translation units.  Not part of the public interface.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/mt_rowreduce.h"
+
+namespace mt {
+
+enum : int {
+    OP_RMSNORM = MT_OP_RMSNORM,
+    OP_LAYERNORM = MT_OP_LAYERNORM,
+    OP_RESIDUAL_LAYERNORM = MT_OP_RESIDUAL_LAYERNORM,
+    OP_SOFTMAX = MT_OP_SOFTMAX,
+    OP_ROW_SUM = MT_OP_ROW_SUM,
+    OP_CROSS_ENTROPY = MT_OP_CROSS_ENTROPY,
+    OP_COUNT = 6
+};
+
+// Kernel arguments; one struct for all operators (unused fields are NULL).
+struct KArgs {
+    const float *x;        // input matrix (logits for cross-entropy)
+    const float *res;      // residual (residual LayerNorm)
+    const float *w;        // RMSNorm weight / LayerNorm gamma (NULL = 1)
+    const float *b;        // LayerNorm beta (NULL = 0)
+    float *y;              // output matrix
+    float *h;              // residual LayerNorm h_out (NULL = not written)
+    float *out;            // per-row output (row sum, cross-entropy loss)
+    const int32_t *labels; // cross-entropy labels
+    int64_t rows;
+    int32_t cols;
+    int32_t W;             // threads per row (power of two)
+    int32_t log2W;
+    int32_t B;             // rows per CTA
+    float eps;
+    // Unaligned mode only: 1 when the pointer keeps x's 16-byte phase, so
+    // its row body can use vector accesses too.
+    int32_t y_vec, h_vec, r_vec;
+};
+
+// Instantiated register-path chunk counts.
+constexpr int kChunkSet[] = {1, 2, 4, 8, 16};
+constexpr int kNumChunkSet = 5;
+
+// Largest CTA the register-path kernel with V*K values per thread is
+// compiled for (its __launch_bounds__): 64 registers per thread at 1024
+// threads leaves room for 16 values; 128 at 512 for 32; 255 at 256 for 64.
+constexpr int reg_max_threads(int vk) {
+    return vk <= 16 ? 1024 : (vk <= 32 ? 512 : 256);
+}
+constexpr int kLoopMaxThreads = 512;
+
+// Per-operator launchers, one translation unit each.  `aligned` selects the
+// kernels whose every access of the row body is a V-wide vector access
+// without a head; `grid` is already resolved (> 0).
+#define MT_DECLARE_LAUNCHER(name)                                            \
+    cudaError_t name(const mt_plan_t &plan, const KArgs &a, bool aligned,    \
+                     cudaStream_t stream, int *max_threads_out);             \
+    cudaError_t name##_occupancy(const mt_plan_t &plan, bool aligned,        \
+                                 int *blocks_per_sm);
+MT_DECLARE_LAUNCHER(launch_rmsnorm)
+MT_DECLARE_LAUNCHER(launch_layernorm)
+MT_DECLARE_LAUNCHER(launch_residual_layernorm)
+MT_DECLARE_LAUNCHER(launch_softmax)
+MT_DECLARE_LAUNCHER(launch_row_sum)
+MT_DECLARE_LAUNCHER(launch_cross_entropy)
+#undef MT_DECLARE_LAUNCHER
+
+// One-CTA fixed-order mean of `rows` per-row losses.
+cudaError_t launch_mean(const float *loss, float *mean, int64_t rows,
+                        cudaStream_t stream);
+
+// Planner (planner.cpp).
+mt_status plan_lookup(int op, int64_t rows, int64_t cols, mt_plan_t *out);
+mt_status plan_check(int op, int64_t cols, const mt_plan_t &p);
+
+}  // namespace mt

@@ -1,0 +1,854 @@
+// mt_kernels.cuh -- the per-row reduction kernels (sm_103a).
+//
+// Work mapping ("Consecutive-worker reduction layout checkpoint",
+// §Implementation and semantics): a row is served by W consecutive threads
+// ("workers"); worker w owns, in chunk k, the V consecutive elements
+//     i = (k*W + w)*V + e,   0 <= e < V,
+// of the row body, so a warp's V=4 accesses of one chunk are 16-byte vectors
+// covering 512 contiguous bytes.  Complete packs take unguarded vector
+// accesses; only the last, partial pack is guarded element by element.
+//
+// Alignment.  CUDA vector accesses must be naturally aligned.  When every
+// row starts on a 4V-byte boundary (the "aligned" kernels: cols % V == 0 and
+// aligned base pointers) the body is the whole row.  Otherwise each row first
+// peels a head of hd = (-row_address/4) mod V scalar elements, owned one each
+// by workers 0..hd-1, and the map above applies to the rest.
+//
+// Reduction ("Thread Ownership and Software Staging", §Register-tiled
+// reductions): each thread combines its own slots, then the W lanes of a row
+// combine with xor shuffles; for W > 32 each warp's lane 0 publishes one
+// partial to shared memory, one __syncthreads() publishes them, and every
+// warp reads all of its row's partials and finishes the reduction itself --
+// no second barrier and no broadcast.  Consecutive reductions alternate
+// between two scratch buffers, so the next reduction's barrier is what keeps
+// a buffer from being overwritten before every warp has read it.
+//
+// Register path: the whole row (V*K values per thread) is loaded once,
+// before any arithmetic, and the output is written from registers (the
+// rmsnorm_register idea: "retains its input values across the reduction").
+// Loop path: rows wider than the register budget are streamed in a strided
+// loop; the normalising operators re-read x (from L2) to write y.
+//
+// Blocks hold B = blockDim / W row groups and loop over row groups with a
+// grid stride, so a grid of "resident CTAs" is persistent.  All threads of
+// a block run the same number of loop iterations (rows past the end are
+// inactive but still take part in every shuffle and barrier).
+#pragma once
+
+#include <math.h>
+#include <stdint.h>
+
+#include "mt_internal.h"
+
+namespace mt {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// NaN-propagating max (fmaxf would drop a NaN).
+__device__ __forceinline__ float nanmax(float a, float b) {
+    return (a > b || a != a) ? a : b;
+}
+
+// Error-free transformation of a + b (Knuth's two-sum): s + err == a + b
+// exactly.  Used for the compensated row sum.
+__device__ __forceinline__ void two_sum(float a, float b, float &s,
+                                        float &err) {
+    s = __fadd_rn(a, b);
+    const float bp = __fsub_rn(s, a);
+    const float ap = __fsub_rn(s, bp);
+    err = __fadd_rn(__fsub_rn(a, ap), __fsub_rn(b, bp));
+}
+
+// ---- vector access -------------------------------------------------------
+template <int V>
+__device__ __forceinline__ void ld_vec(const float *p, float *d) {
+    if constexpr (V == 4) {
+        const float4 t = *reinterpret_cast<const float4 *>(p);
+        d[0] = t.x; d[1] = t.y; d[2] = t.z; d[3] = t.w;
+    } else if constexpr (V == 2) {
+        const float2 t = *reinterpret_cast<const float2 *>(p);
+        d[0] = t.x; d[1] = t.y;
+    } else {
+        d[0] = *p;
+    }
+}
+
+// Read-only parameter vectors (weight, gamma, beta): never written by the
+// kernel, so the read-only data path is safe.
+template <int V>
+__device__ __forceinline__ void ldg_vec(const float *p, float *d) {
+    if constexpr (V == 4) {
+        const float4 t = __ldg(reinterpret_cast<const float4 *>(p));
+        d[0] = t.x; d[1] = t.y; d[2] = t.z; d[3] = t.w;
+    } else if constexpr (V == 2) {
+        const float2 t = __ldg(reinterpret_cast<const float2 *>(p));
+        d[0] = t.x; d[1] = t.y;
+    } else {
+        d[0] = __ldg(p);
+    }
+}
+
+template <int V>
+__device__ __forceinline__ void st_vec(float *p, const float *d) {
+    if constexpr (V == 4) {
+        *reinterpret_cast<float4 *>(p) = make_float4(d[0], d[1], d[2], d[3]);
+    } else if constexpr (V == 2) {
+        *reinterpret_cast<float2 *>(p) = make_float2(d[0], d[1]);
+    } else {
+        *p = d[0];
+    }
+}
+
+// Up to V values of a parameter vector starting at column `col`; only the
+// first `nv` exist (the rest, and every value of a NULL vector, read as
+// `dflt`).  `vec` says the address is 4V-byte aligned.
+template <int V>
+__device__ __forceinline__ void param_pack(const float *p, int col, int nv,
+                                           bool vec, float dflt, float *d) {
+    if (p == nullptr || nv <= 0) {
+#pragma unroll
+        for (int e = 0; e < V; ++e) d[e] = dflt;
+    } else if (vec && nv == V) {
+        ldg_vec<V>(p + col, d);
+    } else {
+#pragma unroll
+        for (int e = 0; e < V; ++e) d[e] = e < nv ? __ldg(p + col + e) : dflt;
+    }
+}
+
+// ---- cooperative reductions ---------------------------------------------
+struct SumOp {
+    __device__ __forceinline__ float operator()(float a, float b) const {
+        return a + b;
+    }
+    static __device__ __forceinline__ float ident() { return 0.f; }
+};
+struct MaxOp {
+    __device__ __forceinline__ float operator()(float a, float b) const {
+        return nanmax(a, b);
+    }
+    static __device__ __forceinline__ float ident() { return -INFINITY; }
+};
+
+struct RedScratch {
+    float buf[2][2][32];  // [alternating buffer][component][warp]
+};
+
+// All-reduce of one value over the W threads of each row; every thread of
+// the row returns the same bits.
+template <class Op>
+__device__ __forceinline__ float row_allreduce(float v, int W,
+                                               RedScratch &red,
+                                               int &parity) {
+    Op op;
+    if (W <= 32) {
+        for (int off = W >> 1; off > 0; off >>= 1)
+            v = op(v, __shfl_xor_sync(kFull, v, off));
+        return v;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        v = op(v, __shfl_xor_sync(kFull, v, off));
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int nw = W >> 5;
+    float *buf = red.buf[parity][0];
+    parity ^= 1;
+    if (lane == 0) buf[warp] = v;
+    __syncthreads();
+    const int first = warp & ~(nw - 1);
+    float t = lane < nw ? buf[first + lane] : Op::ident();
+    for (int off = nw >> 1; off > 0; off >>= 1)
+        t = op(t, __shfl_xor_sync(kFull, t, off));
+    return __shfl_sync(kFull, t, 0);
+}
+
+// Compensated (sum, error) pairs: (s1,c1)+(s2,c2) = two_sum(s1,s2) with the
+// rounding error folded into the compensation term.
+__device__ __forceinline__ void pair_add(float &s, float &c, float s2,
+                                         float c2) {
+    float t, e;
+    two_sum(s, s2, t, e);
+    s = t;
+    c = c + c2 + e;
+}
+
+__device__ __forceinline__ void row_allreduce_compensated(float &s, float &c,
+                                                          int W,
+                                                          RedScratch &red,
+                                                          int &parity) {
+    if (W <= 32) {
+        for (int off = W >> 1; off > 0; off >>= 1) {
+            const float s2 = __shfl_xor_sync(kFull, s, off);
+            const float c2 = __shfl_xor_sync(kFull, c, off);
+            pair_add(s, c, s2, c2);
+        }
+        return;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float s2 = __shfl_xor_sync(kFull, s, off);
+        const float c2 = __shfl_xor_sync(kFull, c, off);
+        pair_add(s, c, s2, c2);
+    }
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int nw = W >> 5;
+    float(*buf)[32] = red.buf[parity];
+    parity ^= 1;
+    if (lane == 0) {
+        buf[0][warp] = s;
+        buf[1][warp] = c;
+    }
+    __syncthreads();
+    const int first = warp & ~(nw - 1);
+    float ts = lane < nw ? buf[0][first + lane] : 0.f;
+    float tc = lane < nw ? buf[1][first + lane] : 0.f;
+    for (int off = nw >> 1; off > 0; off >>= 1) {
+        const float s2 = __shfl_xor_sync(kFull, ts, off);
+        const float c2 = __shfl_xor_sync(kFull, tc, off);
+        pair_add(ts, tc, s2, c2);
+    }
+    s = __shfl_sync(kFull, ts, 0);
+    c = __shfl_sync(kFull, tc, 0);
+}
+
+// Online (max, sum of exp(x - max)) pairs for softmax / cross-entropy on the
+// loop path: (m1,s1) + (m2,s2) = (m, s1*e^(m1-m) + s2*e^(m2-m)).
+// `self_first` fixes the operand order of the final fused multiply-add, so
+// the two lanes of a shuffle pair compute the same bits.
+__device__ __forceinline__ void lse_merge(float &m, float &s, float m2,
+                                          float s2, bool self_first = true) {
+    const float mm = nanmax(m, m2);
+    const float f1 = (m == mm) ? 1.f : expf(m - mm);
+    const float f2 = (m2 == mm) ? 1.f : expf(m2 - mm);
+    s = self_first ? fmaf(s, f1, s2 * f2) : fmaf(s2, f2, s * f1);
+    m = mm;
+}
+
+__device__ __forceinline__ void row_allreduce_lse(float &m, float &s, int W,
+                                                  RedScratch &red,
+                                                  int &parity) {
+    const int lane = threadIdx.x & 31;
+    if (W <= 32) {
+        for (int off = W >> 1; off > 0; off >>= 1) {
+            const float m2 = __shfl_xor_sync(kFull, m, off);
+            const float s2 = __shfl_xor_sync(kFull, s, off);
+            lse_merge(m, s, m2, s2, (lane & off) == 0);
+        }
+        return;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float m2 = __shfl_xor_sync(kFull, m, off);
+        const float s2 = __shfl_xor_sync(kFull, s, off);
+        lse_merge(m, s, m2, s2, (lane & off) == 0);
+    }
+    const int warp = threadIdx.x >> 5;
+    const int nw = W >> 5;
+    float(*buf)[32] = red.buf[parity];
+    parity ^= 1;
+    if (lane == 0) {
+        buf[0][warp] = m;
+        buf[1][warp] = s;
+    }
+    __syncthreads();
+    const int first = warp & ~(nw - 1);
+    float tm = lane < nw ? buf[0][first + lane] : -INFINITY;
+    float ts = lane < nw ? buf[1][first + lane] : 0.f;
+    for (int off = nw >> 1; off > 0; off >>= 1) {
+        const float m2 = __shfl_xor_sync(kFull, tm, off);
+        const float s2 = __shfl_xor_sync(kFull, ts, off);
+        lse_merge(tm, ts, m2, s2, (lane & off) == 0);
+    }
+    m = __shfl_sync(kFull, tm, 0);
+    s = __shfl_sync(kFull, ts, 0);
+}
+
+// ---- per-row geometry ------------------------------------------------------
+template <int V, bool AL>
+struct RowGeom {
+    int64_t base;  // element offset of the row
+    int hd;        // head length (unaligned kernels only)
+    int nb;        // body length
+    __device__ __forceinline__ RowGeom(const float *x, int64_t row,
+                                       int cols) {
+        base = row * (int64_t)cols;
+        hd = 0;
+        if constexpr (!AL && V > 1) {
+            const unsigned words =
+                (unsigned)(reinterpret_cast<uintptr_t>(x + base) >> 2);
+            hd = (int)((0u - words) & (unsigned)(V - 1));
+            hd = hd < cols ? hd : cols;
+        }
+        nb = cols - hd;
+    }
+};
+
+// Loads V consecutive values at body offset `off` of a row (`p` = row
+// start + head): a vector access for a complete pack when `vec`, otherwise
+// guarded scalars; missing values read as `fill`.
+template <int V>
+__device__ __forceinline__ void load_pack(const float *p, int off, int nb,
+                                          bool active, bool vec, float fill,
+                                          float *d) {
+    if (active && off + V <= nb) {
+        if (vec) {
+            ld_vec<V>(p + off, d);
+        } else {
+#pragma unroll
+            for (int e = 0; e < V; ++e) d[e] = p[off + e];
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < V; ++e)
+            d[e] = (active && off + e < nb) ? p[off + e] : fill;
+    }
+}
+
+template <int V>
+__device__ __forceinline__ void store_pack(float *p, int off, int nb,
+                                           bool active, bool vec,
+                                           const float *d) {
+    if (!active) return;
+    if (off + V <= nb) {
+        if (vec) {
+            st_vec<V>(p + off, d);
+        } else {
+#pragma unroll
+            for (int e = 0; e < V; ++e) p[off + e] = d[e];
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < V; ++e)
+            if (off + e < nb) p[off + e] = d[e];
+    }
+}
+
+// =========================================================================
+// Register path
+// =========================================================================
+template <int OP, int V, int K, bool AL>
+__global__ void __launch_bounds__(reg_max_threads(V * K))
+    reg_kernel(const KArgs a) {
+    __shared__ RedScratch red;
+    int parity = 0;
+    const int W = a.W;
+    const int worker = threadIdx.x & (W - 1);
+    const int slot = threadIdx.x >> a.log2W;
+    const int cols = a.cols;
+    const int64_t ngroups = (a.rows + a.B - 1) / a.B;
+    constexpr bool kMaxFill = (OP == OP_SOFTMAX || OP == OP_CROSS_ENTROPY);
+    const float fill = kMaxFill ? -INFINITY : 0.f;
+    constexpr bool kHead = !AL && V > 1;
+    const bool yvec = AL || a.y_vec;
+
+    for (int64_t g = blockIdx.x; g < ngroups; g += gridDim.x) {
+        const int64_t row = g * a.B + slot;
+        const bool active = row < a.rows;
+        const RowGeom<V, AL> geo(a.x, active ? row : 0, cols);
+        const float *xb = a.x + geo.base + geo.hd;  // body start
+        const int nb = geo.nb;
+        const bool head = kHead && active && worker < geo.hd;
+
+        // ---- single read of the row into registers --------------------
+        float v[K][V];
+        float hv = fill;
+#pragma unroll
+        for (int k = 0; k < K; ++k)
+            load_pack<V>(xb, (k * W + worker) * V, nb, active, true, fill,
+                         v[k]);
+        if (head) hv = a.x[geo.base + worker];
+
+        if constexpr (OP == OP_RESIDUAL_LAYERNORM) {
+            const float *rb = a.res + geo.base + geo.hd;
+            const bool rvec = AL || a.r_vec;
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                float t[V];
+                load_pack<V>(rb, (k * W + worker) * V, nb, active, rvec, 0.f,
+                             t);
+#pragma unroll
+                for (int e = 0; e < V; ++e) v[k][e] = __fadd_rn(v[k][e], t[e]);
+            }
+            if (head) hv = __fadd_rn(hv, a.res[geo.base + worker]);
+            if (a.h != nullptr) {
+                float *hb = a.h + geo.base + geo.hd;
+                const bool hvec = AL || a.h_vec;
+#pragma unroll
+                for (int k = 0; k < K; ++k)
+                    store_pack<V>(hb, (k * W + worker) * V, nb, active, hvec,
+                                  v[k]);
+                if (head) a.h[geo.base + worker] = hv;
+            }
+        }
+
+        // Cross-entropy: fetch the label and its logit while the row loads
+        // are in flight.
+        float xl = 0.f;
+        if constexpr (OP == OP_CROSS_ENTROPY) {
+            if (active && worker == 0) {
+                const int32_t lab = __ldg(a.labels + row);
+                xl = (lab >= 0 && lab < cols) ? a.x[geo.base + lab] : NAN;
+            }
+        }
+
+        // ---- per-operator reduction and epilogue ----------------------
+        if constexpr (OP == OP_RMSNORM) {
+            float acc[V];
+#pragma unroll
+            for (int e = 0; e < V; ++e) acc[e] = 0.f;
+#pragma unroll
+            for (int k = 0; k < K; ++k)
+#pragma unroll
+                for (int e = 0; e < V; ++e) acc[e] = fmaf(v[k][e], v[k][e], acc[e]);
+            float ss = hv * hv;
+#pragma unroll
+            for (int e = 0; e < V; ++e) ss += acc[e];
+            ss = row_allreduce<SumOp>(ss, W, red, parity);
+            const float r = rsqrtf(ss / (float)cols + a.eps);
+            float *yb = a.y + geo.base + geo.hd;
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                const int off = (k * W + worker) * V;
+                float wv[V], o[V];
+                const int nv = active ? min(max(nb - off, 0), V) : 0;
+                param_pack<V>(a.w, geo.hd + off, nv, AL, 1.f, wv);
+#pragma unroll
+                for (int e = 0; e < V; ++e) o[e] = v[k][e] * r * wv[e];
+                store_pack<V>(yb, off, nb, active, yvec, o);
+            }
+            if (head) {
+                const float wh = a.w ? __ldg(a.w + worker) : 1.f;
+                a.y[geo.base + worker] = hv * r * wh;
+            }
+        } else if constexpr (OP == OP_LAYERNORM ||
+                             OP == OP_RESIDUAL_LAYERNORM) {
+            float acc[V];
+#pragma unroll
+            for (int e = 0; e < V; ++e) acc[e] = 0.f;
+#pragma unroll
+            for (int k = 0; k < K; ++k)
+#pragma unroll
+                for (int e = 0; e < V; ++e) acc[e] += v[k][e];
+            float s = hv;
+#pragma unroll
+            for (int e = 0; e < V; ++e) s += acc[e];
+            s = row_allreduce<SumOp>(s, W, red, parity);
+            const float mean = s / (float)cols;
+#pragma unroll
+            for (int e = 0; e < V; ++e) acc[e] = 0.f;
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                const int off = (k * W + worker) * V;
+#pragma unroll
+                for (int e = 0; e < V; ++e) {
+                    const float d = v[k][e] - mean;
+                    if (active && off + e < nb) acc[e] = fmaf(d, d, acc[e]);
+                }
+            }
+            float q = 0.f;
+            if (head) {
+                const float d = hv - mean;
+                q = d * d;
+            }
+#pragma unroll
+            for (int e = 0; e < V; ++e) q += acc[e];
+            q = row_allreduce<SumOp>(q, W, red, parity);
+            const float rstd = rsqrtf(q / (float)cols + a.eps);
+            float *yb = a.y + geo.base + geo.hd;
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                const int off = (k * W + worker) * V;
+                float gv[V], bv[V], o[V];
+                const int nv = active ? min(max(nb - off, 0), V) : 0;
+                param_pack<V>(a.w, geo.hd + off, nv, AL, 1.f, gv);
+                param_pack<V>(a.b, geo.hd + off, nv, AL, 0.f, bv);
+#pragma unroll
+                for (int e = 0; e < V; ++e)
+                    o[e] = fmaf((v[k][e] - mean) * rstd, gv[e], bv[e]);
+                store_pack<V>(yb, off, nb, active, yvec, o);
+            }
+            if (head) {
+                const float gh = a.w ? __ldg(a.w + worker) : 1.f;
+                const float bh = a.b ? __ldg(a.b + worker) : 0.f;
+                a.y[geo.base + worker] = fmaf((hv - mean) * rstd, gh, bh);
+            }
+        } else if constexpr (OP == OP_SOFTMAX) {
+            float mx[V];
+#pragma unroll
+            for (int e = 0; e < V; ++e) mx[e] = hv;
+#pragma unroll
+            for (int k = 0; k < K; ++k)
+#pragma unroll
+                for (int e = 0; e < V; ++e) mx[e] = nanmax(mx[e], v[k][e]);
+            float m = mx[0];
+#pragma unroll
+            for (int e = 1; e < V; ++e) m = nanmax(m, mx[e]);
+            m = row_allreduce<MaxOp>(m, W, red, parity);
+            float acc[V];
+#pragma unroll
+            for (int e = 0; e < V; ++e) acc[e] = 0.f;
+#pragma unroll
+            for (int k = 0; k < K; ++k)
+#pragma unroll
+                for (int e = 0; e < V; ++e) {
+                    v[k][e] = expf(v[k][e] - m);
+                    acc[e] += v[k][e];
+                }
+            float s = 0.f;
+            if (head) {
+                hv = expf(hv - m);
+                s = hv;
+            }
+#pragma unroll
+            for (int e = 0; e < V; ++e) s += acc[e];
+            s = row_allreduce<SumOp>(s, W, red, parity);
+            const float inv = 1.f / s;
+            float *yb = a.y + geo.base + geo.hd;
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                float o[V];
+#pragma unroll
+                for (int e = 0; e < V; ++e) o[e] = v[k][e] * inv;
+                store_pack<V>(yb, (k * W + worker) * V, nb, active, yvec, o);
+            }
+            if (head) a.y[geo.base + worker] = hv * inv;
+        } else if constexpr (OP == OP_ROW_SUM) {
+            float s = hv, c = 0.f;
+#pragma unroll
+            for (int k = 0; k < K; ++k)
+#pragma unroll
+                for (int e = 0; e < V; ++e) {
+                    float t, err;
+                    two_sum(s, v[k][e], t, err);
+                    s = t;
+                    c += err;
+                }
+            row_allreduce_compensated(s, c, W, red, parity);
+            if (active && worker == 0) a.out[row] = s + c;
+        } else if constexpr (OP == OP_CROSS_ENTROPY) {
+            float mx[V];
+#pragma unroll
+            for (int e = 0; e < V; ++e) mx[e] = hv;
+#pragma unroll
+            for (int k = 0; k < K; ++k)
+#pragma unroll
+                for (int e = 0; e < V; ++e) mx[e] = nanmax(mx[e], v[k][e]);
+            float m = mx[0];
+#pragma unroll
+            for (int e = 1; e < V; ++e) m = nanmax(m, mx[e]);
+            m = row_allreduce<MaxOp>(m, W, red, parity);
+            float acc[V];
+#pragma unroll
+            for (int e = 0; e < V; ++e) acc[e] = 0.f;
+#pragma unroll
+            for (int k = 0; k < K; ++k)
+#pragma unroll
+                for (int e = 0; e < V; ++e) acc[e] += expf(v[k][e] - m);
+            float s = head ? expf(hv - m) : 0.f;
+#pragma unroll
+            for (int e = 0; e < V; ++e) s += acc[e];
+            s = row_allreduce<SumOp>(s, W, red, parity);
+            if (active && worker == 0) a.out[row] = (m + logf(s)) - xl;
+        }
+    }
+}
+
+// =========================================================================
+// Loop path (rows wider than the register budget)
+// =========================================================================
+// Calls f(vals, nvalid, off) for every pack of the thread's part of the row
+// body, U packs' loads in flight at a time; then the head element, if any,
+// as f(&hv, 1, -1 - worker) (off < 0 marks the head: column = -1 - off).
+template <int V, bool AL, int U, class LoadF, class F>
+__device__ __forceinline__ void stream_row(int worker, int W, int hd, int nb,
+                                           bool active, LoadF load, F f) {
+    if (!active) return;
+    int64_t p = worker;
+    const int64_t step = (int64_t)U * W;
+    for (; (p + (int64_t)(U - 1) * W + 1) * V <= nb; p += step) {
+        float t[U][V];
+#pragma unroll
+        for (int u = 0; u < U; ++u) load((int)((p + u * W) * V), V, t[u]);
+#pragma unroll
+        for (int u = 0; u < U; ++u) f(t[u], V, (int)((p + u * W) * V));
+    }
+    for (; p * V < nb; p += W) {
+        const int off = (int)(p * V);
+        const int nv = nb - off < V ? nb - off : V;
+        float t[V];
+        load(off, nv, t);
+        f(t, nv, off);
+    }
+    if constexpr (!AL && V > 1) {
+        if (worker < hd) {
+            float t[V];
+            load(-1 - worker, 1, t);
+            f(t, 1, -1 - worker);
+        }
+    }
+}
+
+template <int OP, int V, bool AL>
+__global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
+    constexpr int U = 4;
+    __shared__ RedScratch red;
+    int parity = 0;
+    const int W = a.W;
+    const int worker = threadIdx.x & (W - 1);
+    const int slot = threadIdx.x >> a.log2W;
+    const int cols = a.cols;
+    const int64_t ngroups = (a.rows + a.B - 1) / a.B;
+    const bool yvec = AL || a.y_vec;
+
+    for (int64_t g = blockIdx.x; g < ngroups; g += gridDim.x) {
+        const int64_t row = g * a.B + slot;
+        const bool active = row < a.rows;
+        const RowGeom<V, AL> geo(a.x, active ? row : 0, cols);
+        const int64_t base = geo.base;
+        const int hd = geo.hd, nb = geo.nb;
+        const float *xb = a.x + base + hd;
+        const float *xrow = a.x + base;
+        // Loads the (residual-added) input values of one pack or the head.
+        auto load_x = [&](int off, int nv, float *t) {
+            if (off < 0) {
+                t[0] = xrow[-1 - off];
+                if constexpr (OP == OP_RESIDUAL_LAYERNORM)
+                    t[0] = __fadd_rn(t[0], a.res[base - 1 - off]);
+                return;
+            }
+            if (nv == V) {
+                ld_vec<V>(xb + off, t);
+            } else {
+#pragma unroll
+                for (int e = 0; e < V; ++e) t[e] = e < nv ? xb[off + e] : 0.f;
+            }
+            if constexpr (OP == OP_RESIDUAL_LAYERNORM) {
+                const float *rb = a.res + base + hd;
+                float r[V];
+                if (nv == V && (AL || a.r_vec)) {
+                    ld_vec<V>(rb + off, r);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < V; ++e) r[e] = e < nv ? rb[off + e] : 0.f;
+                }
+#pragma unroll
+                for (int e = 0; e < V; ++e) t[e] = __fadd_rn(t[e], r[e]);
+            }
+        };
+        // Column of element e of a pack at body offset `off` (or the head).
+        auto column = [&](int off, int e) { return off < 0 ? -1 - off : hd + off + e; };
+
+        if constexpr (OP == OP_RMSNORM) {
+            float ss = 0.f;
+            stream_row<V, AL, U>(worker, W, hd, nb, active, load_x,
+                                 [&](const float *t, int nv, int) {
+#pragma unroll
+                                     for (int e = 0; e < V; ++e)
+                                         if (e < nv) ss = fmaf(t[e], t[e], ss);
+                                 });
+            ss = row_allreduce<SumOp>(ss, W, red, parity);
+            const float r = rsqrtf(ss / (float)cols + a.eps);
+            float *yb = a.y + base + hd;
+            stream_row<V, AL, U>(
+                worker, W, hd, nb, active, load_x,
+                [&](const float *t, int nv, int off) {
+                    float o[V];
+                    if (off < 0) {
+                        const int c = column(off, 0);
+                        a.y[base + c] = t[0] * r * (a.w ? __ldg(a.w + c) : 1.f);
+                        return;
+                    }
+                    float wv[V];
+                    param_pack<V>(a.w, hd + off, nv, AL, 1.f, wv);
+#pragma unroll
+                    for (int e = 0; e < V; ++e) o[e] = t[e] * r * wv[e];
+                    store_pack<V>(yb, off, nb, true, yvec, o);
+                });
+        } else if constexpr (OP == OP_LAYERNORM ||
+                             OP == OP_RESIDUAL_LAYERNORM) {
+            float s = 0.f;
+            stream_row<V, AL, U>(worker, W, hd, nb, active, load_x,
+                                 [&](const float *t, int nv, int) {
+#pragma unroll
+                                     for (int e = 0; e < V; ++e)
+                                         if (e < nv) s += t[e];
+                                 });
+            s = row_allreduce<SumOp>(s, W, red, parity);
+            const float mean = s / (float)cols;
+            float q = 0.f;
+            stream_row<V, AL, U>(worker, W, hd, nb, active, load_x,
+                                 [&](const float *t, int nv, int) {
+#pragma unroll
+                                     for (int e = 0; e < V; ++e)
+                                         if (e < nv) {
+                                             const float d = t[e] - mean;
+                                             q = fmaf(d, d, q);
+                                         }
+                                 });
+            q = row_allreduce<SumOp>(q, W, red, parity);
+            const float rstd = rsqrtf(q / (float)cols + a.eps);
+            float *yb = a.y + base + hd;
+            float *hb = a.h ? a.h + base + hd : nullptr;
+            const bool hvec = AL || a.h_vec;
+            stream_row<V, AL, U>(
+                worker, W, hd, nb, active, load_x,
+                [&](const float *t, int nv, int off) {
+                    if (off < 0) {
+                        const int c = column(off, 0);
+                        const float gh = a.w ? __ldg(a.w + c) : 1.f;
+                        const float bh = a.b ? __ldg(a.b + c) : 0.f;
+                        a.y[base + c] = fmaf((t[0] - mean) * rstd, gh, bh);
+                        if (OP == OP_RESIDUAL_LAYERNORM && a.h) a.h[base + c] = t[0];
+                        return;
+                    }
+                    float gv[V], bv[V], o[V];
+                    param_pack<V>(a.w, hd + off, nv, AL, 1.f, gv);
+                    param_pack<V>(a.b, hd + off, nv, AL, 0.f, bv);
+#pragma unroll
+                    for (int e = 0; e < V; ++e)
+                        o[e] = fmaf((t[e] - mean) * rstd, gv[e], bv[e]);
+                    store_pack<V>(yb, off, nb, true, yvec, o);
+                    if (OP == OP_RESIDUAL_LAYERNORM && hb)
+                        store_pack<V>(hb, off, nb, true, hvec, t);
+                });
+        } else if constexpr (OP == OP_SOFTMAX || OP == OP_CROSS_ENTROPY) {
+            float m = -INFINITY, s = 0.f;
+            stream_row<V, AL, U>(worker, W, hd, nb, active, load_x,
+                                 [&](const float *t, int nv, int) {
+                                     float pm = -INFINITY;
+#pragma unroll
+                                     for (int e = 0; e < V; ++e)
+                                         if (e < nv) pm = nanmax(pm, t[e]);
+                                     float ps = 0.f;
+#pragma unroll
+                                     for (int e = 0; e < V; ++e)
+                                         if (e < nv) ps += expf(t[e] - pm);
+                                     lse_merge(m, s, pm, ps);
+                                 });
+            row_allreduce_lse(m, s, W, red, parity);
+            if constexpr (OP == OP_SOFTMAX) {
+                const float inv = 1.f / s;
+                float *yb = a.y + base + hd;
+                stream_row<V, AL, U>(
+                    worker, W, hd, nb, active, load_x,
+                    [&](const float *t, int nv, int off) {
+                        if (off < 0) {
+                            a.y[base + column(off, 0)] = expf(t[0] - m) * inv;
+                            return;
+                        }
+                        float o[V];
+#pragma unroll
+                        for (int e = 0; e < V; ++e) o[e] = expf(t[e] - m) * inv;
+                        store_pack<V>(yb, off, nb, true, yvec, o);
+                    });
+            } else {
+                if (active && worker == 0) {
+                    const int32_t lab = __ldg(a.labels + row);
+                    const float xl =
+                        (lab >= 0 && lab < cols) ? a.x[base + lab] : NAN;
+                    a.out[row] = (m + logf(s)) - xl;
+                }
+            }
+        } else if constexpr (OP == OP_ROW_SUM) {
+            float s = 0.f, c = 0.f;
+            stream_row<V, AL, U>(worker, W, hd, nb, active, load_x,
+                                 [&](const float *t, int nv, int) {
+#pragma unroll
+                                     for (int e = 0; e < V; ++e)
+                                         if (e < nv) {
+                                             float u, err;
+                                             two_sum(s, t[e], u, err);
+                                             s = u;
+                                             c += err;
+                                         }
+                                 });
+            row_allreduce_compensated(s, c, W, red, parity);
+            if (active && worker == 0) a.out[row] = s + c;
+        }
+    }
+}
+
+// =========================================================================
+// Launch helpers
+// =========================================================================
+using KernelFn = void (*)(KArgs);
+
+template <int OP, int V, bool AL>
+__host__ KernelFn reg_kernel_for_chunks(int K) {
+    switch (K) {
+        case 1: return reg_kernel<OP, V, 1, AL>;
+        case 2: return reg_kernel<OP, V, 2, AL>;
+        case 4: return reg_kernel<OP, V, 4, AL>;
+        case 8: return reg_kernel<OP, V, 8, AL>;
+        case 16: return reg_kernel<OP, V, 16, AL>;
+        default: return nullptr;
+    }
+}
+
+template <int OP>
+__host__ KernelFn select_kernel(const mt_plan_t &p, bool aligned) {
+    const int V = p.values_per_thread;
+    if (p.path == MT_PATH_LOOP) {
+        if (V == 1) return loop_kernel<OP, 1, true>;
+        if (V == 2) return aligned ? loop_kernel<OP, 2, true> : loop_kernel<OP, 2, false>;
+        if (V == 4) return aligned ? loop_kernel<OP, 4, true> : loop_kernel<OP, 4, false>;
+        return nullptr;
+    }
+    if (V == 1) return reg_kernel_for_chunks<OP, 1, true>(p.chunks);
+    if (V == 2)
+        return aligned ? reg_kernel_for_chunks<OP, 2, true>(p.chunks)
+                       : reg_kernel_for_chunks<OP, 2, false>(p.chunks);
+    if (V == 4)
+        return aligned ? reg_kernel_for_chunks<OP, 4, true>(p.chunks)
+                       : reg_kernel_for_chunks<OP, 4, false>(p.chunks);
+    return nullptr;
+}
+
+template <int OP>
+__host__ cudaError_t launch_op(const mt_plan_t &p, const KArgs &a,
+                               bool aligned, cudaStream_t stream,
+                               int *max_threads_out) {
+    KernelFn k = select_kernel<OP>(p, aligned);
+    if (k == nullptr) return cudaErrorInvalidValue;
+    if (max_threads_out) {
+        cudaFuncAttributes attr;
+        cudaError_t e = cudaFuncGetAttributes(&attr, k);
+        if (e != cudaSuccess) return e;
+        *max_threads_out = attr.maxThreadsPerBlock;
+        if (p.threads_per_row * p.rows_per_block > attr.maxThreadsPerBlock)
+            return cudaErrorLaunchOutOfResources;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.grid);
+    cfg.blockDim = dim3((unsigned)(p.threads_per_row * p.rows_per_block));
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = nullptr;
+    cfg.numAttrs = 0;
+    return cudaLaunchKernelEx(&cfg, k, a);
+}
+
+template <int OP>
+__host__ cudaError_t occupancy_op(const mt_plan_t &p, bool aligned,
+                                  int *blocks_per_sm) {
+    KernelFn k = select_kernel<OP>(p, aligned);
+    if (k == nullptr) return cudaErrorInvalidValue;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        blocks_per_sm, k, p.threads_per_row * p.rows_per_block, 0);
+}
+
+}  // namespace mt
+
+#define MT_DEFINE_LAUNCHER(name, OPV)                                        \
+    namespace mt {                                                           \
+    cudaError_t name(const mt_plan_t &plan, const KArgs &a, bool aligned,    \
+                     cudaStream_t stream, int *max_threads_out) {            \
+        return launch_op<OPV>(plan, a, aligned, stream, max_threads_out);    \
+    }                                                                        \
+    cudaError_t name##_occupancy(const mt_plan_t &plan, bool aligned,        \
+                                 int *blocks_per_sm) {                       \
+        return occupancy_op<OPV>(plan, aligned, blocks_per_sm);              \
+    }                                                                        \
+    }

@@ -1,0 +1,35 @@
+// ops_cross_entropy.cu -- instantiates the cross-entropy kernels and the
+// one-CTA kernel that averages the per-row losses.
+#include "mt_kernels.cuh"
+
+MT_DEFINE_LAUNCHER(launch_cross_entropy, OP_CROSS_ENTROPY)
+
+namespace mt {
+
+// mean = (sum of loss[0..rows)) / rows.  One CTA; each thread sums a strided
+// subset in index order with compensated arithmetic, then the block combines
+// the partials in a fixed shuffle/shared-memory order, so the result does not
+// depend on timing (no atomics).
+__global__ void __launch_bounds__(1024)
+    mean_kernel(const float *loss, float *mean, int64_t rows) {
+    __shared__ RedScratch red;
+    int parity = 0;
+    float s = 0.f, c = 0.f;
+    for (int64_t i = threadIdx.x; i < rows; i += blockDim.x) {
+        float t, err;
+        two_sum(s, loss[i], t, err);
+        s = t;
+        c += err;
+    }
+    row_allreduce_compensated(s, c, (int)blockDim.x, red, parity);
+    if (threadIdx.x == 0)
+        *mean = (float)((double)(s + c) / (double)rows);
+}
+
+cudaError_t launch_mean(const float *loss, float *mean, int64_t rows,
+                        cudaStream_t stream) {
+    mean_kernel<<<1, 1024, 0, stream>>>(loss, mean, rows);
+    return cudaGetLastError();
+}
+
+}  // namespace mt

@@ -1,0 +1,363 @@
+"""GPU parity: the CUDA library against the CPU oracle, element by element,
+through the C ABI, on the published shapes and the edge cases of the work
+mapping.  Tolerance |gpu - ref| <= 1e-5*(1+|ref|); bit-exact where the result
+is exactly representable (integer row sums, the residual sum h_out).
+
+The lane-mapping matrix follows the test the pages describe ("Consecutive-
+worker reduction layout checkpoint", §Verification checkpoint: V = 2/4/8
+across N = 1/31/33/127/128/129/257/4103, five rows, packed short rows and
+eight-subgroup wide rows), widened to every operator and to V = 1/2/4, W from
+1 to 1024 and rows-per-block packing.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import row_reduction_gb300 as mt
+from row_reduction_gb300 import inputs
+from gpu_util import Guarded, assert_close, to_dev
+
+pytestmark = pytest.mark.gpu
+
+OPS = list(inputs.OPS)
+SEED = inputs.TUNE_SEED
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from row_reduction_gb300 import build
+    build.build()
+    oracle.build()
+
+
+# ---------------------------------------------------------------- helpers
+def call(op, p, rows, cols, eps=None, plan=None, stream=None):
+    """Calls the *_with_plan C entry point of `op` with device addresses."""
+    if op == "rmsnorm":
+        mt.mt_rmsnorm_f32_with_plan(p["x"], p.get("weight"), p["y"], rows,
+                                    cols, eps, stream, plan)
+    elif op == "layernorm":
+        mt.mt_layernorm_f32_with_plan(p["x"], p.get("gamma"), p.get("beta"),
+                                      p["y"], rows, cols, eps, stream, plan)
+    elif op == "residual_layernorm":
+        mt.mt_residual_layernorm_f32_with_plan(
+            p["x"], p["residual"], p.get("gamma"), p.get("beta"), p["y"],
+            p.get("h_out"), rows, cols, eps, stream, plan)
+    elif op == "softmax":
+        mt.mt_softmax_f32_with_plan(p["x"], p["y"], rows, cols, stream, plan)
+    elif op == "row_sum":
+        mt.mt_row_sum_f32_with_plan(p["x"], p["out"], rows, cols, stream,
+                                    plan)
+    elif op == "cross_entropy":
+        mt.mt_cross_entropy_f32_with_plan(p["x"], p["labels"], p["loss"],
+                                          p.get("mean_loss"), rows, cols,
+                                          stream, plan)
+    else:
+        raise ValueError(op)
+
+
+def outputs_of(op, rows, cols):
+    if op in ("rmsnorm", "layernorm", "softmax"):
+        return {"y": rows * cols}
+    if op == "residual_layernorm":
+        return {"y": rows * cols, "h_out": rows * cols}
+    if op == "row_sum":
+        return {"out": rows}
+    return {"loss": rows, "mean_loss": 1}
+
+
+def run_guarded(op, d, rows, cols, plan=None, offsets=None):
+    """Runs `op` on guarded copies of the inputs in `d`; returns numpy
+    outputs after checking every guard region."""
+    offsets = offsets or {}
+    bufs = {}
+    for k, v in d.items():
+        if isinstance(v, np.ndarray):
+            fill = float("nan") if v.dtype == np.float32 else -7
+            dt = torch.float32 if v.dtype == np.float32 else torch.int32
+            bufs[k] = Guarded(v.size, offsets.get(k, 0), fill, dt, v)
+    for k, n in outputs_of(op, rows, cols).items():
+        bufs[k] = Guarded(n, offsets.get(k, 0), Guarded.SENTINEL)
+    call(op, {k: b.ptr for k, b in bufs.items()}, rows, cols, d.get("eps"),
+         plan)
+    torch.cuda.synchronize()
+    for b in bufs.values():
+        b.check()
+    res = {}
+    for k in outputs_of(op, rows, cols):
+        a = bufs[k].numpy()
+        res[k] = a.reshape(rows, cols) if a.size == rows * cols and \
+            k in ("y", "h_out") else a
+    return res
+
+
+def compare(op, got, ref, what):
+    for k, r in ref.items():
+        if k == "h_out":
+            assert np.array_equal(got[k].view(np.uint32),
+                                  r.view(np.uint32)), f"{what}: h_out bits"
+        else:
+            assert_close(got[k], r, f"{what} {k}")
+
+
+# --------------------------------------------------- published shapes
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("shape", inputs.FAMILY_SHAPES)
+def test_family_shapes_default_plan(op, shape):
+    rows, cols = shape
+    d = inputs.make(op, rows, cols, SEED)
+    got = run_guarded(op, d, rows, cols)
+    compare(op, got, oracle.run(op, d), f"{op} {shape}")
+
+
+@pytest.mark.parametrize("shape", inputs.RMSNORM_SHAPES)
+def test_rmsnorm_published_small_shapes(shape):
+    d = inputs.make("rmsnorm", *shape, seed=SEED + 1)
+    got = run_guarded("rmsnorm", d, *shape)
+    compare("rmsnorm", got, oracle.run("rmsnorm", d), f"rmsnorm {shape}")
+
+
+@pytest.mark.parametrize("shape", inputs.RMSNORM_SWEEP)
+def test_rmsnorm_sweep_full_size(shape):
+    """Full-size sweep shapes (1% outliers) with the default plan: sampled
+    rows against the oracle, and on every row the unit-weight invariant
+    mean((y/w)^2) = ms/(ms+eps) recomputed in float64."""
+    rows, cols = shape
+    d = inputs.make("rmsnorm", rows, cols, SEED + 2, outliers=True)
+    t = to_dev(d)
+    y = mt.rmsnorm(t["x"], t["weight"], d["eps"])
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(7)
+    sample = np.unique(np.concatenate(
+        [[0, rows - 1], rng.integers(0, rows, 30)]))
+    ref = oracle.rmsnorm(d["x"][sample], d["weight"], d["eps"])
+    assert_close(y[torch.from_numpy(sample).cuda()].cpu().numpy(), ref,
+                 f"rmsnorm {shape} sampled rows")
+    xd = t["x"].double()
+    ms = (xd * xd).mean(dim=1)
+    eps = float(np.float32(d["eps"]))
+    u = (y.double() / t["weight"].double())
+    lhs = (u * u).mean(dim=1)
+    rhs = ms / (ms + eps)
+    assert torch.allclose(lhs, rhs, rtol=2e-5, atol=0)
+
+
+# ------------------------------------------------ lane-mapping matrix
+MAP_N = [1, 31, 33, 127, 128, 129, 257, 4103]
+
+
+def candidate_plans(cols):
+    plans = []
+    for V in (1, 2, 4):
+        for W in (1, 2, 4, 8, 32, 64, 256, 1024):
+            for packed in (False, True):
+                B = max(1, 32 // W) if not packed else max(1, 256 // W)
+                # register path: smallest instantiated chunk count
+                for K in (1, 2, 4, 8, 16):
+                    if W * V * K >= cols:
+                        plans.append(mt.make_plan(W, V, K, B))
+                        break
+                if W <= 512:
+                    plans.append(mt.make_plan(W, V, 0, B, mt.MT_PATH_LOOP))
+    out, seen = [], set()
+    for p in plans:
+        key = tuple(p.as_dict().values())
+        if key not in seen and mt.mt_plan_check(0, cols, p) == mt.MT_OK:
+            seen.add(key)
+            out.append(p)
+    return out
+
+
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("cols", MAP_N)
+def test_mapping_matrix(op, cols):
+    for rows in (5, 17):
+        d = inputs.make(op, rows, cols, SEED + cols + rows)
+        ref = oracle.run(op, d)
+        t = to_dev(d)
+        plans = candidate_plans(cols)
+        assert plans
+        for p in plans:
+            outs = {k: torch.full((n,), Guarded.SENTINEL, device="cuda")
+                    for k, n in outputs_of(op, rows, cols).items()}
+            ptrs = {k: v.data_ptr() for k, v in t.items()
+                    if isinstance(v, torch.Tensor)}
+            ptrs.update({k: v.data_ptr() for k, v in outs.items()})
+            call(op, ptrs, rows, cols, d.get("eps"), p)
+            got = {k: (v.cpu().numpy().reshape(rows, cols)
+                       if k in ("y", "h_out") else v.cpu().numpy())
+                   for k, v in outs.items()}
+            compare(op, got, ref, f"{op} {rows}x{cols} "
+                    f"{mt.mt_describe_plan(p)}")
+
+
+# --------------------------------------- alignment heads and guards
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("cols", [3, 127, 257, 4096, 4103])
+@pytest.mark.parametrize("xoff,yoff", [(1, 1), (2, 0), (3, 1), (0, 2)])
+def test_unaligned_bases(op, cols, xoff, yoff):
+    """Base pointers shifted by 1-3 floats: rows start off the 16-byte grid
+    (heads are peeled) and outputs may be out of phase with x (scalar
+    stores).  Guards are NaN on inputs and a sentinel on outputs."""
+    rows = 9
+    d = inputs.make(op, rows, cols, SEED + 3 * cols + xoff)
+    offs = {"x": xoff, "y": yoff, "h_out": (yoff + 1) % 4,
+            "residual": (xoff + 2) % 4, "weight": 1, "gamma": 3, "beta": 2,
+            "out": yoff, "loss": 1, "labels": 1}
+    ref = oracle.run(op, d)
+    got = run_guarded(op, d, rows, cols, offsets=offs)
+    compare(op, got, ref, f"{op} x+{xoff} y+{yoff} cols={cols}")
+    for V in (2, 4):
+        for W in (4, 32, 128):
+            p = mt.make_plan(W, V, 16, max(1, 32 // W))
+            if cols > W * V * 16:
+                continue
+            got = run_guarded(op, d, rows, cols, plan=p, offsets=offs)
+            compare(op, got, ref, f"{op} forced {mt.mt_describe_plan(p)}")
+            p = mt.make_plan(W, V, 0, max(1, 32 // W), mt.MT_PATH_LOOP)
+            got = run_guarded(op, d, rows, cols, plan=p, offsets=offs)
+            compare(op, got, ref, f"{op} forced {mt.mt_describe_plan(p)}")
+
+
+# ------------------------------------------------------ wide rows
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("cols", [16384, 32771, 100003])
+def test_wide_rows(op, cols):
+    rows = 3
+    d = inputs.make(op, rows, cols, SEED + cols)
+    got = run_guarded(op, d, rows, cols)
+    compare(op, got, oracle.run(op, d), f"{op} {rows}x{cols}")
+
+
+# --------------------------------------------------- exact results
+def test_row_sum_of_integers_is_bit_exact():
+    for rows, cols in ((17, 257), (64, 4096), (3, 100003), (1024, 4096)):
+        x = inputs.integer_valued(rows, cols, SEED)
+        ref = x.astype(np.int64).sum(axis=1).astype(np.float32)
+        xt = torch.from_numpy(x).cuda()
+        for p in [None] + candidate_plans(cols)[:12]:
+            if p is not None and cols > 4103:
+                break
+            got = mt.row_sum(xt, plan=p).cpu().numpy()
+            assert np.array_equal(got, ref), (rows, cols, p)
+
+
+def test_row_sum_near_zero_rows():
+    """Rows whose sum cancels to near zero keep the 1e-5*(1+|ref|)
+    tolerance (compensated accumulation)."""
+    rows, cols = 64, 4096
+    d = inputs.make("row_sum", rows, cols, SEED)
+    x = d["x"].copy()
+    x[:, cols // 2:] = -x[:, :cols // 2][:, ::-1]   # exact cancellation
+    x[:, 0] += np.float32(1e-3)
+    ref = oracle.row_sum(x)
+    got = mt.row_sum(torch.from_numpy(x).cuda()).cpu().numpy()
+    assert_close(got, ref, "near-zero sums")
+
+
+def test_residual_h_out_bit_exact_and_aliasing():
+    rows, cols = 33, 1000
+    d = inputs.make("residual_layernorm", rows, cols, SEED)
+    t = to_dev(d)
+    y, h = mt.residual_layernorm(t["x"], t["residual"], t["gamma"],
+                                 t["beta"], d["eps"], return_h=True)
+    assert torch.equal(h, t["x"] + t["residual"])
+    ref_y, _ = oracle.residual_layernorm(d["x"], d["residual"], d["gamma"],
+                                         d["beta"], d["eps"])
+    assert_close(y.cpu().numpy(), ref_y, "resln")
+    # y written over x and h over the residual
+    x2, r2 = t["x"].clone(), t["residual"].clone()
+    mt.mt_residual_layernorm_f32(x2, r2, t["gamma"], t["beta"], x2, r2, rows,
+                                 cols, d["eps"])
+    assert torch.equal(x2, y) and torch.equal(r2, h)
+
+
+@pytest.mark.parametrize("op", ["rmsnorm", "layernorm", "softmax"])
+def test_in_place(op):
+    for rows, cols in ((17, 257), (64, 4096), (2, 40000)):
+        d = inputs.make(op, rows, cols, SEED)
+        t = to_dev(d)
+        ref = mt.run(op, t)["y"]
+        x = t["x"]
+        if op == "rmsnorm":
+            mt.mt_rmsnorm_f32(x, t["weight"], x, rows, cols, d["eps"])
+        elif op == "layernorm":
+            mt.mt_layernorm_f32(x, t["gamma"], t["beta"], x, rows, cols,
+                                d["eps"])
+        else:
+            mt.mt_softmax_f32(x, x, rows, cols)
+        assert torch.equal(x, ref)
+
+
+def test_softmax_special_rows():
+    x = np.array([[1.0, np.nan, 2.0, 3.0], [1000.0, 1000.0, -1000.0, 0.0],
+                  [5.0, 5.0, 5.0, 5.0], [-np.inf, 0.0, 0.0, -np.inf]],
+                 dtype=np.float32)
+    ref = oracle.softmax(x)
+    got = mt.softmax(torch.from_numpy(x).cuda()).cpu().numpy()
+    assert_close(got, ref, "softmax special rows")
+
+
+def test_cross_entropy_labels_and_mean():
+    rows, cols = 64, 4096
+    d = inputs.make("cross_entropy", rows, cols, SEED)
+    d["labels"][3] = cols        # out of range -> NaN row
+    d["labels"][7] = -1
+    t = to_dev(d)
+    loss, m = mt.cross_entropy(t["x"], t["labels"])
+    ref_loss, ref_mean = oracle.cross_entropy(d["x"], d["labels"])
+    assert_close(loss.cpu().numpy(), ref_loss, "loss")
+    assert math.isnan(float(m)) and math.isnan(ref_mean)
+    d["labels"][3], d["labels"][7] = 0, cols - 1
+    t = to_dev(d)
+    loss, m = mt.cross_entropy(t["x"], t["labels"])
+    ref_loss, ref_mean = oracle.cross_entropy(d["x"], d["labels"])
+    assert_close(loss.cpu().numpy(), ref_loss, "loss")
+    assert_close(m.cpu().numpy(), np.array([ref_mean]), "mean")
+    # Mean over many rows (the mean kernel's strided loop).
+    d = inputs.make("cross_entropy", 70000, 33, SEED)
+    t = to_dev(d)
+    loss, m = mt.cross_entropy(t["x"], t["labels"])
+    ref_loss, ref_mean = oracle.cross_entropy(d["x"], d["labels"])
+    assert_close(m.cpu().numpy(), np.array([ref_mean]), "mean 70000 rows")
+
+
+@pytest.mark.parametrize("op", OPS)
+def test_determinism(op):
+    rows, cols = 1024, 4096
+    d = inputs.make(op, rows, cols, SEED)
+    t = to_dev(d)
+    a = mt.run(op, t)
+    b = mt.run(op, t)
+    for k in a:
+        assert torch.equal(a[k].view(torch.int32), b[k].view(torch.int32))
+
+
+def test_non_default_stream_and_zero_rows():
+    d = inputs.make("rmsnorm", 64, 4096, SEED)
+    t = to_dev(d)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        y = mt.rmsnorm(t["x"], t["weight"], d["eps"], stream=s)
+    s.synchronize()
+    assert_close(y.cpu().numpy(), oracle.rmsnorm(d["x"], d["weight"],
+                                                 d["eps"]), "stream")
+    e = torch.empty(0, 4096, device="cuda")
+    assert mt.rmsnorm(e, t["weight"]).shape == (0, 4096)
+
+
+def test_forced_plan_errors_on_gpu():
+    x = torch.zeros(4, 4096, device="cuda")
+    with pytest.raises(mt.MTError) as ei:
+        mt.rmsnorm(x, plan=mt.make_plan(256, 4, 2, 1))
+    assert ei.value.status == mt.MT_ERR_OUT_OF_RESOURCES
+    with pytest.raises(mt.MTError) as ei:
+        mt.rmsnorm(x, plan=mt.make_plan(96, 4, 16, 1))
+    assert ei.value.status == mt.MT_ERR_INVALID_ARGUMENT
+    # explicit grids, including one smaller than the row-group count
+    for g in (1, 3, 1000):
+        y = mt.rmsnorm(x + 1, plan=mt.make_plan(256, 4, 4, 1, grid=g))
+        assert torch.allclose(y, torch.ones_like(y), rtol=1e-5)
