@@ -40,29 +40,19 @@ sys.path.insert(0, ROOT)
 
 import numpy as np  # noqa: E402
 
+from row_reduction_gb300.timing import (  # noqa: E402
+    Workload, algorithmic_bytes, time_e2e, time_graph_steps,
+    time_plain_steps)
+
 METRIC = ("RMSNorm FP32 µs/op and HBM GB/s (% of GB300 peak), "
           "1×127 … 1024×4096")
 FALLBACK_HBM_GBS = 6800.0
 
 
 # ---------------------------------------------------------------- helpers
-def algorithmic_bytes(op, rows, cols, h_out=False, mean=False):
-    """Bytes an operator must move once: each input read once, each output
-    written once, parameter vectors counted once."""
-    rc = rows * cols
-    if op == "rmsnorm":
-        return 8 * rc + 4 * cols
-    if op == "layernorm":
-        return 8 * rc + 8 * cols
-    if op == "residual_layernorm":
-        return 12 * rc + 8 * cols + (4 * rc if h_out else 0)
-    if op == "softmax":
-        return 8 * rc
-    if op == "row_sum":
-        return 4 * rc + 4 * rows
-    if op == "cross_entropy":
-        return 4 * rc + 8 * rows + (4 if mean else 0)
-    raise ValueError(op)
+def plan_text(op, rows, cols):
+    import row_reduction_gb300 as mt
+    return mt.mt_describe_plan(mt.mt_plan_query(op, rows, cols))
 
 
 def measured_peak():
@@ -158,206 +148,6 @@ class ClockSampler:
                     "samples": 0}
         return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxs),
                 "reasons": sorted(reasons), "samples": len(sms)}
-
-
-# ------------------------------------------------------------ GPU harness
-class Workload:
-    """A pool of buffer sets for one (op, rows, cols) plus fast launchers."""
-
-    def __init__(self, op, rows, cols, seed, outliers, l2_bytes,
-                 max_pool_bytes=16 << 30):
-        import torch
-        import row_reduction_gb300 as mt
-        from row_reduction_gb300 import inputs
-        self.op, self.rows, self.cols = op, rows, cols
-        d = inputs.make(op, rows, cols, seed, outliers=outliers)
-        self.host = d
-        self.eps = float(d.get("eps", 0.0))
-        self.mean = op == "cross_entropy"
-        self.h_out = op == "residual_layernorm"
-        self.bytes = algorithmic_bytes(op, rows, cols, self.h_out, self.mean)
-        params = {k: torch.from_numpy(d[k]).cuda() for k in
-                  ("weight", "gamma", "beta") if k in d}
-        set_bytes = max(self.bytes, 1)
-        n = max(1, math.ceil(4 * l2_bytes / set_bytes))
-        n = max(1, min(n, max_pool_bytes // set_bytes, 256))
-        self.sets = []
-        for i in range(n):
-            s = dict(params)
-            s["x"] = torch.from_numpy(d["x"]).cuda()
-            if "residual" in d:
-                s["residual"] = torch.from_numpy(d["residual"]).cuda()
-            if "labels" in d:
-                s["labels"] = torch.from_numpy(d["labels"]).cuda()
-            if op in ("rmsnorm", "layernorm", "softmax",
-                      "residual_layernorm"):
-                s["y"] = torch.empty_like(s["x"])
-            if self.h_out:
-                s["h_out"] = torch.empty_like(s["x"])
-            if op == "row_sum":
-                s["out"] = torch.empty(rows, device="cuda")
-            if op == "cross_entropy":
-                s["loss"] = torch.empty(rows, device="cuda")
-                s["mean_loss"] = torch.empty(1, device="cuda")
-            self.sets.append(s)
-        self.pool_bytes = n * set_bytes
-        # Tiny shapes cannot fill 4x L2 with 256 sets; they are launch-bound
-        # and reported as "l2_resident".
-        self.l2_resident = self.pool_bytes < 4 * l2_bytes
-        self.launches_per_step = 2 if self.mean else 1
-        self.plan_text = mt.mt_describe_plan(mt.mt_plan_query(op, rows, cols))
-
-    def call_fn(self, i, stream_handle):
-        """A zero-argument callable issuing step i's library call (raw
-        ctypes entry point, arguments prepared once)."""
-        import ctypes
-        import row_reduction_gb300 as mt
-        L = mt.lib()
-        s = self.sets[i % len(self.sets)]
-        P = lambda k: s[k].data_ptr() if k in s else None  # noqa: E731
-        R, C, eps = self.rows, self.cols, ctypes.c_float(self.eps)
-        st = stream_handle
-        if self.op == "rmsnorm":
-            f, a = L.mt_rmsnorm_f32, (P("x"), P("weight"), P("y"), R, C, eps,
-                                      st)
-        elif self.op == "layernorm":
-            f, a = L.mt_layernorm_f32, (P("x"), P("gamma"), P("beta"),
-                                        P("y"), R, C, eps, st)
-        elif self.op == "residual_layernorm":
-            f, a = L.mt_residual_layernorm_f32, (
-                P("x"), P("residual"), P("gamma"), P("beta"), P("y"),
-                P("h_out"), R, C, eps, st)
-        elif self.op == "softmax":
-            f, a = L.mt_softmax_f32, (P("x"), P("y"), R, C, st)
-        elif self.op == "row_sum":
-            f, a = L.mt_row_sum_f32, (P("x"), P("out"), R, C, st)
-        else:
-            f, a = L.mt_cross_entropy_f32, (P("x"), P("labels"), P("loss"),
-                                            P("mean_loss"), R, C, st)
-
-        def go():
-            rc = f(*a)
-            if rc != 0:
-                raise RuntimeError(f"{self.op} failed with status {rc}")
-        return go
-
-
-def capture(work, first, count, stream):
-    """A CUDA graph of `count` consecutive steps starting at step `first`."""
-    import torch
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        h = torch.cuda.current_stream().cuda_stream
-        for i in range(first, first + count):
-            work.call_fn(i, h)()
-    return g
-
-
-def time_graph_steps(work, steps, warmup, per_graph=64, barrier=None,
-                     sampler=None):
-    """Times exactly `steps` steps (after `warmup`) replayed from graphs;
-    returns elapsed seconds on the device."""
-    import torch
-    stream = torch.cuda.Stream()
-    h = stream.cuda_stream
-    with torch.cuda.stream(stream):
-        for i in range(3):                       # fill the library's caches
-            work.call_fn(i, h)()
-    stream.synchronize()
-    # Graphs cycle through whole pools, so consecutive steps never reuse a
-    # buffer set before every other set has been used.
-    n = len(work.sets)
-    G = n * max(1, math.ceil(per_graph / n))
-    if steps < G:
-        G = steps
-    full = capture(work, 0, G, stream)
-    rem = steps % G
-    tail = capture(work, 0, rem, stream) if rem else None
-    with torch.cuda.stream(stream):
-        for _ in range(max(1, math.ceil(warmup / G))):
-            full.replay()
-    stream.synchronize()
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    if barrier:
-        barrier()
-    ctx = sampler if sampler is not None else _Null()
-    with ctx:
-        with torch.cuda.stream(stream):
-            start.record(stream)
-            for _ in range(steps // G):
-                full.replay()
-            if tail is not None:
-                tail.replay()
-            end.record(stream)
-        end.synchronize()
-    torch.cuda.synchronize()
-    if barrier:
-        barrier()
-    return start.elapsed_time(end) / 1e3
-
-
-class _Null:
-    def __enter__(self):
-        return self
-
-    def __exit__(self, *a):
-        return False
-
-
-def time_plain_steps(work, steps, warmup):
-    """Same steps, each launched from Python (host launch cost included)."""
-    import torch
-    stream = torch.cuda.Stream()
-    h = stream.cuda_stream
-    fns = [work.call_fn(i, h) for i in range(len(work.sets))]
-    with torch.cuda.stream(stream):
-        for i in range(warmup):
-            fns[i % len(fns)]()
-    stream.synchronize()
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        start.record(stream)
-        for i in range(steps):
-            fns[i % len(fns)]()
-        end.record(stream)
-    end.synchronize()
-    return start.elapsed_time(end) / 1e3
-
-
-def time_e2e(work, steps, warmup):
-    """Each step: pinned host x -> device, library call, y -> pinned host."""
-    import torch
-    s0 = work.sets[0]
-    x_host = torch.from_numpy(work.host["x"]).pin_memory()
-    out_key = {"row_sum": "out", "cross_entropy": "loss"}.get(work.op, "y")
-    out_host = torch.empty(s0[out_key].shape, dtype=s0[out_key].dtype,
-                           pin_memory=True)
-    stream = torch.cuda.Stream()
-    h = stream.cuda_stream
-    fn = work.call_fn(0, h)
-
-    def step():
-        s0["x"].copy_(x_host, non_blocking=True)
-        fn()
-        out_host.copy_(s0[out_key], non_blocking=True)
-
-    with torch.cuda.stream(stream):
-        for _ in range(warmup):
-            step()
-    stream.synchronize()
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        start.record(stream)
-        for _ in range(steps):
-            step()
-        end.record(stream)
-    end.synchronize()
-    return (start.elapsed_time(end) / 1e3, x_host.numel() * 4,
-            out_host.numel() * 4)
 
 
 def cpu_baseline(op, d, rows, cols, budget_s=10.0):
@@ -486,7 +276,7 @@ def run_ours(args, rank, world, local_rank):
                         "x~N(0,1) with 1% x100 outliers, "
                         "weight~1+0.1N(0,1), eps=1e-6",
             "op": args.op, "rows": args.rows, "cols": args.cols,
-            "plan": work.plan_text,
+            "plan": plan_text(args.op, args.rows, args.cols),
             "l2": f"inputs larger than L2: rotating pool of "
                   f"{len(work.sets)} buffer sets, "
                   f"{work.pool_bytes / 2**20:.0f} MiB >= 4x L2 "
@@ -534,7 +324,7 @@ def run_sweep(l2, peak):
         gbs = work.bytes / (el / steps) / 1e9
         out.append({"op": op, "rows": r, "cols": c, "outliers": outl,
                     "us_per_op": us, "gbs": gbs, "frac_of_peak": gbs / peak,
-                    "plan": work.plan_text, "pool_sets": len(work.sets),
+                    "plan": plan_text(op, r, c), "pool_sets": len(work.sets),
                     "l2_resident": work.l2_resident, "steps": steps})
         del work
         torch.cuda.empty_cache()

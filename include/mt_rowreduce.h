@@ -108,7 +108,15 @@ typedef struct mt_plan {
     int32_t grid;              /* CTAs to launch; 0 = min(row groups, CTAs
                                   resident on the device), the CTAs then loop
                                   over row groups (grid-stride) */
+    int32_t flags;             /* MT_PLAN_* bits */
 } mt_plan_t;
+
+/* Plan flag: launch as a programmatic dependent of the previous kernel on
+ * the stream.  The kernel may start while that kernel finishes; it only
+ * prefetches its first rows into L2 and then waits for the previous
+ * kernel's completion (and memory visibility) before it reads or writes any
+ * operand, so results are the same as with an ordinary launch. */
+#define MT_PLAN_PDL 1
 
 /* ---- operators ---------------------------------------------------------
  * Each takes its plan from the built-in, measured plan table

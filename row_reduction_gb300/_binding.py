@@ -36,6 +36,8 @@ OP_IDS = {"rmsnorm": 0, "layernorm": 1, "residual_layernorm": 2,
 MT_PATH_REGISTERS = 0
 MT_PATH_LOOP = 1
 
+MT_PLAN_PDL = 1
+
 # Symbols declared in include/mt_rowreduce.h.
 EXPORTS = (
     "mt_rmsnorm_f32", "mt_rmsnorm_f32_with_plan",
@@ -56,7 +58,8 @@ class MtPlan(ctypes.Structure):
                 ("chunks", ctypes.c_int32),
                 ("rows_per_block", ctypes.c_int32),
                 ("path", ctypes.c_int32),
-                ("grid", ctypes.c_int32)]
+                ("grid", ctypes.c_int32),
+                ("flags", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {f: getattr(self, f) for f, _ in self._fields_}
@@ -66,8 +69,8 @@ class MtPlan(ctypes.Structure):
 
 
 def make_plan(W, V, chunks=0, rows_per_block=1, path=MT_PATH_REGISTERS,
-              grid=0) -> MtPlan:
-    return MtPlan(W, V, chunks, rows_per_block, path, grid)
+              grid=0, flags=0) -> MtPlan:
+    return MtPlan(W, V, chunks, rows_per_block, path, grid, flags)
 
 
 class MTError(RuntimeError):

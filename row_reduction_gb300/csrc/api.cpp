@@ -132,6 +132,7 @@ mt_status dispatch(int op, KArgs a, const VecPtrs &vp,
     while ((1 << l) < a.W) ++l;
     a.log2W = l;
     a.B = p.rows_per_block;
+    a.pdl = (p.flags & MT_PLAN_PDL) ? 1 : 0;
 
     const int64_t ngroups = (a.rows + a.B - 1) / a.B;
     int64_t grid = p.grid;
@@ -183,9 +184,13 @@ mt_status mt_rmsnorm_f32_with_plan(const float *x, const float *weight,
                                    float *y, int64_t rows, int64_t cols,
                                    float eps, mt_stream_t stream,
                                    const mt_plan_t *plan) {
-    if (!x || !y || misaligned4(x) || misaligned4(y) || misaligned4(weight))
-        return MT_ERR_INVALID_ARGUMENT;
     if (mt_status st = check_shape(rows, cols)) return st;
+    if (rows > 0 && (!x || !y))
+        return MT_ERR_INVALID_ARGUMENT;
+    if (misaligned4(x) ||
+        misaligned4(y) ||
+        misaligned4(weight))
+        return MT_ERR_INVALID_ARGUMENT;
     mt::KArgs a = mt::base_args(x, rows, cols);
     a.w = weight;
     a.y = y;
@@ -208,10 +213,14 @@ mt_status mt_layernorm_f32_with_plan(const float *x, const float *gamma,
                                      int64_t rows, int64_t cols, float eps,
                                      mt_stream_t stream,
                                      const mt_plan_t *plan) {
-    if (!x || !y || misaligned4(x) || misaligned4(y) || misaligned4(gamma) ||
+    if (mt_status st = check_shape(rows, cols)) return st;
+    if (rows > 0 && (!x || !y))
+        return MT_ERR_INVALID_ARGUMENT;
+    if (misaligned4(x) ||
+        misaligned4(y) ||
+        misaligned4(gamma) ||
         misaligned4(beta))
         return MT_ERR_INVALID_ARGUMENT;
-    if (mt_status st = check_shape(rows, cols)) return st;
     mt::KArgs a = mt::base_args(x, rows, cols);
     a.w = gamma;
     a.b = beta;
@@ -235,11 +244,16 @@ mt_status mt_residual_layernorm_f32_with_plan(
     const float *x, const float *residual, const float *gamma,
     const float *beta, float *y, float *h_out, int64_t rows, int64_t cols,
     float eps, mt_stream_t stream, const mt_plan_t *plan) {
-    if (!x || !residual || !y || misaligned4(x) || misaligned4(residual) ||
-        misaligned4(y) || misaligned4(h_out) || misaligned4(gamma) ||
+    if (mt_status st = check_shape(rows, cols)) return st;
+    if (rows > 0 && (!x || !residual || !y))
+        return MT_ERR_INVALID_ARGUMENT;
+    if (misaligned4(x) ||
+        misaligned4(residual) ||
+        misaligned4(y) ||
+        misaligned4(h_out) ||
+        misaligned4(gamma) ||
         misaligned4(beta))
         return MT_ERR_INVALID_ARGUMENT;
-    if (mt_status st = check_shape(rows, cols)) return st;
     mt::KArgs a = mt::base_args(x, rows, cols);
     a.res = residual;
     a.w = gamma;
@@ -270,9 +284,12 @@ mt_status mt_residual_layernorm_f32(const float *x, const float *residual,
 mt_status mt_softmax_f32_with_plan(const float *x, float *y, int64_t rows,
                                    int64_t cols, mt_stream_t stream,
                                    const mt_plan_t *plan) {
-    if (!x || !y || misaligned4(x) || misaligned4(y))
-        return MT_ERR_INVALID_ARGUMENT;
     if (mt_status st = check_shape(rows, cols)) return st;
+    if (rows > 0 && (!x || !y))
+        return MT_ERR_INVALID_ARGUMENT;
+    if (misaligned4(x) ||
+        misaligned4(y))
+        return MT_ERR_INVALID_ARGUMENT;
     mt::KArgs a = mt::base_args(x, rows, cols);
     a.y = y;
     VecPtrs vp;
@@ -288,9 +305,12 @@ mt_status mt_softmax_f32(const float *x, float *y, int64_t rows,
 mt_status mt_row_sum_f32_with_plan(const float *x, float *out, int64_t rows,
                                    int64_t cols, mt_stream_t stream,
                                    const mt_plan_t *plan) {
-    if (!x || !out || misaligned4(x) || misaligned4(out))
-        return MT_ERR_INVALID_ARGUMENT;
     if (mt_status st = check_shape(rows, cols)) return st;
+    if (rows > 0 && (!x || !out))
+        return MT_ERR_INVALID_ARGUMENT;
+    if (misaligned4(x) ||
+        misaligned4(out))
+        return MT_ERR_INVALID_ARGUMENT;
     mt::KArgs a = mt::base_args(x, rows, cols);
     a.out = out;
     return dispatch(mt::OP_ROW_SUM, a, VecPtrs(), plan,
@@ -307,10 +327,14 @@ mt_status mt_cross_entropy_f32_with_plan(const float *logits,
                                          float *mean_loss, int64_t rows,
                                          int64_t cols, mt_stream_t stream,
                                          const mt_plan_t *plan) {
-    if (!logits || !labels || !loss || misaligned4(logits) ||
-        misaligned4(labels) || misaligned4(loss) || misaligned4(mean_loss))
-        return MT_ERR_INVALID_ARGUMENT;
     if (mt_status st = check_shape(rows, cols)) return st;
+    if (rows > 0 && (!logits || !labels || !loss))
+        return MT_ERR_INVALID_ARGUMENT;
+    if (misaligned4(logits) ||
+        misaligned4(labels) ||
+        misaligned4(loss) ||
+        misaligned4(mean_loss))
+        return MT_ERR_INVALID_ARGUMENT;
     mt::KArgs a = mt::base_args(logits, rows, cols);
     a.labels = labels;
     a.out = loss;

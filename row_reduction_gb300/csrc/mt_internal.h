@@ -38,6 +38,9 @@ struct KArgs {
     // Unaligned mode only: 1 when the pointer keeps x's 16-byte phase, so
     // its row body can use vector accesses too.
     int32_t y_vec, h_vec, r_vec;
+    // Launched as a programmatic dependent: prefetch the first row group
+    // into L2 before waiting on the previous grid.
+    int32_t pdl;
 };
 
 // Instantiated register-path chunk counts.

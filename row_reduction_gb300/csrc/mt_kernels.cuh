@@ -265,6 +265,53 @@ __device__ __forceinline__ void row_allreduce_lse(float &m, float &s, int W,
     s = __shfl_sync(kFull, ts, 0);
 }
 
+// ---- launch overlap ---------------------------------------------------------
+// Programmatic dependent launch: the next kernel on the stream may start as
+// soon as every CTA of this one has started; griddepcontrol.wait then holds
+// it until this grid has completed and its writes are visible.  Without the
+// launch attribute both instructions have no effect.
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_wait_prerequisites() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Asks L2 to fetch the 16-byte-aligned interior of [p, p + bytes) with bulk
+// prefetches of at most 64 KiB each.  A prefetch changes no value, so it may
+// run before the wait on the previous grid.
+__device__ __forceinline__ void prefetch_l2(const void *p, int64_t bytes) {
+    uintptr_t s = (reinterpret_cast<uintptr_t>(p) + 15) & ~(uintptr_t)15;
+    const uintptr_t e =
+        (reinterpret_cast<uintptr_t>(p) + (uintptr_t)bytes) & ~(uintptr_t)15;
+    while (s < e) {
+        const uintptr_t n = e - s < 65536 ? e - s : 65536;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(s),
+                     "r"((unsigned)n)
+                     : "memory");
+        s += n;
+    }
+}
+
+// Kernel prologue: with `pdl`, thread 0 prefetches the CTA's first row group
+// (x and, for residual LayerNorm, the residual) into L2; then every thread
+// lets dependents launch and waits for the previous grid.
+template <int OP>
+__device__ __forceinline__ void kernel_prologue(const KArgs &a) {
+    if (a.pdl && threadIdx.x == 0) {
+        const int64_t r0 = (int64_t)blockIdx.x * a.B;
+        if (r0 < a.rows) {
+            const int64_t nr = a.rows - r0 < a.B ? a.rows - r0 : a.B;
+            const int64_t bytes = nr * (int64_t)a.cols * 4;
+            prefetch_l2(a.x + r0 * a.cols, bytes);
+            if constexpr (OP == OP_RESIDUAL_LAYERNORM)
+                prefetch_l2(a.res + r0 * a.cols, bytes);
+        }
+    }
+    grid_launch_dependents();
+    grid_wait_prerequisites();
+}
+
 // ---- per-row geometry ------------------------------------------------------
 template <int V, bool AL>
 struct RowGeom {
@@ -331,6 +378,7 @@ __device__ __forceinline__ void store_pack(float *p, int off, int nb,
 template <int OP, int V, int K, bool AL>
 __global__ void __launch_bounds__(reg_max_threads(V * K))
     reg_kernel(const KArgs a) {
+    kernel_prologue<OP>(a);
     __shared__ RedScratch red;
     int parity = 0;
     const int W = a.W;
@@ -592,6 +640,7 @@ __device__ __forceinline__ void stream_row(int worker, int W, int hd, int nb,
 
 template <int OP, int V, bool AL>
 __global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
+    kernel_prologue<OP>(a);
     constexpr int U = 4;
     __shared__ RedScratch red;
     int parity = 0;
@@ -820,13 +869,16 @@ __host__ cudaError_t launch_op(const mt_plan_t &p, const KArgs &a,
         if (p.threads_per_row * p.rows_per_block > attr.maxThreadsPerBlock)
             return cudaErrorLaunchOutOfResources;
     }
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.grid);
     cfg.blockDim = dim3((unsigned)(p.threads_per_row * p.rows_per_block));
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
-    cfg.attrs = nullptr;
-    cfg.numAttrs = 0;
+    cfg.attrs = a.pdl ? attr : nullptr;
+    cfg.numAttrs = a.pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, k, a);
 }
 

@@ -1,0 +1,280 @@
+"""Device timing of library calls, shared by the tuner and the benchmark.
+
+A :class:`Workload` holds a pool of input/output buffer sets for one
+(operator, rows, cols); consecutive steps cycle through the pool, which is
+sized to at least 4x the L2 cache (capped at 256 sets), so no step finds its
+input in L2 unless the whole pool fits there (tiny, launch-bound shapes;
+``l2_resident`` says so).  Steps are captured into CUDA graphs of whole pool
+cycles and replayed back to back on one stream; CUDA events on that stream
+bracket the timed replays.  The timing method follows the pages' contract of
+batched GPU intervals divided by the batch size ("Consecutive-worker
+reduction layout checkpoint", §Measurement contract).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+
+from . import _binding as B
+from . import inputs
+
+MAX_SETS = 256
+
+
+def algorithmic_bytes(op, rows, cols, h_out=False, mean=False):
+    """Bytes the operator must move once: every input element read once,
+    every output written once, parameter vectors counted once."""
+    rc = rows * cols
+    if op == "rmsnorm":
+        return 8 * rc + 4 * cols
+    if op == "layernorm":
+        return 8 * rc + 8 * cols
+    if op == "residual_layernorm":
+        return 12 * rc + 8 * cols + (4 * rc if h_out else 0)
+    if op == "softmax":
+        return 8 * rc
+    if op == "row_sum":
+        return 4 * rc + 4 * rows
+    if op == "cross_entropy":
+        return 4 * rc + 8 * rows + (4 if mean else 0)
+    raise ValueError(op)
+
+
+class Workload:
+    """Buffer pool plus prepared raw C-ABI calls for one shape."""
+
+    def __init__(self, op, rows, cols, seed, outliers=False,
+                 l2_bytes=126 << 20, max_pool_bytes=16 << 30, data=None):
+        import torch
+        self.op, self.rows, self.cols = op, rows, cols
+        d = data if data is not None else inputs.make(op, rows, cols, seed,
+                                                      outliers=outliers)
+        self.host = d
+        self.eps = float(d.get("eps", 0.0))
+        self.mean = op == "cross_entropy"
+        self.h_out = op == "residual_layernorm"
+        self.bytes = algorithmic_bytes(op, rows, cols, self.h_out, self.mean)
+        params = {k: torch.from_numpy(d[k]).cuda() for k in
+                  ("weight", "gamma", "beta") if k in d}
+        set_bytes = max(self.bytes, 1)
+        n = max(1, math.ceil(4 * l2_bytes / set_bytes))
+        n = max(1, min(n, max_pool_bytes // set_bytes, MAX_SETS))
+        x0 = torch.from_numpy(d["x"]).cuda()
+        self.sets = []
+        for _ in range(n):
+            s = dict(params)
+            s["x"] = x0.clone()
+            if "residual" in d:
+                s["residual"] = torch.from_numpy(d["residual"]).cuda()
+            if "labels" in d:
+                s["labels"] = torch.from_numpy(d["labels"]).cuda()
+            if op in ("rmsnorm", "layernorm", "softmax",
+                      "residual_layernorm"):
+                s["y"] = torch.empty_like(x0)
+            if self.h_out:
+                s["h_out"] = torch.empty_like(x0)
+            if op == "row_sum":
+                s["out"] = torch.empty(rows, device="cuda")
+            if op == "cross_entropy":
+                s["loss"] = torch.empty(rows, device="cuda")
+                s["mean_loss"] = torch.empty(1, device="cuda")
+            self.sets.append(s)
+        del x0
+        self.pool_bytes = n * set_bytes
+        self.l2_resident = self.pool_bytes < 4 * l2_bytes
+        self.launches_per_step = 2 if self.mean else 1
+
+    def outputs(self, i=0):
+        s = self.sets[i % len(self.sets)]
+        return {k: s[k] for k in ("y", "h_out", "out", "loss", "mean_loss")
+                if k in s}
+
+    def call_fn(self, i, stream_handle, plan=None):
+        """A zero-argument callable issuing step i's C-ABI call (the plain
+        entry point, or the *_with_plan one when `plan` is given)."""
+        L = B.lib()
+        s = self.sets[i % len(self.sets)]
+
+        def P(k):
+            return s[k].data_ptr() if k in s else None
+        R, C, eps = self.rows, self.cols, ctypes.c_float(self.eps)
+        st = stream_handle
+        names = {"rmsnorm": (("x", "weight", "y"), True),
+                 "layernorm": (("x", "gamma", "beta", "y"), True),
+                 "residual_layernorm": (("x", "residual", "gamma", "beta",
+                                         "y", "h_out"), True),
+                 "softmax": (("x", "y"), False),
+                 "row_sum": (("x", "out"), False),
+                 "cross_entropy": (("x", "labels", "loss", "mean_loss"),
+                                   False)}
+        keys, has_eps = names[self.op]
+        args = [P(k) for k in keys] + [R, C] + ([eps] if has_eps else [])
+        args.append(st)
+        fname = f"mt_{self.op}_f32"
+        if plan is not None:
+            fname += "_with_plan"
+            self._plan_ref = plan if isinstance(plan, B.MtPlan) else \
+                B.MtPlan(**plan)
+            args.append(ctypes.byref(self._plan_ref))
+        f = getattr(L, fname)
+        args = tuple(args)
+
+        def go():
+            rc = f(*args)
+            if rc != 0:
+                raise B.MTError(rc, fname)
+        return go
+
+
+def _graph_of(work, count, stream, plan=None):
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        h = torch.cuda.current_stream().cuda_stream
+        for i in range(count):
+            work.call_fn(i, h, plan)()
+    return g
+
+
+def graph_size(work, per_graph=64):
+    n = len(work.sets)
+    return n * max(1, math.ceil(per_graph / n))
+
+
+def time_graph_steps(work, steps, warmup, plan=None, per_graph=64,
+                     barrier=None, sampler=None):
+    """Device seconds for exactly `steps` steps (after `warmup` steps),
+    replayed from CUDA graphs.  `sampler` (a context manager) runs around
+    the timed region; `barrier` is called before and after it."""
+    import torch
+    stream = torch.cuda.Stream()
+    h = stream.cuda_stream
+    with torch.cuda.stream(stream):
+        for i in range(3):              # fill the library's per-device caches
+            work.call_fn(i, h, plan)()
+    stream.synchronize()
+    G = min(graph_size(work, per_graph), max(1, steps))
+    full = _graph_of(work, G, stream, plan)
+    rem = steps % G
+    tail = _graph_of(work, rem, stream, plan) if rem else None
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, math.ceil(warmup / G))):
+            full.replay()
+    stream.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    ctx = sampler if sampler is not None else _Null()
+    with ctx:
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for _ in range(steps // G):
+                full.replay()
+            if tail is not None:
+                tail.replay()
+            end.record(stream)
+        end.synchronize()
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    return start.elapsed_time(end) / 1e3
+
+
+def time_rounds(work, plan=None, rounds=5, min_round_s=0.01, per_graph=64):
+    """Per-round µs/op of `rounds` timed rounds (graph replays), each at
+    least `min_round_s` long; returns the list."""
+    import torch
+    stream = torch.cuda.Stream()
+    h = stream.cuda_stream
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            work.call_fn(i, h, plan)()
+    stream.synchronize()
+    G = graph_size(work, per_graph)
+    g = _graph_of(work, G, stream, plan)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        g.replay()
+        start.record(stream)
+        g.replay()
+        end.record(stream)
+    end.synchronize()
+    one = max(start.elapsed_time(end) / 1e3, 1e-6)
+    reps = max(1, math.ceil(min_round_s / one))
+    out = []
+    for _ in range(rounds):
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for _ in range(reps):
+                g.replay()
+            end.record(stream)
+        end.synchronize()
+        out.append(start.elapsed_time(end) * 1e3 / (reps * G))
+    del g
+    return out
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+def time_plain_steps(work, steps, warmup):
+    """The same steps, each launched from Python (host launch cost in)."""
+    import torch
+    stream = torch.cuda.Stream()
+    h = stream.cuda_stream
+    fns = [work.call_fn(i, h) for i in range(len(work.sets))]
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            fns[i % len(fns)]()
+    stream.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for i in range(steps):
+            fns[i % len(fns)]()
+        end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / 1e3
+
+
+def time_e2e(work, steps, warmup):
+    """Each step copies x from pinned host memory, calls the library and
+    copies the result back to pinned host memory.  Returns (seconds,
+    host-to-device bytes per step, device-to-host bytes per step)."""
+    import torch
+    s0 = work.sets[0]
+    x_host = torch.from_numpy(work.host["x"]).pin_memory()
+    out_key = {"row_sum": "out", "cross_entropy": "loss"}.get(work.op, "y")
+    out_host = torch.empty(s0[out_key].shape, dtype=s0[out_key].dtype,
+                           pin_memory=True)
+    stream = torch.cuda.Stream()
+    fn = work.call_fn(0, stream.cuda_stream)
+
+    def step():
+        s0["x"].copy_(x_host, non_blocking=True)
+        fn()
+        out_host.copy_(s0[out_key], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step()
+    stream.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(steps):
+            step()
+        end.record(stream)
+    end.synchronize()
+    return (start.elapsed_time(end) / 1e3, x_host.numel() * 4,
+            out_host.numel() * 4)
