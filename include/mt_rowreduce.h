@@ -117,6 +117,10 @@ typedef struct mt_plan {
  * kernel's completion (and memory visibility) before it reads or writes any
  * operand, so results are the same as with an ordinary launch. */
 #define MT_PLAN_PDL 1
+/* Plan flag: when the grid is smaller than the number of row groups (CTAs
+ * loop over row groups), each CTA asks L2 to prefetch its next row group
+ * while it processes the current one. */
+#define MT_PLAN_PREFETCH_NEXT 2
 
 /* ---- operators ---------------------------------------------------------
  * Each takes its plan from the built-in, measured plan table

@@ -37,6 +37,7 @@ MT_PATH_REGISTERS = 0
 MT_PATH_LOOP = 1
 
 MT_PLAN_PDL = 1
+MT_PLAN_PREFETCH_NEXT = 2
 
 # Symbols declared in include/mt_rowreduce.h.
 EXPORTS = (

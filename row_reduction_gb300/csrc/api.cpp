@@ -133,6 +133,7 @@ mt_status dispatch(int op, KArgs a, const VecPtrs &vp,
     a.log2W = l;
     a.B = p.rows_per_block;
     a.pdl = (p.flags & MT_PLAN_PDL) ? 1 : 0;
+    a.prefetch_next = (p.flags & MT_PLAN_PREFETCH_NEXT) ? 1 : 0;
 
     const int64_t ngroups = (a.rows + a.B - 1) / a.B;
     int64_t grid = p.grid;

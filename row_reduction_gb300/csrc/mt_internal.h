@@ -41,6 +41,8 @@ struct KArgs {
     // Launched as a programmatic dependent: prefetch the first row group
     // into L2 before waiting on the previous grid.
     int32_t pdl;
+    // Persistent CTAs prefetch their next row group into L2.
+    int32_t prefetch_next;
 };
 
 // Instantiated register-path chunk counts.

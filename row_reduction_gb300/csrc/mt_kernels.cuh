@@ -293,6 +293,22 @@ __device__ __forceinline__ void prefetch_l2(const void *p, int64_t bytes) {
     }
 }
 
+// Persistent CTAs: with `prefetch_next`, thread 0 asks L2 for the row group
+// the CTA will process after `g`, so its DRAM reads overlap this one.
+template <int OP>
+__device__ __forceinline__ void prefetch_next_group(const KArgs &a,
+                                                    int64_t g,
+                                                    int64_t ngroups) {
+    const int64_t gn = g + gridDim.x;
+    if (!a.prefetch_next || threadIdx.x != 0 || gn >= ngroups) return;
+    const int64_t r0 = gn * a.B;
+    const int64_t nr = a.rows - r0 < a.B ? a.rows - r0 : a.B;
+    const int64_t bytes = nr * (int64_t)a.cols * 4;
+    prefetch_l2(a.x + r0 * a.cols, bytes);
+    if constexpr (OP == OP_RESIDUAL_LAYERNORM)
+        prefetch_l2(a.res + r0 * a.cols, bytes);
+}
+
 // Kernel prologue: with `pdl`, thread 0 prefetches the CTA's first row group
 // (x and, for residual LayerNorm, the residual) into L2; then every thread
 // lets dependents launch and waits for the previous grid.
@@ -334,12 +350,20 @@ struct RowGeom {
 
 // Loads V consecutive values at body offset `off` of a row (`p` = row
 // start + head): a vector access for a complete pack when `vec`, otherwise
-// guarded scalars; missing values read as `fill`.
-template <int V>
+// guarded scalars; missing values read as `fill`.  In aligned kernels
+// (AL) cols % V == 0, so a pack is either complete or wholly past the end.
+template <int V, bool AL>
 __device__ __forceinline__ void load_pack(const float *p, int off, int nb,
                                           bool active, bool vec, float fill,
                                           float *d) {
-    if (active && off + V <= nb) {
+    if constexpr (AL) {
+        if (active && off < nb) {
+            ld_vec<V>(p + off, d);
+        } else {
+#pragma unroll
+            for (int e = 0; e < V; ++e) d[e] = fill;
+        }
+    } else if (active && off + V <= nb) {
         if (vec) {
             ld_vec<V>(p + off, d);
         } else {
@@ -353,12 +377,14 @@ __device__ __forceinline__ void load_pack(const float *p, int off, int nb,
     }
 }
 
-template <int V>
+template <int V, bool AL>
 __device__ __forceinline__ void store_pack(float *p, int off, int nb,
                                            bool active, bool vec,
                                            const float *d) {
     if (!active) return;
-    if (off + V <= nb) {
+    if constexpr (AL) {
+        if (off < nb) st_vec<V>(p + off, d);
+    } else if (off + V <= nb) {
         if (vec) {
             st_vec<V>(p + off, d);
         } else {
@@ -369,6 +395,25 @@ __device__ __forceinline__ void store_pack(float *p, int off, int nb,
 #pragma unroll
         for (int e = 0; e < V; ++e)
             if (off + e < nb) p[off + e] = d[e];
+    }
+}
+
+// Parameter pack for the register path: aligned kernels read complete
+// vectors (or nothing past the end), the others guard each element.
+template <int V, bool AL>
+__device__ __forceinline__ void param_row_pack(const float *p, int col,
+                                               int off, int nb, bool active,
+                                               float dflt, float *d) {
+    if constexpr (AL) {
+        if (p != nullptr && active && off < nb) {
+            ldg_vec<V>(p + col, d);
+        } else {
+#pragma unroll
+            for (int e = 0; e < V; ++e) d[e] = dflt;
+        }
+    } else {
+        const int nv = active ? min(max(nb - off, 0), V) : 0;
+        param_pack<V>(p, col, nv, false, dflt, d);
     }
 }
 
@@ -392,6 +437,7 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
     const bool yvec = AL || a.y_vec;
 
     for (int64_t g = blockIdx.x; g < ngroups; g += gridDim.x) {
+        prefetch_next_group<OP>(a, g, ngroups);
         const int64_t row = g * a.B + slot;
         const bool active = row < a.rows;
         const RowGeom<V, AL> geo(a.x, active ? row : 0, cols);
@@ -404,7 +450,7 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
         float hv = fill;
 #pragma unroll
         for (int k = 0; k < K; ++k)
-            load_pack<V>(xb, (k * W + worker) * V, nb, active, true, fill,
+            load_pack<V, AL>(xb, (k * W + worker) * V, nb, active, true, fill,
                          v[k]);
         if (head) hv = a.x[geo.base + worker];
 
@@ -414,7 +460,7 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
 #pragma unroll
             for (int k = 0; k < K; ++k) {
                 float t[V];
-                load_pack<V>(rb, (k * W + worker) * V, nb, active, rvec, 0.f,
+                load_pack<V, AL>(rb, (k * W + worker) * V, nb, active, rvec, 0.f,
                              t);
 #pragma unroll
                 for (int e = 0; e < V; ++e) v[k][e] = __fadd_rn(v[k][e], t[e]);
@@ -425,7 +471,7 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
                 const bool hvec = AL || a.h_vec;
 #pragma unroll
                 for (int k = 0; k < K; ++k)
-                    store_pack<V>(hb, (k * W + worker) * V, nb, active, hvec,
+                    store_pack<V, AL>(hb, (k * W + worker) * V, nb, active, hvec,
                                   v[k]);
                 if (head) a.h[geo.base + worker] = hv;
             }
@@ -460,11 +506,11 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
             for (int k = 0; k < K; ++k) {
                 const int off = (k * W + worker) * V;
                 float wv[V], o[V];
-                const int nv = active ? min(max(nb - off, 0), V) : 0;
-                param_pack<V>(a.w, geo.hd + off, nv, AL, 1.f, wv);
+                param_row_pack<V, AL>(a.w, geo.hd + off, off, nb, active, 1.f,
+                                      wv);
 #pragma unroll
                 for (int e = 0; e < V; ++e) o[e] = v[k][e] * r * wv[e];
-                store_pack<V>(yb, off, nb, active, yvec, o);
+                store_pack<V, AL>(yb, off, nb, active, yvec, o);
             }
             if (head) {
                 const float wh = a.w ? __ldg(a.w + worker) : 1.f;
@@ -509,13 +555,14 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
             for (int k = 0; k < K; ++k) {
                 const int off = (k * W + worker) * V;
                 float gv[V], bv[V], o[V];
-                const int nv = active ? min(max(nb - off, 0), V) : 0;
-                param_pack<V>(a.w, geo.hd + off, nv, AL, 1.f, gv);
-                param_pack<V>(a.b, geo.hd + off, nv, AL, 0.f, bv);
+                param_row_pack<V, AL>(a.w, geo.hd + off, off, nb, active, 1.f,
+                                      gv);
+                param_row_pack<V, AL>(a.b, geo.hd + off, off, nb, active, 0.f,
+                                      bv);
 #pragma unroll
                 for (int e = 0; e < V; ++e)
                     o[e] = fmaf((v[k][e] - mean) * rstd, gv[e], bv[e]);
-                store_pack<V>(yb, off, nb, active, yvec, o);
+                store_pack<V, AL>(yb, off, nb, active, yvec, o);
             }
             if (head) {
                 const float gh = a.w ? __ldg(a.w + worker) : 1.f;
@@ -559,7 +606,7 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
                 float o[V];
 #pragma unroll
                 for (int e = 0; e < V; ++e) o[e] = v[k][e] * inv;
-                store_pack<V>(yb, (k * W + worker) * V, nb, active, yvec, o);
+                store_pack<V, AL>(yb, (k * W + worker) * V, nb, active, yvec, o);
             }
             if (head) a.y[geo.base + worker] = hv * inv;
         } else if constexpr (OP == OP_ROW_SUM) {
@@ -652,6 +699,7 @@ __global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
     const bool yvec = AL || a.y_vec;
 
     for (int64_t g = blockIdx.x; g < ngroups; g += gridDim.x) {
+        prefetch_next_group<OP>(a, g, ngroups);
         const int64_t row = g * a.B + slot;
         const bool active = row < a.rows;
         const RowGeom<V, AL> geo(a.x, active ? row : 0, cols);
@@ -713,7 +761,7 @@ __global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
                     param_pack<V>(a.w, hd + off, nv, AL, 1.f, wv);
 #pragma unroll
                     for (int e = 0; e < V; ++e) o[e] = t[e] * r * wv[e];
-                    store_pack<V>(yb, off, nb, true, yvec, o);
+                    store_pack<V, AL>(yb, off, nb, true, yvec, o);
                 });
         } else if constexpr (OP == OP_LAYERNORM ||
                              OP == OP_RESIDUAL_LAYERNORM) {
@@ -758,9 +806,9 @@ __global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
 #pragma unroll
                     for (int e = 0; e < V; ++e)
                         o[e] = fmaf((t[e] - mean) * rstd, gv[e], bv[e]);
-                    store_pack<V>(yb, off, nb, true, yvec, o);
+                    store_pack<V, AL>(yb, off, nb, true, yvec, o);
                     if (OP == OP_RESIDUAL_LAYERNORM && hb)
-                        store_pack<V>(hb, off, nb, true, hvec, t);
+                        store_pack<V, AL>(hb, off, nb, true, hvec, t);
                 });
         } else if constexpr (OP == OP_SOFTMAX || OP == OP_CROSS_ENTROPY) {
             float m = -INFINITY, s = 0.f;
@@ -790,7 +838,7 @@ __global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
                         float o[V];
 #pragma unroll
                         for (int e = 0; e < V; ++e) o[e] = expf(t[e] - m) * inv;
-                        store_pack<V>(yb, off, nb, true, yvec, o);
+                        store_pack<V, AL>(yb, off, nb, true, yvec, o);
                     });
             } else {
                 if (active && worker == 0) {

@@ -87,7 +87,8 @@ mt_status plan_check(int op, int64_t cols, const mt_plan_t &p) {
     if (V > 1 && W < V) return MT_ERR_INVALID_ARGUMENT;
     if (B < 1 || B > 1024) return MT_ERR_INVALID_ARGUMENT;
     if (p.grid < 0) return MT_ERR_INVALID_ARGUMENT;
-    if (p.flags & ~MT_PLAN_PDL) return MT_ERR_INVALID_ARGUMENT;
+    if (p.flags & ~(MT_PLAN_PDL | MT_PLAN_PREFETCH_NEXT))
+        return MT_ERR_INVALID_ARGUMENT;
     const int64_t threads = W * B;
     if (threads % 32 != 0) return MT_ERR_INVALID_ARGUMENT;
     if (p.path == MT_PATH_REGISTERS) {
@@ -158,11 +159,13 @@ size_t mt_describe_plan(const mt_plan_t *p, char *buf, size_t n) {
                                                         : "invalid";
         len = snprintf(tmp, sizeof(tmp),
                        "path=%s W=%d V=%d chunks=%d rows_per_block=%d "
-                       "threads=%d grid=%s%s",
+                       "threads=%d grid=%s%s%s",
                        path, p->threads_per_row, p->values_per_thread,
                        p->chunks, p->rows_per_block,
                        p->threads_per_row * p->rows_per_block, grid,
-                       (p->flags & MT_PLAN_PDL) ? " pdl" : "");
+                       (p->flags & MT_PLAN_PDL) ? " pdl" : "",
+                       (p->flags & MT_PLAN_PREFETCH_NEXT) ? " prefetch_next"
+                                                          : "");
     }
     if (len < 0) len = 0;
     if (buf != nullptr && n > 0) {

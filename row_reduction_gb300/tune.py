@@ -38,6 +38,7 @@ from . import inputs
 from .timing import Workload, time_rounds
 
 CHUNKS = (1, 2, 4, 8, 16)
+FLAG_SETS = (B.MT_PLAN_PDL, B.MT_PLAN_PDL | B.MT_PLAN_PREFETCH_NEXT, 0)
 
 
 def pow2ceil(v):
@@ -62,7 +63,7 @@ def candidates(op, rows, cols):
                     Bk = threads // W
                     if Bk > 1 and Bk > pow2ceil(rows):
                         continue
-                    for fl in (B.MT_PLAN_PDL, 0):
+                    for fl in FLAG_SETS:
                         if K is not None:
                             out.append(B.make_plan(W, V, K, Bk, flags=fl))
                         if cols >= 8192:
