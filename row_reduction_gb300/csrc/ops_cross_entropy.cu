@@ -12,6 +12,10 @@ namespace mt {
 // depend on timing (no atomics).
 __global__ void __launch_bounds__(1024)
     mean_kernel(const float *loss, float *mean, int64_t rows) {
+    // Launched as a programmatic dependent of the loss kernel: wait until
+    // that grid has completed and its losses are visible.
+    grid_wait_prerequisites();
+    grid_launch_dependents();
     __shared__ RedScratch red;
     int parity = 0;
     float s = 0.f, c = 0.f;
@@ -28,8 +32,18 @@ __global__ void __launch_bounds__(1024)
 
 cudaError_t launch_mean(const float *loss, float *mean, int64_t rows,
                         cudaStream_t stream) {
-    mean_kernel<<<1, 1024, 0, stream>>>(loss, mean, rows);
-    return cudaGetLastError();
+    // Programmatic dependent launch lets this one-CTA kernel start while the
+    // loss kernel finishes; it waits for that grid before reading.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(1024);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, mean_kernel, loss, mean, rows);
 }
 
 }  // namespace mt
