@@ -64,18 +64,22 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_sources_sha():
+def kernel_sources_sha(op="rmsnorm", plan=None):
+    """Hash of what defines one operator's kernel: the kernel templates, the
+    launch code, that operator's translation unit and its plan."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "row_reduction_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in ("mt_kernels.cuh", "mt_internal.h", "api.cpp",
+                 f"ops_{op}.cu"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + b"\0" + f.read())
+    h.update((plan or "").encode())
     return h.hexdigest()
 
 
-def profiled_traffic(workload_key):
+def profiled_traffic(workload_key, op, plan):
     """DRAM bytes per launch from the committed ncu summary of this
-    workload, if it was taken on the current kernel sources."""
+    workload, if it was taken on the current kernel code and plan."""
     path = os.path.join(ROOT, "profiles", f"{workload_key}.ncu.txt")
     if not os.path.exists(path):
         return None
@@ -84,7 +88,7 @@ def profiled_traffic(workload_key):
         if ":" in line:
             k, v = line.split(":", 1)
             fields[k.strip()] = v.strip()
-    if fields.get("kernel_sources_sha256") != kernel_sources_sha():
+    if fields.get("kernel_sources_sha256") != kernel_sources_sha(op, plan):
         return None
     try:
         return int(fields["dram_bytes_per_launch"])
@@ -251,7 +255,8 @@ def run_ours(args, rank, world, local_rank):
     achieved = work.bytes / per_step / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak,
                 "unit": "GB/s", "frac": achieved / peak,
-                "traffic": profiled_traffic(key),
+                "traffic": profiled_traffic(
+                    key, args.op, plan_text(args.op, args.rows, args.cols)),
                 "peak_source": f"{peak_kind} HBM copy bandwidth "
                                "(MEASURED_PEAKS.json hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s"}
