@@ -50,6 +50,21 @@ FALLBACK_HBM_GBS = 6800.0
 
 
 # ---------------------------------------------------------------- helpers
+def max_over_ranks(elapsed, device):
+    """The slowest rank's elapsed seconds (all ranks get the same value)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([elapsed], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(bytes_per_step, steps, elapsed, world):
+    """Whole-job GB/s: every rank moves bytes_per_step per step (replicas,
+    weak scaling); time is the slowest rank's."""
+    return world * bytes_per_step * steps / elapsed / 1e9
+
+
 def plan_text(op, rows, cols):
     import row_reduction_gb300 as mt
     return mt.mt_describe_plan(mt.mt_plan_query(op, rows, cols))
@@ -242,11 +257,9 @@ def run_ours(args, rank, world, local_rank):
     elapsed = time_graph_steps(work, args.steps, args.warmup,
                                barrier=barrier, sampler=sampler)
     if world > 1:
-        t = torch.tensor([elapsed], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
+        elapsed = max_over_ranks(elapsed, "cuda")
     per_step = elapsed / args.steps
-    value = world * work.bytes * args.steps / elapsed / 1e9
+    value = job_value(work.bytes, args.steps, elapsed, world)
     if rank != 0:
         return 0
 
