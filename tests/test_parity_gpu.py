@@ -361,3 +361,79 @@ def test_forced_plan_errors_on_gpu():
     for g in (1, 3, 1000):
         y = mt.rmsnorm(x + 1, plan=mt.make_plan(256, 4, 4, 1, grid=g))
         assert torch.allclose(y, torch.ones_like(y), rtol=1e-5)
+
+
+# ------------------------------------------- cross-entropy mean paths
+def _ce_case(rows, cols, seed):
+    d = inputs.make("cross_entropy", rows, cols, seed)
+    t = to_dev(d)
+    _, ref_mean = oracle.cross_entropy(d["x"], d["labels"])
+    return d, t, ref_mean
+
+
+def test_cross_entropy_mean_over_many_rows_and_grids():
+    """The mean kernel sums per-row losses in a fixed order; the result
+    matches the oracle whatever grid the loss kernel used, and the losses
+    do not depend on the grid."""
+    rows, cols = 70000, 33
+    d, t, ref_mean = _ce_case(rows, cols, SEED + 5)
+    ref_loss = oracle.cross_entropy(d["x"], d["labels"])[0]
+    base = None
+    for grid in (0, 1, 7, 8000, 20000):
+        p = mt.make_plan(64, 1, 1, 1, grid=grid, flags=mt.MT_PLAN_PDL)
+        loss, m = mt.cross_entropy(t["x"], t["labels"], plan=p)
+        if base is None:
+            base = loss
+            assert_close(loss.cpu().numpy(), ref_loss, "losses")
+        assert torch.equal(loss, base)
+        assert_close(m.cpu().numpy(), np.array([ref_mean]), f"grid {grid}")
+
+
+def test_cross_entropy_mean_under_graph_capture():
+    """The loss kernel and the dependent mean kernel captured into a CUDA
+    graph, with and without an eager call on the stream first, replay
+    correctly many times."""
+    rows, cols = 1024, 4096
+    d, t, ref_mean = _ce_case(rows, cols, SEED + 6)
+    loss = torch.empty(rows, device="cuda")
+    for warm in (False, True):
+        s = torch.cuda.Stream()
+        means = torch.full((8,), float("nan"), device="cuda")
+        if warm:
+            with torch.cuda.stream(s):
+                mt.mt_cross_entropy_f32(t["x"], t["labels"], loss,
+                                        means[0:1], rows, cols, s)
+            s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            mt.mt_cross_entropy_f32(t["x"], t["labels"], loss, means[1:2],
+                                    rows, cols,
+                                    torch.cuda.current_stream())
+        for i in range(5):
+            means[1] = float("nan")
+            g.replay()
+            torch.cuda.synchronize()
+            assert_close(means[1:2].cpu().numpy(), np.array([ref_mean]),
+                         f"graph replay {i} (warm={warm})")
+
+
+def test_cross_entropy_mean_on_concurrent_streams():
+    rows, cols = 4096, 1000
+    cases = [_ce_case(rows, cols, SEED + 7 + k) for k in range(2)]
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    outs = [(torch.empty(rows, device="cuda"),
+             torch.empty(20, device="cuda")) for _ in range(2)]
+    torch.cuda.synchronize()
+    for i in range(20):
+        for k in range(2):
+            _, t, _ = cases[k]
+            with torch.cuda.stream(streams[k]):
+                mt.mt_cross_entropy_f32(t["x"], t["labels"], outs[k][0],
+                                        outs[k][1][i:i + 1], rows, cols,
+                                        streams[k])
+    torch.cuda.synchronize()
+    for k in range(2):
+        ref_mean = cases[k][2]
+        got = outs[k][1].cpu().numpy()
+        assert_close(got, np.full(20, ref_mean), f"stream {k}")
+        assert len(set(got.tolist())) == 1     # deterministic per stream
