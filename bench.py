@@ -85,7 +85,7 @@ def kernel_sources_sha(op="rmsnorm", plan=None):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "row_reduction_gb300", "csrc")
     for name in ("mt_kernels.cuh", "mt_internal.h", "api.cpp",
-                 f"ops_{op}.cu"):
+                 f"ops_{op}_f32.cu"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + b"\0" + f.read())
     h.update((plan or "").encode())

@@ -19,18 +19,20 @@
  *            cols FP32 values; per-row outputs hold rows FP32 values; labels
  *            hold rows int32 values.
  * Memory     every data pointer is a DEVICE pointer owned by the caller and
- *            must be at least 4-byte aligned.  Calls allocate no device
+ *            must be aligned to its element size (4 bytes for FP32, labels
+ *            and per-row outputs; 2 bytes for FP16/BF16).  Calls allocate no device
  *            memory and never synchronise the host; work is enqueued on
  *            `stream` (NULL = the legacy default stream) on the current
  *            device, and device-side faults surface at the caller's next
- *            synchronisation.  16-byte aligned pointers and cols % 4 == 0 get
- *            the fully vectorised path; other alignments are handled by a
- *            per-row scalar head before the vector body.
+ *            synchronisation.  16-byte aligned pointers and cols a multiple
+ *            of V get the fully vectorised path; other alignments are
+ *            handled by a per-row scalar head before the vector body.
  * Aliasing   y == x (in place) is allowed; so are h_out == x and
  *            h_out == residual.  Any other (partial) overlap between an
  *            output and an input is undefined.
  * Errors     arguments are checked before anything is enqueued: a NULL
- *            required pointer, a pointer that is not 4-byte aligned,
+ *            required pointer (rows > 0), a pointer not aligned to its
+ *            element size,
  *            rows < 0, cols < 1, cols > INT32_MAX or rows*cols overflowing
  *            int64 give MT_ERR_INVALID_ARGUMENT and enqueue nothing.
  *            rows == 0 returns MT_OK without a launch (outputs untouched).
@@ -80,6 +82,19 @@ typedef enum mt_op {
     MT_OP_CROSS_ENTROPY = 5
 } mt_op;
 
+/* Storage type of the matrices and parameter vectors of a call.  All
+ * arithmetic is FP32 whatever the storage type; per-row outputs (row sums,
+ * losses, the mean) are FP32 for every type. */
+typedef enum mt_dtype {
+    MT_DTYPE_F32 = 0,
+    MT_DTYPE_F16 = 1,  /* IEEE binary16 */
+    MT_DTYPE_BF16 = 2  /* bfloat16: the upper 16 bits of an FP32 */
+} mt_dtype;
+
+/* 16-bit storage, passed by bit pattern. */
+typedef uint16_t mt_f16_t;
+typedef uint16_t mt_bf16_t;
+
 typedef enum mt_path {
     /* The whole row is read once into registers (V*chunks values per
      * thread) and written from them. */
@@ -98,7 +113,9 @@ typedef enum mt_path {
  * §Implementation and semantics.) */
 typedef struct mt_plan {
     int32_t threads_per_row;   /* W: power of two, 1..1024 */
-    int32_t values_per_thread; /* V: 1, 2 or 4 (V=4: one 16-byte access) */
+    int32_t values_per_thread; /* V: FP32 1, 2 or 4; FP16/BF16 2, 4 or 8
+                                  (V*element size = 16 is one 16-byte
+                                  access) */
     int32_t chunks;            /* register path: chunks held per thread, one
                                   of 1, 2, 4, 8, 16; W*V*chunks >= cols.
                                   Loop path: ignored (set 0). */
@@ -193,6 +210,66 @@ MT_API mt_status mt_cross_entropy_f32_with_plan(const float *logits,
                                          int64_t cols, mt_stream_t stream,
                                          const mt_plan_t *plan);
 
+/* ---- FP16 / BF16 storage ------------------------------------------------
+ * Same operators with 16-bit matrices and parameter vectors: every value is
+ * widened to FP32 on load, all statistics and the epilogue (including the
+ * weight / gamma / beta multiply-add) are FP32, and the result is rounded to
+ * the storage type once, at the store (round to nearest even).  Residual
+ * LayerNorm normalises the FP32 sum x + r and stores h_out = round(x + r).
+ * Row sums, losses and the mean stay FP32.  Pointers must be 2-byte
+ * aligned; everything else is as for the FP32 calls. */
+MT_API mt_status mt_rmsnorm_f16(const mt_f16_t *x, const mt_f16_t *weight,
+                                mt_f16_t *y, int64_t rows, int64_t cols,
+                                float eps, mt_stream_t stream);
+MT_API mt_status mt_rmsnorm_bf16(const mt_bf16_t *x, const mt_bf16_t *weight,
+                                 mt_bf16_t *y, int64_t rows, int64_t cols,
+                                 float eps, mt_stream_t stream);
+MT_API mt_status mt_layernorm_f16(const mt_f16_t *x, const mt_f16_t *gamma,
+                                  const mt_f16_t *beta, mt_f16_t *y,
+                                  int64_t rows, int64_t cols, float eps,
+                                  mt_stream_t stream);
+MT_API mt_status mt_layernorm_bf16(const mt_bf16_t *x, const mt_bf16_t *gamma,
+                                   const mt_bf16_t *beta, mt_bf16_t *y,
+                                   int64_t rows, int64_t cols, float eps,
+                                   mt_stream_t stream);
+MT_API mt_status mt_residual_layernorm_f16(
+    const mt_f16_t *x, const mt_f16_t *residual, const mt_f16_t *gamma,
+    const mt_f16_t *beta, mt_f16_t *y, mt_f16_t *h_out, int64_t rows,
+    int64_t cols, float eps, mt_stream_t stream);
+MT_API mt_status mt_residual_layernorm_bf16(
+    const mt_bf16_t *x, const mt_bf16_t *residual, const mt_bf16_t *gamma,
+    const mt_bf16_t *beta, mt_bf16_t *y, mt_bf16_t *h_out, int64_t rows,
+    int64_t cols, float eps, mt_stream_t stream);
+MT_API mt_status mt_softmax_f16(const mt_f16_t *x, mt_f16_t *y, int64_t rows,
+                                int64_t cols, mt_stream_t stream);
+MT_API mt_status mt_softmax_bf16(const mt_bf16_t *x, mt_bf16_t *y,
+                                 int64_t rows, int64_t cols,
+                                 mt_stream_t stream);
+MT_API mt_status mt_row_sum_f16(const mt_f16_t *x, float *out, int64_t rows,
+                                int64_t cols, mt_stream_t stream);
+MT_API mt_status mt_row_sum_bf16(const mt_bf16_t *x, float *out, int64_t rows,
+                                 int64_t cols, mt_stream_t stream);
+MT_API mt_status mt_cross_entropy_f16(const mt_f16_t *logits,
+                                      const int32_t *labels, float *loss,
+                                      float *mean_loss, int64_t rows,
+                                      int64_t cols, mt_stream_t stream);
+MT_API mt_status mt_cross_entropy_bf16(const mt_bf16_t *logits,
+                                       const int32_t *labels, float *loss,
+                                       float *mean_loss, int64_t rows,
+                                       int64_t cols, mt_stream_t stream);
+
+/* Any operator and storage type with an explicit plan (NULL = the table's
+ * plan).  Pointer arguments follow the typed calls above; pointers an
+ * operator does not use must be NULL: x, weight (gamma), beta, residual, y,
+ * h_out are of `dtype`; out (row sums / losses) and mean_loss are FP32;
+ * labels are int32.  eps is ignored by softmax, row sum and
+ * cross-entropy. */
+MT_API mt_status mt_row_reduce_with_plan(
+    int op, int dtype, const void *x, const void *residual,
+    const void *weight, const void *beta, const int32_t *labels, void *y,
+    void *h_out, float *out, float *mean_loss, int64_t rows, int64_t cols,
+    float eps, mt_stream_t stream, const mt_plan_t *plan);
+
 /* ---- planning and introspection (host only; no CUDA call) ------------- */
 
 /* The plan the operators use for (op, rows, cols): a lookup in the table of
@@ -204,6 +281,13 @@ MT_API mt_status mt_plan_query(int op, int64_t rows, int64_t cols, mt_plan_t *ou
 /* Legality of a plan for (op, cols) without launching anything: MT_OK, or
  * the error the *_with_plan call would return. */
 MT_API mt_status mt_plan_check(int op, int64_t cols, const mt_plan_t *plan);
+
+/* The same two calls for any storage type (mt_dtype); the plain forms above
+ * are MT_DTYPE_F32.  An unknown dtype gives MT_ERR_INVALID_ARGUMENT. */
+MT_API mt_status mt_plan_query_dtype(int op, int dtype, int64_t rows,
+                                     int64_t cols, mt_plan_t *out);
+MT_API mt_status mt_plan_check_dtype(int op, int dtype, int64_t cols,
+                                     const mt_plan_t *plan);
 
 /* Private-slot bound of the consecutive-worker map: the most values any one
  * of W workers owns in a row of n elements with V consecutive values per

@@ -14,7 +14,13 @@ from ._binding import (  # noqa: F401
     MT_ERR_OUT_OF_RESOURCES, MT_ERR_UNSUPPORTED, MT_OK, MT_OP_CROSS_ENTROPY,
     MT_OP_LAYERNORM, MT_OP_RESIDUAL_LAYERNORM, MT_OP_RMSNORM, MT_OP_ROW_SUM,
     MT_OP_SOFTMAX, MT_PATH_LOOP, MT_PATH_REGISTERS, MT_PLAN_PDL,
-    MT_PLAN_PREFETCH_NEXT, OP_IDS, MTError, MtPlan,
+    MT_PLAN_PREFETCH_NEXT, OP_IDS, DTYPE_IDS, MT_DTYPE_F32, MT_DTYPE_F16,
+    MT_DTYPE_BF16, MTError, MtPlan, dtype_of, mt_row_reduce_with_plan,
+    mt_plan_query_dtype, mt_plan_check_dtype, mt_rmsnorm_f16,
+    mt_rmsnorm_bf16, mt_layernorm_f16, mt_layernorm_bf16,
+    mt_residual_layernorm_f16, mt_residual_layernorm_bf16, mt_softmax_f16,
+    mt_softmax_bf16, mt_row_sum_f16, mt_row_sum_bf16, mt_cross_entropy_f16,
+    mt_cross_entropy_bf16,
     lib, make_plan, mt_cross_entropy_f32, mt_cross_entropy_f32_with_plan,
     mt_describe_plan, mt_last_cuda_error, mt_layernorm_f32,
     mt_layernorm_f32_with_plan, mt_plan_check, mt_plan_query,
@@ -32,11 +38,14 @@ def _shape(x):
 
 
 def rmsnorm(x, weight=None, eps=1e-6, out=None, plan=None, stream=None):
-    """y = x / sqrt(mean(x^2) + eps) * weight, per row (FP32, CUDA)."""
+    """y = x / sqrt(mean(x^2) + eps) * weight, per row.  x may be FP32, FP16
+    or BF16 (weight and y take x's type; arithmetic is FP32)."""
     import torch
     rows, cols = _shape(x)
     y = torch.empty_like(x) if out is None else out
-    mt_rmsnorm_f32_with_plan(x, weight, y, rows, cols, eps, stream, plan)
+    mt_row_reduce_with_plan("rmsnorm", dtype_of(x), x, weight=weight, y=y,
+                            rows=rows, cols=cols, eps=eps, stream=stream,
+                            plan=plan)
     return y
 
 
@@ -46,8 +55,9 @@ def layernorm(x, gamma=None, beta=None, eps=1e-5, out=None, plan=None,
     import torch
     rows, cols = _shape(x)
     y = torch.empty_like(x) if out is None else out
-    mt_layernorm_f32_with_plan(x, gamma, beta, y, rows, cols, eps, stream,
-                               plan)
+    mt_row_reduce_with_plan("layernorm", dtype_of(x), x, weight=gamma,
+                            beta=beta, y=y, rows=rows, cols=cols, eps=eps,
+                            stream=stream, plan=plan)
     return y
 
 
@@ -60,8 +70,10 @@ def residual_layernorm(x, residual, gamma=None, beta=None, eps=1e-5,
     y = torch.empty_like(x) if out is None else out
     if return_h and h_out is None:
         h_out = torch.empty_like(x)
-    mt_residual_layernorm_f32_with_plan(x, residual, gamma, beta, y, h_out,
-                                        rows, cols, eps, stream, plan)
+    mt_row_reduce_with_plan("residual_layernorm", dtype_of(x), x,
+                            residual=residual, weight=gamma, beta=beta, y=y,
+                            h_out=h_out, rows=rows, cols=cols, eps=eps,
+                            stream=stream, plan=plan)
     return (y, h_out) if return_h else y
 
 
@@ -70,33 +82,34 @@ def softmax(x, out=None, plan=None, stream=None):
     import torch
     rows, cols = _shape(x)
     y = torch.empty_like(x) if out is None else out
-    mt_softmax_f32_with_plan(x, y, rows, cols, stream, plan)
+    mt_row_reduce_with_plan("softmax", dtype_of(x), x, y=y, rows=rows,
+                            cols=cols, stream=stream, plan=plan)
     return y
 
 
 def row_sum(x, out=None, plan=None, stream=None):
-    """out[r] = sum of row r."""
+    """out[r] = sum of row r (FP32 for every input type)."""
     import torch
     rows, cols = _shape(x)
-    o = torch.empty(rows, dtype=x.dtype, device=x.device) if out is None \
-        else out
-    mt_row_sum_f32_with_plan(x, o, rows, cols, stream, plan)
+    o = torch.empty(rows, dtype=torch.float32, device=x.device) \
+        if out is None else out
+    mt_row_reduce_with_plan("row_sum", dtype_of(x), x, out=o, rows=rows,
+                            cols=cols, stream=stream, plan=plan)
     return o
 
 
 def cross_entropy(logits, labels, mean=True, plan=None, stream=None):
-    """Per-row loss logsumexp(row) - row[label] and, with mean, its mean.
-
-    Returns (loss, mean_loss) when mean is true (mean_loss a 1-element
-    tensor), else loss.
-    """
+    """Per-row loss logsumexp(row) - row[label] and, with mean, its mean
+    (both FP32).  Returns (loss, mean_loss) when mean is true (mean_loss a
+    1-element tensor), else loss."""
     import torch
     rows, cols = _shape(logits)
-    loss = torch.empty(rows, dtype=logits.dtype, device=logits.device)
-    m = torch.empty(1, dtype=logits.dtype, device=logits.device) if mean \
+    loss = torch.empty(rows, dtype=torch.float32, device=logits.device)
+    m = torch.empty(1, dtype=torch.float32, device=logits.device) if mean \
         else None
-    mt_cross_entropy_f32_with_plan(logits, labels, loss, m, rows, cols,
-                                   stream, plan)
+    mt_row_reduce_with_plan("cross_entropy", dtype_of(logits), logits,
+                            labels=labels, out=loss, mean_loss=m, rows=rows,
+                            cols=cols, stream=stream, plan=plan)
     return (loss, m) if mean else loss
 
 

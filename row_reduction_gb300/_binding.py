@@ -33,6 +33,11 @@ MT_OP_CROSS_ENTROPY = 5
 OP_IDS = {"rmsnorm": 0, "layernorm": 1, "residual_layernorm": 2,
           "softmax": 3, "row_sum": 4, "cross_entropy": 5}
 
+MT_DTYPE_F32 = 0
+MT_DTYPE_F16 = 1
+MT_DTYPE_BF16 = 2
+DTYPE_IDS = {"f32": 0, "f16": 1, "bf16": 2}
+
 MT_PATH_REGISTERS = 0
 MT_PATH_LOOP = 1
 
@@ -49,6 +54,12 @@ EXPORTS = (
     "mt_cross_entropy_f32", "mt_cross_entropy_f32_with_plan",
     "mt_plan_query", "mt_plan_check", "mt_private_slot_bound",
     "mt_describe_plan", "mt_status_string", "mt_last_cuda_error",
+    "mt_rmsnorm_f16", "mt_rmsnorm_bf16", "mt_layernorm_f16",
+    "mt_layernorm_bf16", "mt_residual_layernorm_f16",
+    "mt_residual_layernorm_bf16", "mt_softmax_f16", "mt_softmax_bf16",
+    "mt_row_sum_f16", "mt_row_sum_bf16", "mt_cross_entropy_f16",
+    "mt_cross_entropy_bf16", "mt_row_reduce_with_plan",
+    "mt_plan_query_dtype", "mt_plan_check_dtype",
 )
 
 
@@ -123,7 +134,23 @@ def lib() -> ctypes.CDLL:
                                                    PP],
                 "mt_plan_query": [ctypes.c_int, I64, I64, PP],
                 "mt_plan_check": [ctypes.c_int, I64, PP],
+                "mt_row_reduce_with_plan": [ctypes.c_int, ctypes.c_int, P, P,
+                                            P, P, P, P, P, P, P, I64, I64, F,
+                                            P, PP],
+                "mt_plan_query_dtype": [ctypes.c_int, ctypes.c_int, I64, I64,
+                                        PP],
+                "mt_plan_check_dtype": [ctypes.c_int, ctypes.c_int, I64, PP],
             }
+            for dt in ("f16", "bf16"):
+                sig.update({
+                    f"mt_rmsnorm_{dt}": [P, P, P, I64, I64, F, P],
+                    f"mt_layernorm_{dt}": [P, P, P, P, I64, I64, F, P],
+                    f"mt_residual_layernorm_{dt}": [P, P, P, P, P, P, I64,
+                                                    I64, F, P],
+                    f"mt_softmax_{dt}": [P, P, I64, I64, P],
+                    f"mt_row_sum_{dt}": [P, P, I64, I64, P],
+                    f"mt_cross_entropy_{dt}": [P, P, P, P, I64, I64, P],
+                })
             for name, args in sig.items():
                 fn = getattr(L, name)
                 fn.argtypes = args
@@ -142,6 +169,20 @@ def lib() -> ctypes.CDLL:
 
 
 # ---- marshalling ------------------------------------------------------------
+def _torch_dtype(name):
+    import torch
+    return {"float32": torch.float32, "f32": torch.float32,
+            "f16": torch.float16, "bf16": torch.bfloat16,
+            "int32": torch.int32}[name]
+
+
+def dtype_of(t) -> str:
+    """Storage type name ("f32", "f16", "bf16") of a torch tensor."""
+    import torch
+    return {torch.float32: "f32", torch.float16: "f16",
+            torch.bfloat16: "bf16"}[t.dtype]
+
+
 def _ptr(t, name, dtype="float32"):
     """Device address of a tensor (checked), a raw int, or None."""
     if t is None:
@@ -151,7 +192,7 @@ def _ptr(t, name, dtype="float32"):
     import torch
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name}: expected a CUDA tensor, int or None")
-    want = torch.float32 if dtype == "float32" else torch.int32
+    want = _torch_dtype(dtype)
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
     if t.dtype != want:
@@ -269,6 +310,84 @@ def mt_cross_entropy_f32_with_plan(logits, labels, loss, mean_loss, rows,
         _ptr(logits, "logits"), _ptr(labels, "labels", "int32"),
         _ptr(loss, "loss"), _ptr(mean_loss, "mean_loss"), rows, cols,
         _stream(stream), _plan(plan)), "mt_cross_entropy_f32_with_plan")
+
+
+def _half_entry_points(dt):
+    def rmsnorm(x, weight, y, rows, cols, eps, stream=None):
+        _check(getattr(lib(), f"mt_rmsnorm_{dt}")(
+            _ptr(x, "x", dt), _ptr(weight, "weight", dt), _ptr(y, "y", dt),
+            rows, cols, eps, _stream(stream)), f"mt_rmsnorm_{dt}")
+
+    def layernorm(x, gamma, beta, y, rows, cols, eps, stream=None):
+        _check(getattr(lib(), f"mt_layernorm_{dt}")(
+            _ptr(x, "x", dt), _ptr(gamma, "gamma", dt),
+            _ptr(beta, "beta", dt), _ptr(y, "y", dt), rows, cols, eps,
+            _stream(stream)), f"mt_layernorm_{dt}")
+
+    def residual_layernorm(x, residual, gamma, beta, y, h_out, rows, cols,
+                           eps, stream=None):
+        _check(getattr(lib(), f"mt_residual_layernorm_{dt}")(
+            _ptr(x, "x", dt), _ptr(residual, "residual", dt),
+            _ptr(gamma, "gamma", dt), _ptr(beta, "beta", dt),
+            _ptr(y, "y", dt), _ptr(h_out, "h_out", dt), rows, cols, eps,
+            _stream(stream)), f"mt_residual_layernorm_{dt}")
+
+    def softmax(x, y, rows, cols, stream=None):
+        _check(getattr(lib(), f"mt_softmax_{dt}")(
+            _ptr(x, "x", dt), _ptr(y, "y", dt), rows, cols,
+            _stream(stream)), f"mt_softmax_{dt}")
+
+    def row_sum(x, out, rows, cols, stream=None):
+        _check(getattr(lib(), f"mt_row_sum_{dt}")(
+            _ptr(x, "x", dt), _ptr(out, "out"), rows, cols,
+            _stream(stream)), f"mt_row_sum_{dt}")
+
+    def cross_entropy(logits, labels, loss, mean_loss, rows, cols,
+                      stream=None):
+        _check(getattr(lib(), f"mt_cross_entropy_{dt}")(
+            _ptr(logits, "logits", dt), _ptr(labels, "labels", "int32"),
+            _ptr(loss, "loss"), _ptr(mean_loss, "mean_loss"), rows, cols,
+            _stream(stream)), f"mt_cross_entropy_{dt}")
+    return rmsnorm, layernorm, residual_layernorm, softmax, row_sum, \
+        cross_entropy
+
+
+(mt_rmsnorm_f16, mt_layernorm_f16, mt_residual_layernorm_f16, mt_softmax_f16,
+ mt_row_sum_f16, mt_cross_entropy_f16) = _half_entry_points("f16")
+(mt_rmsnorm_bf16, mt_layernorm_bf16, mt_residual_layernorm_bf16,
+ mt_softmax_bf16, mt_row_sum_bf16,
+ mt_cross_entropy_bf16) = _half_entry_points("bf16")
+
+
+def mt_row_reduce_with_plan(op, dtype, x, residual=None, weight=None,
+                            beta=None, labels=None, y=None, h_out=None,
+                            out=None, mean_loss=None, rows=0, cols=0, eps=0.0,
+                            stream=None, plan=None):
+    """Any operator, any storage type, optional explicit plan."""
+    op_id = OP_IDS.get(op, op)
+    dt = dtype if isinstance(dtype, str) else \
+        {v: k for k, v in DTYPE_IDS.items()}[dtype]
+    _check(lib().mt_row_reduce_with_plan(
+        op_id, DTYPE_IDS[dt], _ptr(x, "x", dt),
+        _ptr(residual, "residual", dt), _ptr(weight, "weight", dt),
+        _ptr(beta, "beta", dt), _ptr(labels, "labels", "int32"),
+        _ptr(y, "y", dt), _ptr(h_out, "h_out", dt), _ptr(out, "out"),
+        _ptr(mean_loss, "mean_loss"), rows, cols, eps, _stream(stream),
+        _plan(plan)), "mt_row_reduce_with_plan")
+
+
+def mt_plan_query_dtype(op, dtype, rows, cols) -> MtPlan:
+    p = MtPlan()
+    _check(lib().mt_plan_query_dtype(OP_IDS.get(op, op),
+                                     DTYPE_IDS.get(dtype, dtype), rows, cols,
+                                     ctypes.byref(p)), "mt_plan_query_dtype")
+    return p
+
+
+def mt_plan_check_dtype(op, dtype, cols, plan) -> int:
+    return lib().mt_plan_check_dtype(OP_IDS.get(op, op),
+                                     DTYPE_IDS.get(dtype, dtype), cols,
+                                     _plan(plan))
 
 
 def mt_plan_query(op, rows, cols) -> MtPlan:

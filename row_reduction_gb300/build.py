@@ -21,9 +21,11 @@ OUT = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT, "libmt_rowreduce.so")
 HEADER = os.path.join(ROOT, "include", "mt_rowreduce.h")
 
-SOURCES = ["api.cpp", "planner.cpp", "ops_rmsnorm.cu", "ops_layernorm.cu",
-           "ops_residual_layernorm.cu", "ops_softmax.cu", "ops_row_sum.cu",
-           "ops_cross_entropy.cu"]
+OPS = ("rmsnorm", "layernorm", "residual_layernorm", "softmax", "row_sum",
+       "cross_entropy")
+DTYPES = ("f32", "f16", "bf16")
+SOURCES = (["api.cpp", "planner.cpp", "mean.cu"] +
+           [f"ops_{op}_{dt}.cu" for op in OPS for dt in DTYPES])
 DEPENDS = ["mt_internal.h", "mt_kernels.cuh", "plan_table.inc"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -71,6 +73,10 @@ def build(force: bool = False, jobs: int | None = None,
         return LIB
     objs = [os.path.join(OUT, "obj", s.rsplit(".", 1)[0] + ".o")
             for s in SOURCES]
+    for name in os.listdir(os.path.join(OUT, "obj")):   # stale objects
+        path = os.path.join(OUT, "obj", name)
+        if path not in objs:
+            os.remove(path)
     # Largest translation units first so the parallel build ends sooner.
     order = sorted(range(len(SOURCES)),
                    key=lambda i: not SOURCES[i].endswith(".cu"))

@@ -22,8 +22,8 @@ mt_status cuda_status(cudaError_t e) {
                                               : MT_ERR_CUDA;
 }
 
-bool misaligned4(const void *p) {
-    return (reinterpret_cast<uintptr_t>(p) & 3u) != 0;
+bool misaligned(const void *p, int bytes) {
+    return (reinterpret_cast<uintptr_t>(p) & (uintptr_t)(bytes - 1)) != 0;
 }
 
 // SM count per device, queried once.
@@ -48,27 +48,35 @@ cudaError_t sm_count(int dev, int *out) {
     return cudaSuccess;
 }
 
-// Resident CTAs per SM for a (device, op, kernel variant, block size).
+typedef cudaError_t (*LaunchFn)(const mt_plan_t &, const KArgs &, bool,
+                                cudaStream_t);
+typedef cudaError_t (*OccFn)(const mt_plan_t &, bool, int *);
+
+#define MT_ROW(op)                                                           \
+    {launch_##op##_f32, launch_##op##_f16, launch_##op##_bf16}
+#define MT_OCC_ROW(op)                                                       \
+    {launch_##op##_f32_occupancy, launch_##op##_f16_occupancy,               \
+     launch_##op##_bf16_occupancy}
+const LaunchFn kLaunch[OP_COUNT][DT_COUNT] = {
+    MT_ROW(rmsnorm), MT_ROW(layernorm), MT_ROW(residual_layernorm),
+    MT_ROW(softmax), MT_ROW(row_sum),   MT_ROW(cross_entropy)};
+const OccFn kOcc[OP_COUNT][DT_COUNT] = {
+    MT_OCC_ROW(rmsnorm), MT_OCC_ROW(layernorm),
+    MT_OCC_ROW(residual_layernorm), MT_OCC_ROW(softmax),
+    MT_OCC_ROW(row_sum), MT_OCC_ROW(cross_entropy)};
+#undef MT_ROW
+#undef MT_OCC_ROW
+
+// Resident CTAs per SM for a (device, op, dtype, kernel variant, block).
 std::mutex g_occ_mu;
 std::unordered_map<uint64_t, int> g_occ;
 
-typedef cudaError_t (*LaunchFn)(const mt_plan_t &, const KArgs &, bool,
-                                cudaStream_t, int *);
-typedef cudaError_t (*OccFn)(const mt_plan_t &, bool, int *);
-
-const LaunchFn kLaunch[OP_COUNT] = {
-    launch_rmsnorm, launch_layernorm, launch_residual_layernorm,
-    launch_softmax, launch_row_sum,   launch_cross_entropy};
-const OccFn kOcc[OP_COUNT] = {
-    launch_rmsnorm_occupancy,   launch_layernorm_occupancy,
-    launch_residual_layernorm_occupancy, launch_softmax_occupancy,
-    launch_row_sum_occupancy,   launch_cross_entropy_occupancy};
-
-cudaError_t blocks_per_sm(int dev, int op, const mt_plan_t &p, bool aligned,
-                          int *out) {
+cudaError_t blocks_per_sm(int dev, int op, int dtype, const mt_plan_t &p,
+                          bool aligned, int *out) {
     const uint64_t key =
-        ((uint64_t)(dev & 0xff) << 56) | ((uint64_t)op << 48) |
-        ((uint64_t)p.path << 44) | ((uint64_t)p.values_per_thread << 40) |
+        ((uint64_t)(dev & 0xff) << 56) | ((uint64_t)op << 50) |
+        ((uint64_t)dtype << 46) | ((uint64_t)p.path << 44) |
+        ((uint64_t)p.values_per_thread << 40) |
         ((uint64_t)(p.chunks & 0xff) << 32) | ((uint64_t)aligned << 31) |
         (uint64_t)(p.threads_per_row * p.rows_per_block);
     {
@@ -80,7 +88,7 @@ cudaError_t blocks_per_sm(int dev, int op, const mt_plan_t &p, bool aligned,
         }
     }
     int n = 0;
-    cudaError_t e = kOcc[op](p, aligned, &n);
+    cudaError_t e = kOcc[op][dtype](p, aligned, &n);
     if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lk(g_occ_mu);
     g_occ[key] = n;
@@ -88,45 +96,117 @@ cudaError_t blocks_per_sm(int dev, int op, const mt_plan_t &p, bool aligned,
     return cudaSuccess;
 }
 
-// Pointers accessed with V-wide vectors besides x (NULL entries ignored).
-struct VecPtrs {
-    const void *y = nullptr, *res = nullptr, *h = nullptr, *w = nullptr,
-               *b = nullptr;
+// Arguments of one call.
+struct Call {
+    int op = 0, dtype = 0;
+    const void *x = nullptr, *res = nullptr, *w = nullptr, *b = nullptr;
+    const int32_t *labels = nullptr;
+    void *y = nullptr, *h = nullptr;
+    float *out = nullptr, *mean = nullptr;
+    int64_t rows = 0, cols = 0;
+    float eps = 0.f;
 };
 
-mt_status dispatch(int op, KArgs a, const VecPtrs &vp,
-                   const mt_plan_t *forced, cudaStream_t stream) {
+// Which pointers each operator takes (the others must be NULL), and which
+// of them must be non-NULL when rows > 0.
+enum : unsigned {
+    U_RES = 1, U_W = 2, U_B = 4, U_LABELS = 8, U_Y = 16, U_H = 32,
+    U_OUT = 64, U_MEAN = 128
+};
+unsigned uses(int op) {
+    switch (op) {
+        case OP_RMSNORM: return U_W | U_Y;
+        case OP_LAYERNORM: return U_W | U_B | U_Y;
+        case OP_RESIDUAL_LAYERNORM: return U_RES | U_W | U_B | U_Y | U_H;
+        case OP_SOFTMAX: return U_Y;
+        case OP_ROW_SUM: return U_OUT;
+        case OP_CROSS_ENTROPY: return U_LABELS | U_OUT | U_MEAN;
+    }
+    return 0;
+}
+unsigned required(int op) {
+    switch (op) {
+        case OP_RMSNORM:
+        case OP_LAYERNORM:
+        case OP_SOFTMAX: return U_Y;
+        case OP_RESIDUAL_LAYERNORM: return U_RES | U_Y;
+        case OP_ROW_SUM: return U_OUT;
+        case OP_CROSS_ENTROPY: return U_LABELS | U_OUT;
+    }
+    return 0;
+}
+
+mt_status validate(const Call &c) {
+    if (c.op < 0 || c.op >= OP_COUNT || c.dtype < 0 || c.dtype >= DT_COUNT)
+        return MT_ERR_INVALID_ARGUMENT;
+    if (c.rows < 0 || c.cols < 1 || c.cols > 0x7fffffff)
+        return MT_ERR_INVALID_ARGUMENT;
+    if (c.rows > 0 && c.rows > INT64_MAX / c.cols)
+        return MT_ERR_INVALID_ARGUMENT;
+    const unsigned present = (c.res ? U_RES : 0) | (c.w ? U_W : 0) |
+                             (c.b ? U_B : 0) | (c.labels ? U_LABELS : 0) |
+                             (c.y ? U_Y : 0) | (c.h ? U_H : 0) |
+                             (c.out ? U_OUT : 0) | (c.mean ? U_MEAN : 0);
+    if (present & ~uses(c.op)) return MT_ERR_INVALID_ARGUMENT;
+    const unsigned req = required(c.op);
+    if (c.rows > 0 && (!c.x || (present & req) != req))
+        return MT_ERR_INVALID_ARGUMENT;
+    const int es = dtype_size(c.dtype);
+    if (misaligned(c.x, es) || misaligned(c.res, es) || misaligned(c.w, es) ||
+        misaligned(c.b, es) || misaligned(c.y, es) || misaligned(c.h, es) ||
+        misaligned(c.labels, 4) || misaligned(c.out, 4) ||
+        misaligned(c.mean, 4))
+        return MT_ERR_INVALID_ARGUMENT;
+    return MT_OK;
+}
+
+mt_status run(const Call &c, const mt_plan_t *forced, cudaStream_t stream) {
+    if (mt_status st = validate(c)) return st;
     mt_plan_t p;
     if (forced != nullptr) {
         p = *forced;
-        const mt_status st = plan_check(op, a.cols, p);
-        if (st != MT_OK) return st;
+        if (mt_status st = plan_check(c.op, c.dtype, c.cols, p)) return st;
     } else {
-        const mt_status st = plan_lookup(op, a.rows, a.cols, &p);
-        if (st != MT_OK) return st;
+        if (mt_status st = plan_lookup(c.op, c.dtype, c.rows, c.cols, &p))
+            return st;
     }
-    if (a.rows == 0) return MT_OK;
+    if (c.rows == 0) return MT_OK;
+
+    KArgs a = {};
+    a.x = c.x;
+    a.res = c.res;
+    a.w = c.w;
+    a.b = c.b;
+    a.y = c.y;
+    a.h = c.h;
+    a.out = c.out;
+    a.labels = c.labels;
+    a.rows = c.rows;
+    a.cols = (int32_t)c.cols;
+    a.eps = c.eps;
 
     // Alignment mode: the "aligned" kernels need every row of every
-    // vector-accessed pointer to start on a 4V-byte boundary.
+    // vector-accessed pointer to start on a V*element-size boundary.  A
+    // pack of one FP32 value is always aligned.
     const int V = p.values_per_thread;
-    const uintptr_t mask = (uintptr_t)(4 * V - 1);
+    const int es = dtype_size(c.dtype);
+    const uintptr_t mask = (uintptr_t)(V * es - 1);
     auto al = [&](const void *q) {
         return q == nullptr || (reinterpret_cast<uintptr_t>(q) & mask) == 0;
     };
-    const bool aligned = V == 1 || (a.cols % V == 0 && al(a.x) && al(vp.y) &&
-                                    al(vp.res) && al(vp.h) && al(vp.w) &&
-                                    al(vp.b));
+    const bool aligned = (V == 1 && es == 4) ||
+                         (c.cols % V == 0 && al(c.x) && al(c.y) &&
+                          al(c.res) && al(c.h) && al(c.w) && al(c.b));
     // Unaligned kernels: a pointer keeps x's phase when its distance from x
-    // is a multiple of 4V bytes; then its row bodies are aligned too.
+    // is a multiple of V elements; then its row bodies are aligned too.
     auto phase = [&](const void *q) -> int32_t {
         if (q == nullptr) return 0;
         return ((reinterpret_cast<uintptr_t>(q) -
-                 reinterpret_cast<uintptr_t>(a.x)) & mask) == 0;
+                 reinterpret_cast<uintptr_t>(c.x)) & mask) == 0;
     };
-    a.y_vec = phase(vp.y);
-    a.h_vec = phase(vp.h);
-    a.r_vec = phase(vp.res);
+    a.y_vec = phase(c.y);
+    a.h_vec = phase(c.h);
+    a.r_vec = phase(c.res);
     a.W = p.threads_per_row;
     int l = 0;
     while ((1 << l) < a.W) ++l;
@@ -144,7 +224,7 @@ mt_status dispatch(int op, KArgs a, const VecPtrs &vp,
         int sms = 0, bps = 0;
         e = sm_count(dev, &sms);
         if (e != cudaSuccess) return cuda_status(e);
-        e = blocks_per_sm(dev, op, p, aligned, &bps);
+        e = blocks_per_sm(dev, c.op, c.dtype, p, aligned, &bps);
         if (e != cudaSuccess) return cuda_status(e);
         if (bps < 1) return MT_ERR_OUT_OF_RESOURCES;
         grid = (int64_t)sms * bps;
@@ -153,204 +233,224 @@ mt_status dispatch(int op, KArgs a, const VecPtrs &vp,
     if (grid > 0x7fffffff) grid = 0x7fffffff;
     p.grid = (int32_t)grid;
 
-    cudaError_t e = kLaunch[op](p, a, aligned, stream, nullptr);
-    return cuda_status(e);
-}
-
-mt_status check_shape(int64_t rows, int64_t cols) {
-    if (rows < 0 || cols < 1 || cols > 0x7fffffff) return MT_ERR_INVALID_ARGUMENT;
-    if (rows > 0 && rows > INT64_MAX / cols) return MT_ERR_INVALID_ARGUMENT;
+    if (mt_status st =
+            cuda_status(kLaunch[c.op][c.dtype](p, a, aligned, stream)))
+        return st;
+    if (c.op == OP_CROSS_ENTROPY && c.mean != nullptr)
+        return cuda_status(launch_mean(c.out, c.mean, c.rows, stream));
     return MT_OK;
 }
 
-KArgs base_args(const float *x, int64_t rows, int64_t cols) {
-    KArgs a = {};
-    a.x = x;
-    a.rows = rows;
-    a.cols = (int32_t)cols;
-    return a;
+Call make_call(int op, int dtype, const void *x, int64_t rows, int64_t cols) {
+    Call c;
+    c.op = op;
+    c.dtype = dtype;
+    c.x = x;
+    c.rows = rows;
+    c.cols = cols;
+    return c;
+}
+
+mt_status rmsnorm_call(int dt, const void *x, const void *w, void *y,
+                       int64_t rows, int64_t cols, float eps, mt_stream_t s,
+                       const mt_plan_t *plan) {
+    Call c = make_call(OP_RMSNORM, dt, x, rows, cols);
+    c.w = w;
+    c.y = y;
+    c.eps = eps;
+    return run(c, plan, (cudaStream_t)s);
+}
+
+mt_status layernorm_call(int dt, const void *x, const void *g,
+                         const void *b, void *y, int64_t rows, int64_t cols,
+                         float eps, mt_stream_t s, const mt_plan_t *plan) {
+    Call c = make_call(OP_LAYERNORM, dt, x, rows, cols);
+    c.w = g;
+    c.b = b;
+    c.y = y;
+    c.eps = eps;
+    return run(c, plan, (cudaStream_t)s);
+}
+
+mt_status resln_call(int dt, const void *x, const void *r, const void *g,
+                     const void *b, void *y, void *h, int64_t rows,
+                     int64_t cols, float eps, mt_stream_t s,
+                     const mt_plan_t *plan) {
+    Call c = make_call(OP_RESIDUAL_LAYERNORM, dt, x, rows, cols);
+    c.res = r;
+    c.w = g;
+    c.b = b;
+    c.y = y;
+    c.h = h;
+    c.eps = eps;
+    return run(c, plan, (cudaStream_t)s);
+}
+
+mt_status softmax_call(int dt, const void *x, void *y, int64_t rows,
+                       int64_t cols, mt_stream_t s, const mt_plan_t *plan) {
+    Call c = make_call(OP_SOFTMAX, dt, x, rows, cols);
+    c.y = y;
+    return run(c, plan, (cudaStream_t)s);
+}
+
+mt_status row_sum_call(int dt, const void *x, float *out, int64_t rows,
+                       int64_t cols, mt_stream_t s, const mt_plan_t *plan) {
+    Call c = make_call(OP_ROW_SUM, dt, x, rows, cols);
+    c.out = out;
+    return run(c, plan, (cudaStream_t)s);
+}
+
+mt_status ce_call(int dt, const void *x, const int32_t *labels, float *loss,
+                  float *mean, int64_t rows, int64_t cols, mt_stream_t s,
+                  const mt_plan_t *plan) {
+    Call c = make_call(OP_CROSS_ENTROPY, dt, x, rows, cols);
+    c.labels = labels;
+    c.out = loss;
+    c.mean = mean;
+    return run(c, plan, (cudaStream_t)s);
 }
 
 }  // namespace
 }  // namespace mt
 
-using mt::check_shape;
-using mt::dispatch;
-using mt::misaligned4;
-using mt::VecPtrs;
+using namespace mt;
 
 extern "C" {
 
+// ---- FP32 -------------------------------------------------------------------
 mt_status mt_rmsnorm_f32_with_plan(const float *x, const float *weight,
                                    float *y, int64_t rows, int64_t cols,
                                    float eps, mt_stream_t stream,
                                    const mt_plan_t *plan) {
-    if (mt_status st = check_shape(rows, cols)) return st;
-    if (rows > 0 && (!x || !y))
-        return MT_ERR_INVALID_ARGUMENT;
-    if (misaligned4(x) ||
-        misaligned4(y) ||
-        misaligned4(weight))
-        return MT_ERR_INVALID_ARGUMENT;
-    mt::KArgs a = mt::base_args(x, rows, cols);
-    a.w = weight;
-    a.y = y;
-    a.eps = eps;
-    VecPtrs vp;
-    vp.y = y;
-    vp.w = weight;
-    return dispatch(mt::OP_RMSNORM, a, vp, plan, (cudaStream_t)stream);
+    return rmsnorm_call(MT_DTYPE_F32, x, weight, y, rows, cols, eps, stream,
+                        plan);
 }
-
 mt_status mt_rmsnorm_f32(const float *x, const float *weight, float *y,
                          int64_t rows, int64_t cols, float eps,
                          mt_stream_t stream) {
-    return mt_rmsnorm_f32_with_plan(x, weight, y, rows, cols, eps, stream,
-                                    nullptr);
+    return rmsnorm_call(MT_DTYPE_F32, x, weight, y, rows, cols, eps, stream,
+                        nullptr);
 }
-
 mt_status mt_layernorm_f32_with_plan(const float *x, const float *gamma,
                                      const float *beta, float *y,
                                      int64_t rows, int64_t cols, float eps,
                                      mt_stream_t stream,
                                      const mt_plan_t *plan) {
-    if (mt_status st = check_shape(rows, cols)) return st;
-    if (rows > 0 && (!x || !y))
-        return MT_ERR_INVALID_ARGUMENT;
-    if (misaligned4(x) ||
-        misaligned4(y) ||
-        misaligned4(gamma) ||
-        misaligned4(beta))
-        return MT_ERR_INVALID_ARGUMENT;
-    mt::KArgs a = mt::base_args(x, rows, cols);
-    a.w = gamma;
-    a.b = beta;
-    a.y = y;
-    a.eps = eps;
-    VecPtrs vp;
-    vp.y = y;
-    vp.w = gamma;
-    vp.b = beta;
-    return dispatch(mt::OP_LAYERNORM, a, vp, plan, (cudaStream_t)stream);
+    return layernorm_call(MT_DTYPE_F32, x, gamma, beta, y, rows, cols, eps,
+                          stream, plan);
 }
-
 mt_status mt_layernorm_f32(const float *x, const float *gamma,
                            const float *beta, float *y, int64_t rows,
                            int64_t cols, float eps, mt_stream_t stream) {
-    return mt_layernorm_f32_with_plan(x, gamma, beta, y, rows, cols, eps,
-                                      stream, nullptr);
+    return layernorm_call(MT_DTYPE_F32, x, gamma, beta, y, rows, cols, eps,
+                          stream, nullptr);
 }
-
 mt_status mt_residual_layernorm_f32_with_plan(
     const float *x, const float *residual, const float *gamma,
     const float *beta, float *y, float *h_out, int64_t rows, int64_t cols,
     float eps, mt_stream_t stream, const mt_plan_t *plan) {
-    if (mt_status st = check_shape(rows, cols)) return st;
-    if (rows > 0 && (!x || !residual || !y))
-        return MT_ERR_INVALID_ARGUMENT;
-    if (misaligned4(x) ||
-        misaligned4(residual) ||
-        misaligned4(y) ||
-        misaligned4(h_out) ||
-        misaligned4(gamma) ||
-        misaligned4(beta))
-        return MT_ERR_INVALID_ARGUMENT;
-    mt::KArgs a = mt::base_args(x, rows, cols);
-    a.res = residual;
-    a.w = gamma;
-    a.b = beta;
-    a.y = y;
-    a.h = h_out;
-    a.eps = eps;
-    VecPtrs vp;
-    vp.y = y;
-    vp.res = residual;
-    vp.h = h_out;
-    vp.w = gamma;
-    vp.b = beta;
-    return dispatch(mt::OP_RESIDUAL_LAYERNORM, a, vp, plan,
-                    (cudaStream_t)stream);
+    return resln_call(MT_DTYPE_F32, x, residual, gamma, beta, y, h_out, rows,
+                      cols, eps, stream, plan);
 }
-
 mt_status mt_residual_layernorm_f32(const float *x, const float *residual,
                                     const float *gamma, const float *beta,
                                     float *y, float *h_out, int64_t rows,
                                     int64_t cols, float eps,
                                     mt_stream_t stream) {
-    return mt_residual_layernorm_f32_with_plan(x, residual, gamma, beta, y,
-                                               h_out, rows, cols, eps, stream,
-                                               nullptr);
+    return resln_call(MT_DTYPE_F32, x, residual, gamma, beta, y, h_out, rows,
+                      cols, eps, stream, nullptr);
 }
-
 mt_status mt_softmax_f32_with_plan(const float *x, float *y, int64_t rows,
                                    int64_t cols, mt_stream_t stream,
                                    const mt_plan_t *plan) {
-    if (mt_status st = check_shape(rows, cols)) return st;
-    if (rows > 0 && (!x || !y))
-        return MT_ERR_INVALID_ARGUMENT;
-    if (misaligned4(x) ||
-        misaligned4(y))
-        return MT_ERR_INVALID_ARGUMENT;
-    mt::KArgs a = mt::base_args(x, rows, cols);
-    a.y = y;
-    VecPtrs vp;
-    vp.y = y;
-    return dispatch(mt::OP_SOFTMAX, a, vp, plan, (cudaStream_t)stream);
+    return softmax_call(MT_DTYPE_F32, x, y, rows, cols, stream, plan);
 }
-
 mt_status mt_softmax_f32(const float *x, float *y, int64_t rows,
                          int64_t cols, mt_stream_t stream) {
-    return mt_softmax_f32_with_plan(x, y, rows, cols, stream, nullptr);
+    return softmax_call(MT_DTYPE_F32, x, y, rows, cols, stream, nullptr);
 }
-
 mt_status mt_row_sum_f32_with_plan(const float *x, float *out, int64_t rows,
                                    int64_t cols, mt_stream_t stream,
                                    const mt_plan_t *plan) {
-    if (mt_status st = check_shape(rows, cols)) return st;
-    if (rows > 0 && (!x || !out))
-        return MT_ERR_INVALID_ARGUMENT;
-    if (misaligned4(x) ||
-        misaligned4(out))
-        return MT_ERR_INVALID_ARGUMENT;
-    mt::KArgs a = mt::base_args(x, rows, cols);
-    a.out = out;
-    return dispatch(mt::OP_ROW_SUM, a, VecPtrs(), plan,
-                    (cudaStream_t)stream);
+    return row_sum_call(MT_DTYPE_F32, x, out, rows, cols, stream, plan);
 }
-
 mt_status mt_row_sum_f32(const float *x, float *out, int64_t rows,
                          int64_t cols, mt_stream_t stream) {
-    return mt_row_sum_f32_with_plan(x, out, rows, cols, stream, nullptr);
+    return row_sum_call(MT_DTYPE_F32, x, out, rows, cols, stream, nullptr);
 }
-
 mt_status mt_cross_entropy_f32_with_plan(const float *logits,
                                          const int32_t *labels, float *loss,
                                          float *mean_loss, int64_t rows,
                                          int64_t cols, mt_stream_t stream,
                                          const mt_plan_t *plan) {
-    if (mt_status st = check_shape(rows, cols)) return st;
-    if (rows > 0 && (!logits || !labels || !loss))
-        return MT_ERR_INVALID_ARGUMENT;
-    if (misaligned4(logits) ||
-        misaligned4(labels) ||
-        misaligned4(loss) ||
-        misaligned4(mean_loss))
-        return MT_ERR_INVALID_ARGUMENT;
-    mt::KArgs a = mt::base_args(logits, rows, cols);
-    a.labels = labels;
-    a.out = loss;
-    const mt_status st = dispatch(mt::OP_CROSS_ENTROPY, a, VecPtrs(), plan,
-                                  (cudaStream_t)stream);
-    if (st != MT_OK || rows == 0 || mean_loss == nullptr) return st;
-    return mt::cuda_status(
-        mt::launch_mean(loss, mean_loss, rows, (cudaStream_t)stream));
+    return ce_call(MT_DTYPE_F32, logits, labels, loss, mean_loss, rows, cols,
+                   stream, plan);
 }
-
 mt_status mt_cross_entropy_f32(const float *logits, const int32_t *labels,
                                float *loss, float *mean_loss, int64_t rows,
                                int64_t cols, mt_stream_t stream) {
-    return mt_cross_entropy_f32_with_plan(logits, labels, loss, mean_loss,
-                                          rows, cols, stream, nullptr);
+    return ce_call(MT_DTYPE_F32, logits, labels, loss, mean_loss, rows, cols,
+                   stream, nullptr);
+}
+
+// ---- FP16 / BF16 ------------------------------------------------------------
+#define MT_HALF_ENTRY_POINTS(suffix, DT, TY)                                  \
+    mt_status mt_rmsnorm_##suffix(const TY *x, const TY *weight, TY *y,      \
+                                  int64_t rows, int64_t cols, float eps,     \
+                                  mt_stream_t stream) {                      \
+        return rmsnorm_call(DT, x, weight, y, rows, cols, eps, stream,       \
+                            nullptr);                                        \
+    }                                                                        \
+    mt_status mt_layernorm_##suffix(const TY *x, const TY *gamma,            \
+                                    const TY *beta, TY *y, int64_t rows,     \
+                                    int64_t cols, float eps,                 \
+                                    mt_stream_t stream) {                    \
+        return layernorm_call(DT, x, gamma, beta, y, rows, cols, eps,        \
+                              stream, nullptr);                              \
+    }                                                                        \
+    mt_status mt_residual_layernorm_##suffix(                                \
+        const TY *x, const TY *residual, const TY *gamma, const TY *beta,    \
+        TY *y, TY *h_out, int64_t rows, int64_t cols, float eps,             \
+        mt_stream_t stream) {                                                \
+        return resln_call(DT, x, residual, gamma, beta, y, h_out, rows,      \
+                          cols, eps, stream, nullptr);                       \
+    }                                                                        \
+    mt_status mt_softmax_##suffix(const TY *x, TY *y, int64_t rows,          \
+                                  int64_t cols, mt_stream_t stream) {        \
+        return softmax_call(DT, x, y, rows, cols, stream, nullptr);          \
+    }                                                                        \
+    mt_status mt_row_sum_##suffix(const TY *x, float *out, int64_t rows,     \
+                                  int64_t cols, mt_stream_t stream) {        \
+        return row_sum_call(DT, x, out, rows, cols, stream, nullptr);        \
+    }                                                                        \
+    mt_status mt_cross_entropy_##suffix(                                     \
+        const TY *logits, const int32_t *labels, float *loss,                \
+        float *mean_loss, int64_t rows, int64_t cols, mt_stream_t stream) {  \
+        return ce_call(DT, logits, labels, loss, mean_loss, rows, cols,      \
+                       stream, nullptr);                                     \
+    }
+MT_HALF_ENTRY_POINTS(f16, MT_DTYPE_F16, mt_f16_t)
+MT_HALF_ENTRY_POINTS(bf16, MT_DTYPE_BF16, mt_bf16_t)
+#undef MT_HALF_ENTRY_POINTS
+
+mt_status mt_row_reduce_with_plan(int op, int dtype, const void *x,
+                                  const void *residual, const void *weight,
+                                  const void *beta, const int32_t *labels,
+                                  void *y, void *h_out, float *out,
+                                  float *mean_loss, int64_t rows,
+                                  int64_t cols, float eps, mt_stream_t stream,
+                                  const mt_plan_t *plan) {
+    Call c = make_call(op, dtype, x, rows, cols);
+    c.res = residual;
+    c.w = weight;
+    c.b = beta;
+    c.labels = labels;
+    c.y = y;
+    c.h = h_out;
+    c.out = out;
+    c.mean = mean_loss;
+    c.eps = eps;
+    return run(c, plan, (cudaStream_t)stream);
 }
 
 const char *mt_status_string(mt_status s) {
@@ -364,6 +464,6 @@ const char *mt_status_string(mt_status s) {
     return "MT_ERR_UNKNOWN";
 }
 
-int mt_last_cuda_error(void) { return mt::g_last_cuda_error; }
+int mt_last_cuda_error(void) { return g_last_cuda_error; }
 
 }  // extern "C"

@@ -1,8 +1,6 @@
-// ops_cross_entropy.cu -- instantiates the cross-entropy kernels and the
-// one-CTA kernel that averages the per-row losses.
+// mean.cu -- the one-CTA kernel that averages the per-row cross-entropy
+// losses.
 #include "mt_kernels.cuh"
-
-MT_DEFINE_LAUNCHER(launch_cross_entropy, OP_CROSS_ENTROPY)
 
 namespace mt {
 

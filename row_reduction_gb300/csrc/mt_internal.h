@@ -19,14 +19,25 @@ enum : int {
     OP_COUNT = 6
 };
 
+enum : int {
+    DT_F32 = MT_DTYPE_F32,
+    DT_F16 = MT_DTYPE_F16,
+    DT_BF16 = MT_DTYPE_BF16,
+    DT_COUNT = 3
+};
+
+inline int dtype_size(int dt) { return dt == DT_F32 ? 4 : 2; }
+
 // Kernel arguments; one struct for all operators (unused fields are NULL).
+// Matrices and parameter vectors hold the storage type of the launch
+// (FP32, FP16 or BF16); per-row outputs are always FP32.
 struct KArgs {
-    const float *x;        // input matrix (logits for cross-entropy)
-    const float *res;      // residual (residual LayerNorm)
-    const float *w;        // RMSNorm weight / LayerNorm gamma (NULL = 1)
-    const float *b;        // LayerNorm beta (NULL = 0)
-    float *y;              // output matrix
-    float *h;              // residual LayerNorm h_out (NULL = not written)
+    const void *x;         // input matrix (logits for cross-entropy)
+    const void *res;       // residual (residual LayerNorm)
+    const void *w;         // RMSNorm weight / LayerNorm gamma (NULL = 1)
+    const void *b;         // LayerNorm beta (NULL = 0)
+    void *y;               // output matrix
+    void *h;               // residual LayerNorm h_out (NULL = not written)
     float *out;            // per-row output (row sum, cross-entropy loss)
     const int32_t *labels; // cross-entropy labels
     int64_t rows;
@@ -57,20 +68,25 @@ constexpr int reg_max_threads(int vk) {
 }
 constexpr int kLoopMaxThreads = 512;
 
-// Per-operator launchers, one translation unit each.  `aligned` selects the
-// kernels whose every access of the row body is a V-wide vector access
-// without a head; `grid` is already resolved (> 0).
+// Launchers, one translation unit per (operator, storage type).  `aligned`
+// selects the kernels whose every access of the row body is a V-wide vector
+// access without a head; `plan.grid` is already resolved (> 0).
 #define MT_DECLARE_LAUNCHER(name)                                            \
     cudaError_t name(const mt_plan_t &plan, const KArgs &a, bool aligned,    \
-                     cudaStream_t stream, int *max_threads_out);             \
+                     cudaStream_t stream);                                   \
     cudaError_t name##_occupancy(const mt_plan_t &plan, bool aligned,        \
                                  int *blocks_per_sm);
-MT_DECLARE_LAUNCHER(launch_rmsnorm)
-MT_DECLARE_LAUNCHER(launch_layernorm)
-MT_DECLARE_LAUNCHER(launch_residual_layernorm)
-MT_DECLARE_LAUNCHER(launch_softmax)
-MT_DECLARE_LAUNCHER(launch_row_sum)
-MT_DECLARE_LAUNCHER(launch_cross_entropy)
+#define MT_DECLARE_OP(op)                                                    \
+    MT_DECLARE_LAUNCHER(launch_##op##_f32)                                   \
+    MT_DECLARE_LAUNCHER(launch_##op##_f16)                                   \
+    MT_DECLARE_LAUNCHER(launch_##op##_bf16)
+MT_DECLARE_OP(rmsnorm)
+MT_DECLARE_OP(layernorm)
+MT_DECLARE_OP(residual_layernorm)
+MT_DECLARE_OP(softmax)
+MT_DECLARE_OP(row_sum)
+MT_DECLARE_OP(cross_entropy)
+#undef MT_DECLARE_OP
 #undef MT_DECLARE_LAUNCHER
 
 // One-CTA fixed-order mean of `rows` per-row losses.
@@ -78,7 +94,8 @@ cudaError_t launch_mean(const float *loss, float *mean, int64_t rows,
                         cudaStream_t stream);
 
 // Planner (planner.cpp).
-mt_status plan_lookup(int op, int64_t rows, int64_t cols, mt_plan_t *out);
-mt_status plan_check(int op, int64_t cols, const mt_plan_t &p);
+mt_status plan_lookup(int op, int dtype, int64_t rows, int64_t cols,
+                      mt_plan_t *out);
+mt_status plan_check(int op, int dtype, int64_t cols, const mt_plan_t &p);
 
 }  // namespace mt

@@ -4,15 +4,25 @@
 // §Implementation and semantics): a row is served by W consecutive threads
 // ("workers"); worker w owns, in chunk k, the V consecutive elements
 //     i = (k*W + w)*V + e,   0 <= e < V,
-// of the row body, so a warp's V=4 accesses of one chunk are 16-byte vectors
-// covering 512 contiguous bytes.  Complete packs take unguarded vector
-// accesses; only the last, partial pack is guarded element by element.
+// of the row body, so with 16-byte packs (V=4 FP32, V=8 FP16/BF16) a warp's
+// accesses of one chunk cover 512 contiguous bytes.  Complete packs take
+// unguarded vector accesses; only the last, partial pack is guarded element
+// by element.
+//
+// Storage types.  T is the element type of the matrices and parameter
+// vectors (float, __half or __nv_bfloat16).  Every value is widened to FP32
+// on load and every statistic and epilogue is computed in FP32; the only
+// rounding to T is the final store ("FP32 reduction and epilogue arithmetic,
+// rounding only on the output store", Thread Ownership and Software
+// Staging, §Register-tiled reductions).  Per-row outputs (row sums, losses,
+// the mean) are FP32 for every T.
 //
 // Alignment.  CUDA vector accesses must be naturally aligned.  When every
-// row starts on a 4V-byte boundary (the "aligned" kernels: cols % V == 0 and
-// aligned base pointers) the body is the whole row.  Otherwise each row first
-// peels a head of hd = (-row_address/4) mod V scalar elements, owned one each
-// by workers 0..hd-1, and the map above applies to the rest.
+// row starts on a V*sizeof(T)-byte boundary (the "aligned" kernels:
+// cols % V == 0 and aligned base pointers) the body is the whole row.
+// Otherwise each row first peels a head of hd = (-row_address/sizeof(T))
+// mod V scalar elements, owned one each by workers 0..hd-1, and the map
+// above applies to the rest.
 //
 // Reduction ("Thread Ownership and Software Staging", §Register-tiled
 // reductions): each thread combines its own slots, then the W lanes of a row
@@ -35,6 +45,8 @@
 // inactive but still take part in every shuffle and barrier).
 #pragma once
 
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <math.h>
 #include <stdint.h>
 
@@ -59,61 +71,146 @@ __device__ __forceinline__ void two_sum(float a, float b, float &s,
     err = __fadd_rn(__fsub_rn(a, ap), __fsub_rn(b, bp));
 }
 
-// ---- vector access -------------------------------------------------------
-template <int V>
-__device__ __forceinline__ void ld_vec(const float *p, float *d) {
-    if constexpr (V == 4) {
-        const float4 t = *reinterpret_cast<const float4 *>(p);
-        d[0] = t.x; d[1] = t.y; d[2] = t.z; d[3] = t.w;
-    } else if constexpr (V == 2) {
-        const float2 t = *reinterpret_cast<const float2 *>(p);
-        d[0] = t.x; d[1] = t.y;
+// ---- storage types ---------------------------------------------------------
+// Conversions between 32-bit words holding T values and FP32.
+template <typename T>
+struct Pack;
+
+template <>
+struct Pack<float> {
+    static constexpr int kPerWord = 1;
+    static __device__ __forceinline__ void unpack(unsigned w, float *d) {
+        d[0] = __uint_as_float(w);
+    }
+    static __device__ __forceinline__ unsigned pack(const float *d) {
+        return __float_as_uint(d[0]);
+    }
+    static __device__ __forceinline__ float scalar(float v) { return v; }
+    static __device__ __forceinline__ float from(float v) { return v; }
+};
+
+template <>
+struct Pack<__nv_bfloat16> {
+    static constexpr int kPerWord = 2;
+    // A bfloat16 is the high half of the FP32 with the same value.
+    static __device__ __forceinline__ void unpack(unsigned w, float *d) {
+        d[0] = __uint_as_float(w << 16);
+        d[1] = __uint_as_float(w & 0xffff0000u);
+    }
+    static __device__ __forceinline__ unsigned pack(const float *d) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(d[0], d[1]);
+        return *reinterpret_cast<const unsigned *>(&h);
+    }
+    static __device__ __forceinline__ float scalar(__nv_bfloat16 v) {
+        return __bfloat162float(v);
+    }
+    static __device__ __forceinline__ __nv_bfloat16 from(float v) {
+        return __float2bfloat16_rn(v);
+    }
+};
+
+template <>
+struct Pack<__half> {
+    static constexpr int kPerWord = 2;
+    static __device__ __forceinline__ void unpack(unsigned w, float *d) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w));
+        d[0] = f.x;
+        d[1] = f.y;
+    }
+    static __device__ __forceinline__ unsigned pack(const float *d) {
+        const __half2 h = __floats2half2_rn(d[0], d[1]);
+        return *reinterpret_cast<const unsigned *>(&h);
+    }
+    static __device__ __forceinline__ float scalar(__half v) {
+        return __half2float(v);
+    }
+    static __device__ __forceinline__ __half from(float v) {
+        return __float2half_rn(v);
+    }
+};
+
+template <typename T>
+__device__ __forceinline__ float to_f(T v) {
+    return Pack<T>::scalar(v);
+}
+template <typename T>
+__device__ __forceinline__ T from_f(float v) {
+    return Pack<T>::from(v);
+}
+
+// ---- vector access ---------------------------------------------------------
+// V values of type T at p (aligned to V*sizeof(T) bytes), widened to FP32.
+// RO selects the read-only data path, used only for the parameter vectors,
+// which no kernel writes.
+template <typename T, int V, bool RO = false>
+__device__ __forceinline__ void ld_vec(const T *p, float *d) {
+    constexpr int kBytes = V * (int)sizeof(T);
+    if constexpr (kBytes >= 4) {
+        constexpr int NW = kBytes / 4;
+        unsigned w[NW];
+        if constexpr (NW == 4) {
+            const uint4 u = RO ? __ldg(reinterpret_cast<const uint4 *>(p))
+                               : *reinterpret_cast<const uint4 *>(p);
+            w[0] = u.x; w[1] = u.y; w[2] = u.z; w[3] = u.w;
+        } else if constexpr (NW == 2) {
+            const uint2 u = RO ? __ldg(reinterpret_cast<const uint2 *>(p))
+                               : *reinterpret_cast<const uint2 *>(p);
+            w[0] = u.x; w[1] = u.y;
+        } else {
+            w[0] = RO ? __ldg(reinterpret_cast<const unsigned *>(p))
+                      : *reinterpret_cast<const unsigned *>(p);
+        }
+#pragma unroll
+        for (int i = 0; i < NW; ++i)
+            Pack<T>::unpack(w[i], d + i * Pack<T>::kPerWord);
     } else {
-        d[0] = *p;
+        d[0] = to_f(RO ? __ldg(p) : *p);
     }
 }
 
-// Read-only parameter vectors (weight, gamma, beta): never written by the
-// kernel, so the read-only data path is safe.
-template <int V>
-__device__ __forceinline__ void ldg_vec(const float *p, float *d) {
-    if constexpr (V == 4) {
-        const float4 t = __ldg(reinterpret_cast<const float4 *>(p));
-        d[0] = t.x; d[1] = t.y; d[2] = t.z; d[3] = t.w;
-    } else if constexpr (V == 2) {
-        const float2 t = __ldg(reinterpret_cast<const float2 *>(p));
-        d[0] = t.x; d[1] = t.y;
+// V FP32 values rounded to T and stored at p (aligned to V*sizeof(T)).
+template <typename T, int V>
+__device__ __forceinline__ void st_vec(T *p, const float *d) {
+    constexpr int kBytes = V * (int)sizeof(T);
+    if constexpr (kBytes >= 4) {
+        constexpr int NW = kBytes / 4;
+        constexpr int PW = Pack<T>::kPerWord;
+        unsigned w[NW];
+#pragma unroll
+        for (int i = 0; i < NW; ++i) w[i] = Pack<T>::pack(d + i * PW);
+        if constexpr (NW == 4) {
+            *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+        } else if constexpr (NW == 2) {
+            *reinterpret_cast<uint2 *>(p) = make_uint2(w[0], w[1]);
+        } else {
+            *reinterpret_cast<unsigned *>(p) = w[0];
+        }
     } else {
-        d[0] = __ldg(p);
-    }
-}
-
-template <int V>
-__device__ __forceinline__ void st_vec(float *p, const float *d) {
-    if constexpr (V == 4) {
-        *reinterpret_cast<float4 *>(p) = make_float4(d[0], d[1], d[2], d[3]);
-    } else if constexpr (V == 2) {
-        *reinterpret_cast<float2 *>(p) = make_float2(d[0], d[1]);
-    } else {
-        *p = d[0];
+        *p = from_f<T>(d[0]);
     }
 }
 
 // Up to V values of a parameter vector starting at column `col`; only the
 // first `nv` exist (the rest, and every value of a NULL vector, read as
-// `dflt`).  `vec` says the address is 4V-byte aligned.
-template <int V>
-__device__ __forceinline__ void param_pack(const float *p, int col, int nv,
+// `dflt`).  `vec` says the address is V*sizeof(T)-byte aligned.
+template <typename T, int V>
+__device__ __forceinline__ void param_pack(const T *p, int col, int nv,
                                            bool vec, float dflt, float *d) {
     if (p == nullptr || nv <= 0) {
 #pragma unroll
         for (int e = 0; e < V; ++e) d[e] = dflt;
     } else if (vec && nv == V) {
-        ldg_vec<V>(p + col, d);
+        ld_vec<T, V, true>(p + col, d);
     } else {
 #pragma unroll
-        for (int e = 0; e < V; ++e) d[e] = e < nv ? __ldg(p + col + e) : dflt;
+        for (int e = 0; e < V; ++e)
+            d[e] = e < nv ? to_f(__ldg(p + col + e)) : dflt;
     }
+}
+
+template <typename T>
+__device__ __forceinline__ float param_at(const T *p, int col, float dflt) {
+    return p ? to_f(__ldg(p + col)) : dflt;
 }
 
 // ---- cooperative reductions ---------------------------------------------
@@ -293,55 +390,52 @@ __device__ __forceinline__ void prefetch_l2(const void *p, int64_t bytes) {
     }
 }
 
+// L2 prefetch of row group g (x and, for residual LayerNorm, the residual).
+template <int OP, typename T>
+__device__ __forceinline__ void prefetch_group(const KArgs &a, int64_t g) {
+    const int64_t r0 = g * a.B;
+    if (r0 >= a.rows) return;
+    const int64_t nr = a.rows - r0 < a.B ? a.rows - r0 : a.B;
+    const int64_t bytes = nr * (int64_t)a.cols * (int64_t)sizeof(T);
+    prefetch_l2(static_cast<const T *>(a.x) + r0 * a.cols, bytes);
+    if constexpr (OP == OP_RESIDUAL_LAYERNORM)
+        prefetch_l2(static_cast<const T *>(a.res) + r0 * a.cols, bytes);
+}
+
 // Persistent CTAs: with `prefetch_next`, thread 0 asks L2 for the row group
 // the CTA will process after `g`, so its DRAM reads overlap this one.
-template <int OP>
+template <int OP, typename T>
 __device__ __forceinline__ void prefetch_next_group(const KArgs &a,
                                                     int64_t g,
                                                     int64_t ngroups) {
     const int64_t gn = g + gridDim.x;
     if (!a.prefetch_next || threadIdx.x != 0 || gn >= ngroups) return;
-    const int64_t r0 = gn * a.B;
-    const int64_t nr = a.rows - r0 < a.B ? a.rows - r0 : a.B;
-    const int64_t bytes = nr * (int64_t)a.cols * 4;
-    prefetch_l2(a.x + r0 * a.cols, bytes);
-    if constexpr (OP == OP_RESIDUAL_LAYERNORM)
-        prefetch_l2(a.res + r0 * a.cols, bytes);
+    prefetch_group<OP, T>(a, gn);
 }
 
 // Kernel prologue: with `pdl`, thread 0 prefetches the CTA's first row group
-// (x and, for residual LayerNorm, the residual) into L2; then every thread
-// lets dependents launch and waits for the previous grid.
-template <int OP>
+// into L2; then every thread lets dependents launch and waits for the
+// previous grid.
+template <int OP, typename T>
 __device__ __forceinline__ void kernel_prologue(const KArgs &a) {
-    if (a.pdl && threadIdx.x == 0) {
-        const int64_t r0 = (int64_t)blockIdx.x * a.B;
-        if (r0 < a.rows) {
-            const int64_t nr = a.rows - r0 < a.B ? a.rows - r0 : a.B;
-            const int64_t bytes = nr * (int64_t)a.cols * 4;
-            prefetch_l2(a.x + r0 * a.cols, bytes);
-            if constexpr (OP == OP_RESIDUAL_LAYERNORM)
-                prefetch_l2(a.res + r0 * a.cols, bytes);
-        }
-    }
+    if (a.pdl && threadIdx.x == 0) prefetch_group<OP, T>(a, blockIdx.x);
     grid_launch_dependents();
     grid_wait_prerequisites();
 }
 
 // ---- per-row geometry ------------------------------------------------------
-template <int V, bool AL>
+template <typename T, int V, bool AL>
 struct RowGeom {
     int64_t base;  // element offset of the row
     int hd;        // head length (unaligned kernels only)
     int nb;        // body length
-    __device__ __forceinline__ RowGeom(const float *x, int64_t row,
-                                       int cols) {
+    __device__ __forceinline__ RowGeom(const T *x, int64_t row, int cols) {
         base = row * (int64_t)cols;
         hd = 0;
         if constexpr (!AL && V > 1) {
-            const unsigned words =
-                (unsigned)(reinterpret_cast<uintptr_t>(x + base) >> 2);
-            hd = (int)((0u - words) & (unsigned)(V - 1));
+            const unsigned elems = (unsigned)(
+                reinterpret_cast<uintptr_t>(x + base) / sizeof(T));
+            hd = (int)((0u - elems) & (unsigned)(V - 1));
             hd = hd < cols ? hd : cols;
         }
         nb = cols - hd;
@@ -352,80 +446,84 @@ struct RowGeom {
 // start + head): a vector access for a complete pack when `vec`, otherwise
 // guarded scalars; missing values read as `fill`.  In aligned kernels
 // (AL) cols % V == 0, so a pack is either complete or wholly past the end.
-template <int V, bool AL>
-__device__ __forceinline__ void load_pack(const float *p, int off, int nb,
+template <typename T, int V, bool AL>
+__device__ __forceinline__ void load_pack(const T *p, int off, int nb,
                                           bool active, bool vec, float fill,
                                           float *d) {
     if constexpr (AL) {
         if (active && off < nb) {
-            ld_vec<V>(p + off, d);
+            ld_vec<T, V>(p + off, d);
         } else {
 #pragma unroll
             for (int e = 0; e < V; ++e) d[e] = fill;
         }
     } else if (active && off + V <= nb) {
         if (vec) {
-            ld_vec<V>(p + off, d);
+            ld_vec<T, V>(p + off, d);
         } else {
 #pragma unroll
-            for (int e = 0; e < V; ++e) d[e] = p[off + e];
+            for (int e = 0; e < V; ++e) d[e] = to_f(p[off + e]);
         }
     } else {
 #pragma unroll
         for (int e = 0; e < V; ++e)
-            d[e] = (active && off + e < nb) ? p[off + e] : fill;
+            d[e] = (active && off + e < nb) ? to_f(p[off + e]) : fill;
     }
 }
 
-template <int V, bool AL>
-__device__ __forceinline__ void store_pack(float *p, int off, int nb,
+template <typename T, int V, bool AL>
+__device__ __forceinline__ void store_pack(T *p, int off, int nb,
                                            bool active, bool vec,
                                            const float *d) {
     if (!active) return;
     if constexpr (AL) {
-        if (off < nb) st_vec<V>(p + off, d);
+        if (off < nb) st_vec<T, V>(p + off, d);
     } else if (off + V <= nb) {
         if (vec) {
-            st_vec<V>(p + off, d);
+            st_vec<T, V>(p + off, d);
         } else {
 #pragma unroll
-            for (int e = 0; e < V; ++e) p[off + e] = d[e];
+            for (int e = 0; e < V; ++e) p[off + e] = from_f<T>(d[e]);
         }
     } else {
 #pragma unroll
         for (int e = 0; e < V; ++e)
-            if (off + e < nb) p[off + e] = d[e];
+            if (off + e < nb) p[off + e] = from_f<T>(d[e]);
     }
 }
 
 // Parameter pack for the register path: aligned kernels read complete
 // vectors (or nothing past the end), the others guard each element.
-template <int V, bool AL>
-__device__ __forceinline__ void param_row_pack(const float *p, int col,
+template <typename T, int V, bool AL>
+__device__ __forceinline__ void param_row_pack(const T *p, int col,
                                                int off, int nb, bool active,
                                                float dflt, float *d) {
     if constexpr (AL) {
         if (p != nullptr && active && off < nb) {
-            ldg_vec<V>(p + col, d);
+            ld_vec<T, V, true>(p + col, d);
         } else {
 #pragma unroll
             for (int e = 0; e < V; ++e) d[e] = dflt;
         }
     } else {
         const int nv = active ? min(max(nb - off, 0), V) : 0;
-        param_pack<V>(p, col, nv, false, dflt, d);
+        param_pack<T, V>(p, col, nv, false, dflt, d);
     }
 }
 
 // =========================================================================
 // Register path
 // =========================================================================
-template <int OP, int V, int K, bool AL>
+template <int OP, typename T, int V, int K, bool AL>
 __global__ void __launch_bounds__(reg_max_threads(V * K))
     reg_kernel(const KArgs a) {
-    kernel_prologue<OP>(a);
+    kernel_prologue<OP, T>(a);
     __shared__ RedScratch red;
     int parity = 0;
+    const T *X = static_cast<const T *>(a.x);
+    const T *Wt = static_cast<const T *>(a.w);
+    const T *Bt = static_cast<const T *>(a.b);
+    T *Y = static_cast<T *>(a.y);
     const int W = a.W;
     const int worker = threadIdx.x & (W - 1);
     const int slot = threadIdx.x >> a.log2W;
@@ -437,11 +535,11 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
     const bool yvec = AL || a.y_vec;
 
     for (int64_t g = blockIdx.x; g < ngroups; g += gridDim.x) {
-        prefetch_next_group<OP>(a, g, ngroups);
+        prefetch_next_group<OP, T>(a, g, ngroups);
         const int64_t row = g * a.B + slot;
         const bool active = row < a.rows;
-        const RowGeom<V, AL> geo(a.x, active ? row : 0, cols);
-        const float *xb = a.x + geo.base + geo.hd;  // body start
+        const RowGeom<T, V, AL> geo(X, active ? row : 0, cols);
+        const T *xb = X + geo.base + geo.hd;  // body start
         const int nb = geo.nb;
         const bool head = kHead && active && worker < geo.hd;
 
@@ -450,30 +548,32 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
         float hv = fill;
 #pragma unroll
         for (int k = 0; k < K; ++k)
-            load_pack<V, AL>(xb, (k * W + worker) * V, nb, active, true, fill,
-                         v[k]);
-        if (head) hv = a.x[geo.base + worker];
+            load_pack<T, V, AL>(xb, (k * W + worker) * V, nb, active, true,
+                                fill, v[k]);
+        if (head) hv = to_f(X[geo.base + worker]);
 
         if constexpr (OP == OP_RESIDUAL_LAYERNORM) {
-            const float *rb = a.res + geo.base + geo.hd;
+            const T *R = static_cast<const T *>(a.res);
+            const T *rb = R + geo.base + geo.hd;
             const bool rvec = AL || a.r_vec;
 #pragma unroll
             for (int k = 0; k < K; ++k) {
                 float t[V];
-                load_pack<V, AL>(rb, (k * W + worker) * V, nb, active, rvec, 0.f,
-                             t);
+                load_pack<T, V, AL>(rb, (k * W + worker) * V, nb, active,
+                                    rvec, 0.f, t);
 #pragma unroll
                 for (int e = 0; e < V; ++e) v[k][e] = __fadd_rn(v[k][e], t[e]);
             }
-            if (head) hv = __fadd_rn(hv, a.res[geo.base + worker]);
+            if (head) hv = __fadd_rn(hv, to_f(R[geo.base + worker]));
             if (a.h != nullptr) {
-                float *hb = a.h + geo.base + geo.hd;
+                T *H = static_cast<T *>(a.h);
+                T *hb = H + geo.base + geo.hd;
                 const bool hvec = AL || a.h_vec;
 #pragma unroll
                 for (int k = 0; k < K; ++k)
-                    store_pack<V, AL>(hb, (k * W + worker) * V, nb, active, hvec,
-                                  v[k]);
-                if (head) a.h[geo.base + worker] = hv;
+                    store_pack<T, V, AL>(hb, (k * W + worker) * V, nb, active,
+                                         hvec, v[k]);
+                if (head) H[geo.base + worker] = from_f<T>(hv);
             }
         }
 
@@ -483,7 +583,7 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
         if constexpr (OP == OP_CROSS_ENTROPY) {
             if (active && worker == 0) {
                 const int32_t lab = __ldg(a.labels + row);
-                xl = (lab >= 0 && lab < cols) ? a.x[geo.base + lab] : NAN;
+                xl = (lab >= 0 && lab < cols) ? to_f(X[geo.base + lab]) : NAN;
             }
         }
 
@@ -495,27 +595,27 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
 #pragma unroll
             for (int k = 0; k < K; ++k)
 #pragma unroll
-                for (int e = 0; e < V; ++e) acc[e] = fmaf(v[k][e], v[k][e], acc[e]);
+                for (int e = 0; e < V; ++e)
+                    acc[e] = fmaf(v[k][e], v[k][e], acc[e]);
             float ss = hv * hv;
 #pragma unroll
             for (int e = 0; e < V; ++e) ss += acc[e];
             ss = row_allreduce<SumOp>(ss, W, red, parity);
             const float r = rsqrtf(ss / (float)cols + a.eps);
-            float *yb = a.y + geo.base + geo.hd;
+            T *yb = Y + geo.base + geo.hd;
 #pragma unroll
             for (int k = 0; k < K; ++k) {
                 const int off = (k * W + worker) * V;
                 float wv[V], o[V];
-                param_row_pack<V, AL>(a.w, geo.hd + off, off, nb, active, 1.f,
-                                      wv);
+                param_row_pack<T, V, AL>(Wt, geo.hd + off, off, nb, active,
+                                         1.f, wv);
 #pragma unroll
                 for (int e = 0; e < V; ++e) o[e] = v[k][e] * r * wv[e];
-                store_pack<V, AL>(yb, off, nb, active, yvec, o);
+                store_pack<T, V, AL>(yb, off, nb, active, yvec, o);
             }
-            if (head) {
-                const float wh = a.w ? __ldg(a.w + worker) : 1.f;
-                a.y[geo.base + worker] = hv * r * wh;
-            }
+            if (head)
+                Y[geo.base + worker] =
+                    from_f<T>(hv * r * param_at(Wt, worker, 1.f));
         } else if constexpr (OP == OP_LAYERNORM ||
                              OP == OP_RESIDUAL_LAYERNORM) {
             float acc[V];
@@ -550,25 +650,24 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
             for (int e = 0; e < V; ++e) q += acc[e];
             q = row_allreduce<SumOp>(q, W, red, parity);
             const float rstd = rsqrtf(q / (float)cols + a.eps);
-            float *yb = a.y + geo.base + geo.hd;
+            T *yb = Y + geo.base + geo.hd;
 #pragma unroll
             for (int k = 0; k < K; ++k) {
                 const int off = (k * W + worker) * V;
                 float gv[V], bv[V], o[V];
-                param_row_pack<V, AL>(a.w, geo.hd + off, off, nb, active, 1.f,
-                                      gv);
-                param_row_pack<V, AL>(a.b, geo.hd + off, off, nb, active, 0.f,
-                                      bv);
+                param_row_pack<T, V, AL>(Wt, geo.hd + off, off, nb, active,
+                                         1.f, gv);
+                param_row_pack<T, V, AL>(Bt, geo.hd + off, off, nb, active,
+                                         0.f, bv);
 #pragma unroll
                 for (int e = 0; e < V; ++e)
                     o[e] = fmaf((v[k][e] - mean) * rstd, gv[e], bv[e]);
-                store_pack<V, AL>(yb, off, nb, active, yvec, o);
+                store_pack<T, V, AL>(yb, off, nb, active, yvec, o);
             }
-            if (head) {
-                const float gh = a.w ? __ldg(a.w + worker) : 1.f;
-                const float bh = a.b ? __ldg(a.b + worker) : 0.f;
-                a.y[geo.base + worker] = fmaf((hv - mean) * rstd, gh, bh);
-            }
+            if (head)
+                Y[geo.base + worker] = from_f<T>(
+                    fmaf((hv - mean) * rstd, param_at(Wt, worker, 1.f),
+                         param_at(Bt, worker, 0.f)));
         } else if constexpr (OP == OP_SOFTMAX) {
             float mx[V];
 #pragma unroll
@@ -600,15 +699,16 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
             for (int e = 0; e < V; ++e) s += acc[e];
             s = row_allreduce<SumOp>(s, W, red, parity);
             const float inv = 1.f / s;
-            float *yb = a.y + geo.base + geo.hd;
+            T *yb = Y + geo.base + geo.hd;
 #pragma unroll
             for (int k = 0; k < K; ++k) {
                 float o[V];
 #pragma unroll
                 for (int e = 0; e < V; ++e) o[e] = v[k][e] * inv;
-                store_pack<V, AL>(yb, (k * W + worker) * V, nb, active, yvec, o);
+                store_pack<T, V, AL>(yb, (k * W + worker) * V, nb, active,
+                                     yvec, o);
             }
-            if (head) a.y[geo.base + worker] = hv * inv;
+            if (head) Y[geo.base + worker] = from_f<T>(hv * inv);
         } else if constexpr (OP == OP_ROW_SUM) {
             float s = hv, c = 0.f;
 #pragma unroll
@@ -685,12 +785,18 @@ __device__ __forceinline__ void stream_row(int worker, int W, int hd, int nb,
     }
 }
 
-template <int OP, int V, bool AL>
+template <int OP, typename T, int V, bool AL>
 __global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
-    kernel_prologue<OP>(a);
-    constexpr int U = 4;
+    kernel_prologue<OP, T>(a);
+    // Packs in flight per thread: 4, or 2 for 8-value packs (keeps the
+    // residual LayerNorm variants within the register budget).
+    constexpr int U = V >= 8 ? 2 : 4;
     __shared__ RedScratch red;
     int parity = 0;
+    const T *X = static_cast<const T *>(a.x);
+    const T *Wt = static_cast<const T *>(a.w);
+    const T *Bt = static_cast<const T *>(a.b);
+    T *Y = static_cast<T *>(a.y);
     const int W = a.W;
     const int worker = threadIdx.x & (W - 1);
     const int slot = threadIdx.x >> a.log2W;
@@ -699,43 +805,46 @@ __global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
     const bool yvec = AL || a.y_vec;
 
     for (int64_t g = blockIdx.x; g < ngroups; g += gridDim.x) {
-        prefetch_next_group<OP>(a, g, ngroups);
+        prefetch_next_group<OP, T>(a, g, ngroups);
         const int64_t row = g * a.B + slot;
         const bool active = row < a.rows;
-        const RowGeom<V, AL> geo(a.x, active ? row : 0, cols);
+        const RowGeom<T, V, AL> geo(X, active ? row : 0, cols);
         const int64_t base = geo.base;
         const int hd = geo.hd, nb = geo.nb;
-        const float *xb = a.x + base + hd;
-        const float *xrow = a.x + base;
+        const T *xb = X + base + hd;
+        const T *xrow = X + base;
         // Loads the (residual-added) input values of one pack or the head.
         auto load_x = [&](int off, int nv, float *t) {
             if (off < 0) {
-                t[0] = xrow[-1 - off];
+                t[0] = to_f(xrow[-1 - off]);
                 if constexpr (OP == OP_RESIDUAL_LAYERNORM)
-                    t[0] = __fadd_rn(t[0], a.res[base - 1 - off]);
+                    t[0] = __fadd_rn(
+                        t[0], to_f(static_cast<const T *>(a.res)[base - 1 - off]));
                 return;
             }
             if (nv == V) {
-                ld_vec<V>(xb + off, t);
+                ld_vec<T, V>(xb + off, t);
             } else {
 #pragma unroll
-                for (int e = 0; e < V; ++e) t[e] = e < nv ? xb[off + e] : 0.f;
+                for (int e = 0; e < V; ++e)
+                    t[e] = e < nv ? to_f(xb[off + e]) : 0.f;
             }
             if constexpr (OP == OP_RESIDUAL_LAYERNORM) {
-                const float *rb = a.res + base + hd;
+                const T *rb = static_cast<const T *>(a.res) + base + hd;
                 float r[V];
                 if (nv == V && (AL || a.r_vec)) {
-                    ld_vec<V>(rb + off, r);
+                    ld_vec<T, V>(rb + off, r);
                 } else {
 #pragma unroll
-                    for (int e = 0; e < V; ++e) r[e] = e < nv ? rb[off + e] : 0.f;
+                    for (int e = 0; e < V; ++e)
+                        r[e] = e < nv ? to_f(rb[off + e]) : 0.f;
                 }
 #pragma unroll
                 for (int e = 0; e < V; ++e) t[e] = __fadd_rn(t[e], r[e]);
             }
         };
-        // Column of element e of a pack at body offset `off` (or the head).
-        auto column = [&](int off, int e) { return off < 0 ? -1 - off : hd + off + e; };
+        // Column of a head element (off < 0).
+        auto column = [&](int off) { return -1 - off; };
 
         if constexpr (OP == OP_RMSNORM) {
             float ss = 0.f;
@@ -747,21 +856,20 @@ __global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
                                  });
             ss = row_allreduce<SumOp>(ss, W, red, parity);
             const float r = rsqrtf(ss / (float)cols + a.eps);
-            float *yb = a.y + base + hd;
+            T *yb = Y + base + hd;
             stream_row<V, AL, U>(
                 worker, W, hd, nb, active, load_x,
                 [&](const float *t, int nv, int off) {
-                    float o[V];
                     if (off < 0) {
-                        const int c = column(off, 0);
-                        a.y[base + c] = t[0] * r * (a.w ? __ldg(a.w + c) : 1.f);
+                        const int c = column(off);
+                        Y[base + c] = from_f<T>(t[0] * r * param_at(Wt, c, 1.f));
                         return;
                     }
-                    float wv[V];
-                    param_pack<V>(a.w, hd + off, nv, AL, 1.f, wv);
+                    float wv[V], o[V];
+                    param_pack<T, V>(Wt, hd + off, nv, AL, 1.f, wv);
 #pragma unroll
                     for (int e = 0; e < V; ++e) o[e] = t[e] * r * wv[e];
-                    store_pack<V, AL>(yb, off, nb, true, yvec, o);
+                    store_pack<T, V, AL>(yb, off, nb, true, yvec, o);
                 });
         } else if constexpr (OP == OP_LAYERNORM ||
                              OP == OP_RESIDUAL_LAYERNORM) {
@@ -786,29 +894,31 @@ __global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
                                  });
             q = row_allreduce<SumOp>(q, W, red, parity);
             const float rstd = rsqrtf(q / (float)cols + a.eps);
-            float *yb = a.y + base + hd;
-            float *hb = a.h ? a.h + base + hd : nullptr;
+            T *yb = Y + base + hd;
+            T *H = static_cast<T *>(a.h);
+            T *hb = H ? H + base + hd : nullptr;
             const bool hvec = AL || a.h_vec;
             stream_row<V, AL, U>(
                 worker, W, hd, nb, active, load_x,
                 [&](const float *t, int nv, int off) {
                     if (off < 0) {
-                        const int c = column(off, 0);
-                        const float gh = a.w ? __ldg(a.w + c) : 1.f;
-                        const float bh = a.b ? __ldg(a.b + c) : 0.f;
-                        a.y[base + c] = fmaf((t[0] - mean) * rstd, gh, bh);
-                        if (OP == OP_RESIDUAL_LAYERNORM && a.h) a.h[base + c] = t[0];
+                        const int c = column(off);
+                        Y[base + c] = from_f<T>(fmaf((t[0] - mean) * rstd,
+                                                     param_at(Wt, c, 1.f),
+                                                     param_at(Bt, c, 0.f)));
+                        if (OP == OP_RESIDUAL_LAYERNORM && H)
+                            H[base + c] = from_f<T>(t[0]);
                         return;
                     }
                     float gv[V], bv[V], o[V];
-                    param_pack<V>(a.w, hd + off, nv, AL, 1.f, gv);
-                    param_pack<V>(a.b, hd + off, nv, AL, 0.f, bv);
+                    param_pack<T, V>(Wt, hd + off, nv, AL, 1.f, gv);
+                    param_pack<T, V>(Bt, hd + off, nv, AL, 0.f, bv);
 #pragma unroll
                     for (int e = 0; e < V; ++e)
                         o[e] = fmaf((t[e] - mean) * rstd, gv[e], bv[e]);
-                    store_pack<V, AL>(yb, off, nb, true, yvec, o);
+                    store_pack<T, V, AL>(yb, off, nb, true, yvec, o);
                     if (OP == OP_RESIDUAL_LAYERNORM && hb)
-                        store_pack<V, AL>(hb, off, nb, true, hvec, t);
+                        store_pack<T, V, AL>(hb, off, nb, true, hvec, t);
                 });
         } else if constexpr (OP == OP_SOFTMAX || OP == OP_CROSS_ENTROPY) {
             float m = -INFINITY, s = 0.f;
@@ -827,24 +937,25 @@ __global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
             row_allreduce_lse(m, s, W, red, parity);
             if constexpr (OP == OP_SOFTMAX) {
                 const float inv = 1.f / s;
-                float *yb = a.y + base + hd;
+                T *yb = Y + base + hd;
                 stream_row<V, AL, U>(
                     worker, W, hd, nb, active, load_x,
                     [&](const float *t, int nv, int off) {
                         if (off < 0) {
-                            a.y[base + column(off, 0)] = expf(t[0] - m) * inv;
+                            Y[base + column(off)] =
+                                from_f<T>(expf(t[0] - m) * inv);
                             return;
                         }
                         float o[V];
 #pragma unroll
                         for (int e = 0; e < V; ++e) o[e] = expf(t[e] - m) * inv;
-                        store_pack<V, AL>(yb, off, nb, true, yvec, o);
+                        store_pack<T, V, AL>(yb, off, nb, true, yvec, o);
                     });
             } else {
                 if (active && worker == 0) {
                     const int32_t lab = __ldg(a.labels + row);
                     const float xl =
-                        (lab >= 0 && lab < cols) ? a.x[base + lab] : NAN;
+                        (lab >= 0 && lab < cols) ? to_f(X[base + lab]) : NAN;
                     a.out[row] = (m + logf(s)) - xl;
                 }
             }
@@ -872,51 +983,57 @@ __global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
 // =========================================================================
 using KernelFn = void (*)(KArgs);
 
-template <int OP, int V, bool AL>
+template <int OP, typename T, int V, bool AL>
 __host__ KernelFn reg_kernel_for_chunks(int K) {
     switch (K) {
-        case 1: return reg_kernel<OP, V, 1, AL>;
-        case 2: return reg_kernel<OP, V, 2, AL>;
-        case 4: return reg_kernel<OP, V, 4, AL>;
-        case 8: return reg_kernel<OP, V, 8, AL>;
-        case 16: return reg_kernel<OP, V, 16, AL>;
+        case 1: return reg_kernel<OP, T, V, 1, AL>;
+        case 2: return reg_kernel<OP, T, V, 2, AL>;
+        case 4: return reg_kernel<OP, T, V, 4, AL>;
+        case 8: return reg_kernel<OP, T, V, 8, AL>;
+        case 16: return reg_kernel<OP, T, V, 16, AL>;
         default: return nullptr;
     }
 }
 
-template <int OP>
-__host__ KernelFn select_kernel(const mt_plan_t &p, bool aligned) {
-    const int V = p.values_per_thread;
+// A pack of one FP32 value needs no alignment head, so it has only the
+// aligned kernels.
+template <int OP, typename T, int V>
+__host__ KernelFn kernel_for(const mt_plan_t &p, bool aligned) {
+    constexpr bool kOnlyAligned = (V == 1 && sizeof(T) == 4);
     if (p.path == MT_PATH_LOOP) {
-        if (V == 1) return loop_kernel<OP, 1, true>;
-        if (V == 2) return aligned ? loop_kernel<OP, 2, true> : loop_kernel<OP, 2, false>;
-        if (V == 4) return aligned ? loop_kernel<OP, 4, true> : loop_kernel<OP, 4, false>;
-        return nullptr;
+        if (kOnlyAligned || aligned) return loop_kernel<OP, T, V, true>;
+        return loop_kernel<OP, T, V, kOnlyAligned>;
     }
-    if (V == 1) return reg_kernel_for_chunks<OP, 1, true>(p.chunks);
-    if (V == 2)
-        return aligned ? reg_kernel_for_chunks<OP, 2, true>(p.chunks)
-                       : reg_kernel_for_chunks<OP, 2, false>(p.chunks);
-    if (V == 4)
-        return aligned ? reg_kernel_for_chunks<OP, 4, true>(p.chunks)
-                       : reg_kernel_for_chunks<OP, 4, false>(p.chunks);
+    if (kOnlyAligned || aligned)
+        return reg_kernel_for_chunks<OP, T, V, true>(p.chunks);
+    return reg_kernel_for_chunks<OP, T, V, kOnlyAligned>(p.chunks);
+}
+
+// Instantiated values per thread per chunk: FP32 V = 1, 2, 4 (4-, 8- and
+// 16-byte packs); FP16/BF16 V = 2, 4, 8 (4-, 8- and 16-byte packs).
+template <int OP, typename T>
+__host__ KernelFn select_kernel(const mt_plan_t &p, bool aligned) {
+    if constexpr (sizeof(T) == 4) {
+        switch (p.values_per_thread) {
+            case 1: return kernel_for<OP, T, 1>(p, aligned);
+            case 2: return kernel_for<OP, T, 2>(p, aligned);
+            case 4: return kernel_for<OP, T, 4>(p, aligned);
+        }
+    } else {
+        switch (p.values_per_thread) {
+            case 2: return kernel_for<OP, T, 2>(p, aligned);
+            case 4: return kernel_for<OP, T, 4>(p, aligned);
+            case 8: return kernel_for<OP, T, 8>(p, aligned);
+        }
+    }
     return nullptr;
 }
 
-template <int OP>
+template <int OP, typename T>
 __host__ cudaError_t launch_op(const mt_plan_t &p, const KArgs &a,
-                               bool aligned, cudaStream_t stream,
-                               int *max_threads_out) {
-    KernelFn k = select_kernel<OP>(p, aligned);
+                               bool aligned, cudaStream_t stream) {
+    KernelFn k = select_kernel<OP, T>(p, aligned);
     if (k == nullptr) return cudaErrorInvalidValue;
-    if (max_threads_out) {
-        cudaFuncAttributes attr;
-        cudaError_t e = cudaFuncGetAttributes(&attr, k);
-        if (e != cudaSuccess) return e;
-        *max_threads_out = attr.maxThreadsPerBlock;
-        if (p.threads_per_row * p.rows_per_block > attr.maxThreadsPerBlock)
-            return cudaErrorLaunchOutOfResources;
-    }
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -930,10 +1047,10 @@ __host__ cudaError_t launch_op(const mt_plan_t &p, const KArgs &a,
     return cudaLaunchKernelEx(&cfg, k, a);
 }
 
-template <int OP>
+template <int OP, typename T>
 __host__ cudaError_t occupancy_op(const mt_plan_t &p, bool aligned,
                                   int *blocks_per_sm) {
-    KernelFn k = select_kernel<OP>(p, aligned);
+    KernelFn k = select_kernel<OP, T>(p, aligned);
     if (k == nullptr) return cudaErrorInvalidValue;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
         blocks_per_sm, k, p.threads_per_row * p.rows_per_block, 0);
@@ -941,14 +1058,16 @@ __host__ cudaError_t occupancy_op(const mt_plan_t &p, bool aligned,
 
 }  // namespace mt
 
-#define MT_DEFINE_LAUNCHER(name, OPV)                                        \
+// One translation unit per (operator, storage type) defines its launcher
+// pair through this macro.
+#define MT_DEFINE_LAUNCHER(name, OPV, TYPE)                                  \
     namespace mt {                                                           \
     cudaError_t name(const mt_plan_t &plan, const KArgs &a, bool aligned,    \
-                     cudaStream_t stream, int *max_threads_out) {            \
-        return launch_op<OPV>(plan, a, aligned, stream, max_threads_out);    \
+                     cudaStream_t stream) {                                  \
+        return launch_op<OPV, TYPE>(plan, a, aligned, stream);               \
     }                                                                        \
     cudaError_t name##_occupancy(const mt_plan_t &plan, bool aligned,        \
                                  int *blocks_per_sm) {                       \
-        return occupancy_op<OPV>(plan, aligned, blocks_per_sm);              \
+        return occupancy_op<OPV, TYPE>(plan, aligned, blocks_per_sm);        \
     }                                                                        \
     }

@@ -24,6 +24,7 @@ namespace {
 
 struct PlanEntry {
     int op;
+    int dtype;
     int64_t cols_min, cols_max;  // inclusive
     int64_t rows_min, rows_max;  // inclusive
     mt_plan_t plan;
@@ -45,15 +46,24 @@ bool chunk_instantiated(int k) {
     return false;
 }
 
-// Heuristic plan for shapes the measured table does not cover: V = 4
-// (16-byte accesses), about `per_thread` values per thread, blocks of about
-// 256 threads; register path while one of the instantiated chunk counts
-// holds the row, else the loop path.
-mt_plan_t heuristic_plan(int op, int64_t rows, int64_t cols) {
+// Values per thread per chunk instantiated for a storage type: FP32 packs of
+// 1, 2, 4 values; FP16/BF16 packs of 2, 4, 8 values (4, 8, 16 bytes).
+bool v_instantiated(int dtype, int64_t V) {
+    if (dtype == DT_F32) return V == 1 || V == 2 || V == 4;
+    return V == 2 || V == 4 || V == 8;
+}
+
+// Heuristic plan for shapes the measured table does not cover: 16-byte
+// packs (V = 16 / element size), about `per_thread` values per thread,
+// blocks of about 256 threads; register path while one of the instantiated
+// chunk counts holds the row, else the loop path.
+mt_plan_t heuristic_plan(int op, int dtype, int64_t rows, int64_t cols) {
     (void)op;
     mt_plan_t p;
     memset(&p, 0, sizeof(p));
-    p.values_per_thread = cols >= 16 ? 4 : 1;
+    const int vmax = 16 / dtype_size(dtype);
+    const int vmin = dtype == DT_F32 ? 1 : 2;
+    p.values_per_thread = cols >= 16 ? vmax : vmin;
     const int V = p.values_per_thread;
     const int64_t per_thread = rows >= 2048 ? 16 : 8;
     int64_t W = pow2_ceil((cols + per_thread - 1) / per_thread);
@@ -77,12 +87,13 @@ mt_plan_t heuristic_plan(int op, int64_t rows, int64_t cols) {
 
 }  // namespace
 
-mt_status plan_check(int op, int64_t cols, const mt_plan_t &p) {
+mt_status plan_check(int op, int dtype, int64_t cols, const mt_plan_t &p) {
     if (op < 0 || op >= OP_COUNT || cols < 1) return MT_ERR_INVALID_ARGUMENT;
+    if (dtype < 0 || dtype >= DT_COUNT) return MT_ERR_INVALID_ARGUMENT;
     const int64_t W = p.threads_per_row, V = p.values_per_thread;
     const int64_t B = p.rows_per_block;
     if (!is_pow2(W) || W > 1024) return MT_ERR_INVALID_ARGUMENT;
-    if (V != 1 && V != 2 && V != 4) return MT_ERR_INVALID_ARGUMENT;
+    if (!v_instantiated(dtype, V)) return MT_ERR_INVALID_ARGUMENT;
     // The alignment head (< V elements) is owned one element per worker.
     if (V > 1 && W < V) return MT_ERR_INVALID_ARGUMENT;
     if (B < 1 || B > 1024) return MT_ERR_INVALID_ARGUMENT;
@@ -107,19 +118,21 @@ mt_status plan_check(int op, int64_t cols, const mt_plan_t &p) {
     return MT_OK;
 }
 
-mt_status plan_lookup(int op, int64_t rows, int64_t cols, mt_plan_t *out) {
-    if (op < 0 || op >= OP_COUNT || rows < 0 || cols < 1 || out == nullptr)
+mt_status plan_lookup(int op, int dtype, int64_t rows, int64_t cols,
+                      mt_plan_t *out) {
+    if (op < 0 || op >= OP_COUNT || dtype < 0 || dtype >= DT_COUNT ||
+        rows < 0 || cols < 1 || out == nullptr)
         return MT_ERR_INVALID_ARGUMENT;
     for (const PlanEntry &e : kPlanTable) {
-        if (e.op != op || cols < e.cols_min || cols > e.cols_max ||
-            rows < e.rows_min || rows > e.rows_max)
+        if (e.op != op || e.dtype != dtype || cols < e.cols_min ||
+            cols > e.cols_max || rows < e.rows_min || rows > e.rows_max)
             continue;
-        if (plan_check(op, cols, e.plan) == MT_OK) {
+        if (plan_check(op, dtype, cols, e.plan) == MT_OK) {
             *out = e.plan;
             return MT_OK;
         }
     }
-    *out = heuristic_plan(op, rows, cols);
+    *out = heuristic_plan(op, dtype, rows, cols);
     return MT_OK;
 }
 
@@ -135,12 +148,23 @@ int64_t mt_private_slot_bound(int64_t n, int32_t W, int32_t V) {
 }
 
 mt_status mt_plan_query(int op, int64_t rows, int64_t cols, mt_plan_t *out) {
-    return mt::plan_lookup(op, rows, cols, out);
+    return mt::plan_lookup(op, MT_DTYPE_F32, rows, cols, out);
 }
 
 mt_status mt_plan_check(int op, int64_t cols, const mt_plan_t *plan) {
     if (plan == nullptr) return MT_ERR_INVALID_ARGUMENT;
-    return mt::plan_check(op, cols, *plan);
+    return mt::plan_check(op, MT_DTYPE_F32, cols, *plan);
+}
+
+mt_status mt_plan_query_dtype(int op, int dtype, int64_t rows, int64_t cols,
+                              mt_plan_t *out) {
+    return mt::plan_lookup(op, dtype, rows, cols, out);
+}
+
+mt_status mt_plan_check_dtype(int op, int dtype, int64_t cols,
+                              const mt_plan_t *plan) {
+    if (plan == nullptr) return MT_ERR_INVALID_ARGUMENT;
+    return mt::plan_check(op, dtype, cols, *plan);
 }
 
 size_t mt_describe_plan(const mt_plan_t *p, char *buf, size_t n) {

@@ -16,6 +16,10 @@ Recipe (NumPy ``default_rng(seed)``, PCG64, FP32 draws):
 
 The tuning seed is ``TUNE_SEED``; held-out validation uses ``HOLDOUT_SEED``.
 Workload ``k`` of a list uses ``seed + k``.
+
+For FP16 / BF16 storage the FP32 draws are rounded to the storage type
+(round to nearest even) by :func:`as_storage`; :func:`widen` gives back their
+exact FP32 values, which is what the oracle receives.
 """
 from __future__ import annotations
 
@@ -91,3 +95,45 @@ def integer_valued(rows: int, cols: int, seed: int, lo: int = -8,
     2^20 of them is an exact FP32 integer, whatever the addition order."""
     rng = np.random.default_rng(seed)
     return rng.integers(lo, hi + 1, (rows, cols)).astype(np.float32)
+
+
+STORAGE = ("f32", "f16", "bf16")
+_MATRICES = ("x", "residual", "weight", "gamma", "beta")
+
+
+def _bf16_bits(a: np.ndarray) -> np.ndarray:
+    """FP32 -> bfloat16 bit patterns, round to nearest even (NaN kept)."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+    r = (u + (((u >> 16) & 1) + 0x7FFF)) >> 16
+    r = np.where(np.isnan(a), (u >> 16) | 0x40, r)
+    return r.astype(np.uint16)
+
+
+def as_storage(d: dict, dtype: str) -> dict:
+    """The same inputs with matrices and parameter vectors in `dtype`
+    storage: float32 arrays for "f32", float16 for "f16", and uint16 bit
+    patterns for "bf16".  Labels and eps are unchanged."""
+    if dtype == "f32":
+        return dict(d)
+    out = dict(d)
+    for k in _MATRICES:
+        if k in d:
+            out[k] = (d[k].astype(np.float16) if dtype == "f16"
+                      else _bf16_bits(d[k]))
+    return out
+
+
+def widen(a: np.ndarray, dtype: str) -> np.ndarray:
+    """Exact FP32 values of an array in `dtype` storage."""
+    if dtype == "bf16":
+        return (a.astype(np.uint32) << 16).view(np.float32)
+    return a.astype(np.float32)
+
+
+def widen_all(d: dict, dtype: str) -> dict:
+    """`widen` applied to every matrix and parameter vector of `d`."""
+    out = dict(d)
+    for k in _MATRICES:
+        if k in d:
+            out[k] = widen(d[k], dtype)
+    return out

@@ -180,7 +180,7 @@ def write_table(records, path):
         "package's tuner",
         "// (row_reduction_gb300/tune.py) from timings on the GPU; do not "
         "edit by",
-        "// hand.  Entry: {op, cols_min, cols_max, rows_min, rows_max,",
+        "// hand.  Entry: {op, dtype, cols_min, cols_max, rows_min, rows_max,",
         "// {W, V, chunks, rows_per_block, path, grid, flags}}.  The last "
         "entry",
         "// (op -1) only terminates the list.",
@@ -188,23 +188,25 @@ def write_table(records, path):
     ]
     by = {}
     for r in records:
-        by.setdefault((r["op"], r["cols"]), []).append(r)
-    for (op, cols), recs in sorted(by.items(),
-                                   key=lambda kv: (B.OP_IDS[kv[0][0]],
-                                                   kv[0][1])):
+        by.setdefault((r["op"], r.get("dtype", "f32"), r["cols"]),
+                      []).append(r)
+    for (op, dt, cols), recs in sorted(
+            by.items(), key=lambda kv: (B.OP_IDS[kv[0][0]],
+                                        B.DTYPE_IDS[kv[0][1]], kv[0][2])):
         ranges = dict((r, (lo, hi)) for r, lo, hi in
                       _rows_ranges([x["rows"] for x in recs]))
         for r in sorted(recs, key=lambda x: x["rows"]):
             lo, hi = ranges[r["rows"]]
             w = r["winner"]
             lines.append(
-                f"    {{{B.OP_IDS[op]}, {cols}, {cols}, {lo}, {hi}, "
+                f"    {{{B.OP_IDS[op]}, {B.DTYPE_IDS[dt]}, {cols}, {cols}, "
+                f"{lo}, {hi}, "
                 f"{{{w['threads_per_row']}, {w['values_per_thread']}, "
                 f"{w['chunks']}, {w['rows_per_block']}, {w['path']}, "
                 f"{w['grid']}, {w.get('flags', 0)}}}}},  "
-                f"// {op} {r['rows']}x{cols}: "
+                f"// {op} {dt} {r['rows']}x{cols}: "
                 f"{r['winner_us']:.3f} us")
-    lines.append("    {-1, 0, 0, 0, 0, {0, 0, 0, 0, 0, 0, 0}},")
+    lines.append("    {-1, 0, 0, 0, 0, 0, {0, 0, 0, 0, 0, 0, 0}},")
     lines.append("};")
     with open(path, "w") as f:
         f.write("\n".join(lines) + "\n")

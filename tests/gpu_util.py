@@ -53,12 +53,18 @@ class Guarded:
     def ptr(self):
         return self.view.data_ptr()
 
+    @staticmethod
+    def _host(t):
+        if t.dtype in (torch.float16, torch.bfloat16):
+            t = t.float()
+        return t.cpu().numpy()
+
     def numpy(self):
-        return self.view.cpu().numpy()
+        return self._host(self.view)
 
     def check(self):
-        head = self.buf[:PAD + self.offset].cpu().numpy()
-        tail = self.buf[PAD + self.offset + self.n:].cpu().numpy()
+        head = self._host(self.buf[:PAD + self.offset])
+        tail = self._host(self.buf[PAD + self.offset + self.n:])
         for part in (head, tail):
             if np.isnan(self.fill):
                 assert np.isnan(part).all(), "guard region was written"

@@ -33,7 +33,7 @@ def header_symbols():
 
 def test_library_exports_every_declared_symbol():
     declared = header_symbols()
-    assert len(declared) == 18
+    assert len(declared) == 33
     L = mt.lib()
     for name in declared:
         assert hasattr(L, name), name
@@ -125,14 +125,36 @@ def test_plan_check(plan, cols, want):
 
 
 @pytest.mark.parametrize("op", list(mt.OP_IDS))
-def test_default_plans_are_legal(op):
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+def test_default_plans_are_legal(op, dtype):
     shapes = [(r, c) for r in (0, 1, 5, 17, 64, 1024, 65536)
               for c in (1, 2, 3, 4, 7, 31, 33, 127, 128, 129, 257, 1000,
                         1024, 4096, 4103, 8192, 16384, 32768, 100003)]
     for rows, cols in shapes:
-        p = mt.mt_plan_query(op, rows, cols)
-        assert mt.mt_plan_check(op, cols, p) == OK, (rows, cols, p)
+        p = mt.mt_plan_query_dtype(op, dtype, rows, cols)
+        assert mt.mt_plan_check_dtype(op, dtype, cols, p) == OK, \
+            (rows, cols, p)
         assert p.grid == 0
+        if dtype == "f32":
+            assert tuple(p.as_dict().values()) == tuple(
+                mt.mt_plan_query(op, rows, cols).as_dict().values())
+
+
+def test_plan_check_per_storage_type():
+    # FP32 packs hold 1, 2 or 4 values; FP16/BF16 packs 2, 4 or 8.
+    K = {1: 8, 2: 4, 4: 2, 8: 1}        # 512 * V * K = 4096
+    for V, want in ((1, OK), (2, OK), (4, OK), (8, INV)):
+        assert mt.mt_plan_check_dtype(0, "f32", 4096,
+                                      mt.make_plan(512, V, K[V], 1)) == want
+    for dt in ("f16", "bf16"):
+        for V, want in ((1, INV), (2, OK), (4, OK), (8, OK)):
+            assert mt.mt_plan_check_dtype(
+                0, dt, 4096, mt.make_plan(512, V, K[V], 1)) == want
+    assert mt.lib().mt_plan_check_dtype(0, 3, 4096, None) == INV
+    import ctypes
+    p = mt.make_plan(256, 4, 4, 1)
+    assert mt.lib().mt_plan_check_dtype(0, 3, 4096, ctypes.byref(p)) == INV
+    assert mt.lib().mt_plan_check_dtype(0, -1, 4096, ctypes.byref(p)) == INV
 
 
 def test_plan_query_errors_and_describe():
@@ -196,3 +218,30 @@ def test_forced_illegal_plan_fails_closed():
     assert f(A, None, A, 4, 4096, 1e-6, None, ctypes.byref(bad)) == INV
     # rows == 0 still validates the plan
     assert f(A, None, A, 0, 4096, 1e-6, None, ctypes.byref(bad)) == INV
+
+
+def test_generic_and_half_entry_points_validate_before_launch():
+    L = mt.lib()
+    f = L.mt_row_reduce_with_plan
+    # op, dtype, x, res, w, b, labels, y, h, out, mean, rows, cols, eps, s, plan
+    assert f(0, 2, A, None, None, None, None, A, None, None, None, 0, 8, 0.0,
+             None, None) == OK
+    # a pointer the operator does not take
+    assert f(0, 2, A, None, None, None, None, A, None, A, None, 4, 8, 0.0,
+             None, None) == INV
+    assert f(3, 0, A, None, A, None, None, A, None, None, None, 4, 8, 0.0,
+             None, None) == INV
+    # a missing required pointer / unknown op or dtype
+    assert f(4, 1, A, None, None, None, None, None, None, None, None, 4, 8,
+             0.0, None, None) == INV
+    assert f(6, 0, A, None, None, None, None, A, None, None, None, 4, 8, 0.0,
+             None, None) == INV
+    assert f(0, 3, A, None, None, None, None, A, None, None, None, 4, 8, 0.0,
+             None, None) == INV
+    # 16-bit storage needs 2-byte alignment; FP32 outputs need 4
+    assert L.mt_rmsnorm_bf16(A + 1, None, A, 4, 8, 1e-6, None) == INV
+    assert L.mt_rmsnorm_bf16(A + 2, None, A + 6, 0, 8, 1e-6, None) == OK
+    assert L.mt_row_sum_f16(A + 2, A + 2, 4, 8, None) == INV
+    assert L.mt_cross_entropy_bf16(A, None, A, None, 4, 8, None) == INV
+    assert L.mt_residual_layernorm_f16(A, None, None, None, A, None, 4, 8,
+                                       1e-5, None) == INV
