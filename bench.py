@@ -65,9 +65,9 @@ def job_value(bytes_per_step, steps, elapsed, world):
     return world * bytes_per_step * steps / elapsed / 1e9
 
 
-def plan_text(op, rows, cols):
+def plan_text(op, rows, cols, dtype="f32"):
     import row_reduction_gb300 as mt
-    return mt.mt_describe_plan(mt.mt_plan_query(op, rows, cols))
+    return mt.mt_describe_plan(mt.mt_plan_query_dtype(op, dtype, rows, cols))
 
 
 def measured_peak():
@@ -323,26 +323,34 @@ def run_ours(args, rank, world, local_rank):
 
 def run_sweep(l2, peak):
     """Every published shape: RMSNorm shapes and bandwidth sweep, then the
-    operator family, each timed like the headline."""
+    operator family, each timed like the headline; then the same RMSNorm
+    sweep and the family at 1024x4096 with BF16 and FP16 storage."""
     from row_reduction_gb300 import inputs
-    cases = [("rmsnorm", r, c, False) for r, c in inputs.RMSNORM_SHAPES]
-    cases += [("rmsnorm", r, c, True) for r, c in inputs.RMSNORM_SWEEP]
-    cases += [(op, r, c, False) for op in inputs.OPS if op != "rmsnorm"
-              for r, c in inputs.FAMILY_SHAPES]
+    cases = [("rmsnorm", r, c, False, "f32") for r, c in inputs.RMSNORM_SHAPES]
+    cases += [("rmsnorm", r, c, True, "f32") for r, c in inputs.RMSNORM_SWEEP]
+    cases += [(op, r, c, False, "f32") for op in inputs.OPS
+              if op != "rmsnorm" for r, c in inputs.FAMILY_SHAPES]
+    for dt in ("bf16", "f16"):
+        cases += [("rmsnorm", r, c, True, dt)
+                  for r, c in inputs.RMSNORM_SWEEP]
+        cases += [(op, 1024, 4096, False, dt) for op in inputs.OPS
+                  if op != "rmsnorm"]
     out = []
     import torch
-    for op, r, c, outl in cases:
+    for op, r, c, outl, dt in cases:
         work = Workload(op, r, c, inputs.TUNE_SEED, outliers=outl,
-                        l2_bytes=l2, max_pool_bytes=8 << 30)
+                        l2_bytes=l2, max_pool_bytes=8 << 30, dtype=dt)
         # about 0.25 s of timed work, at least 64 steps
         probe = time_graph_steps(work, 64, 16)
         steps = int(max(64, min(200000, 0.25 / max(probe / 64, 1e-7))))
         el = time_graph_steps(work, steps, max(16, steps // 20))
         us = el / steps * 1e6
         gbs = work.bytes / (el / steps) / 1e9
-        out.append({"op": op, "rows": r, "cols": c, "outliers": outl,
-                    "us_per_op": us, "gbs": gbs, "frac_of_peak": gbs / peak,
-                    "plan": plan_text(op, r, c), "pool_sets": len(work.sets),
+        out.append({"op": op, "dtype": dt, "rows": r, "cols": c,
+                    "outliers": outl, "us_per_op": us, "gbs": gbs,
+                    "frac_of_peak": gbs / peak,
+                    "plan": plan_text(op, r, c, dt),
+                    "pool_sets": len(work.sets),
                     "l2_resident": work.l2_resident, "steps": steps})
         del work
         torch.cuda.empty_cache()

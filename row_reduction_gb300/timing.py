@@ -21,51 +21,68 @@ from . import inputs
 MAX_SETS = 256
 
 
-def algorithmic_bytes(op, rows, cols, h_out=False, mean=False):
+ELEM_BYTES = {"f32": 4, "f16": 2, "bf16": 2}
+
+
+def algorithmic_bytes(op, rows, cols, h_out=False, mean=False, dtype="f32"):
     """Bytes the operator must move once: every input element read once,
-    every output written once, parameter vectors counted once."""
+    every output written once, parameter vectors counted once.  Matrices
+    and parameter vectors take the storage type's size e; per-row outputs
+    and labels are 4 bytes."""
     rc = rows * cols
+    e = ELEM_BYTES[dtype]
     if op == "rmsnorm":
-        return 8 * rc + 4 * cols
+        return 2 * e * rc + e * cols
     if op == "layernorm":
-        return 8 * rc + 8 * cols
+        return 2 * e * rc + 2 * e * cols
     if op == "residual_layernorm":
-        return 12 * rc + 8 * cols + (4 * rc if h_out else 0)
+        return 3 * e * rc + 2 * e * cols + (e * rc if h_out else 0)
     if op == "softmax":
-        return 8 * rc
+        return 2 * e * rc
     if op == "row_sum":
-        return 4 * rc + 4 * rows
+        return e * rc + 4 * rows
     if op == "cross_entropy":
-        return 4 * rc + 8 * rows + (4 if mean else 0)
+        return e * rc + 8 * rows + (4 if mean else 0)
     raise ValueError(op)
+
+
+def _device(a, dtype):
+    import numpy as np
+    import torch
+    if dtype == "bf16" and a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
+    return torch.from_numpy(a).cuda()
 
 
 class Workload:
     """Buffer pool plus prepared raw C-ABI calls for one shape."""
 
     def __init__(self, op, rows, cols, seed, outliers=False,
-                 l2_bytes=126 << 20, max_pool_bytes=16 << 30, data=None):
+                 l2_bytes=126 << 20, max_pool_bytes=16 << 30, data=None,
+                 dtype="f32"):
         import torch
-        self.op, self.rows, self.cols = op, rows, cols
+        self.op, self.rows, self.cols, self.dtype = op, rows, cols, dtype
         d = data if data is not None else inputs.make(op, rows, cols, seed,
                                                       outliers=outliers)
+        d = inputs.as_storage(d, dtype)
         self.host = d
         self.eps = float(d.get("eps", 0.0))
         self.mean = op == "cross_entropy"
         self.h_out = op == "residual_layernorm"
-        self.bytes = algorithmic_bytes(op, rows, cols, self.h_out, self.mean)
-        params = {k: torch.from_numpy(d[k]).cuda() for k in
+        self.bytes = algorithmic_bytes(op, rows, cols, self.h_out, self.mean,
+                                       dtype)
+        params = {k: _device(d[k], dtype) for k in
                   ("weight", "gamma", "beta") if k in d}
         set_bytes = max(self.bytes, 1)
         n = max(1, math.ceil(4 * l2_bytes / set_bytes))
         n = max(1, min(n, max_pool_bytes // set_bytes, MAX_SETS))
-        x0 = torch.from_numpy(d["x"]).cuda()
+        x0 = _device(d["x"], dtype)
         self.sets = []
         for _ in range(n):
             s = dict(params)
             s["x"] = x0.clone()
             if "residual" in d:
-                s["residual"] = torch.from_numpy(d["residual"]).cuda()
+                s["residual"] = _device(d["residual"], dtype)
             if "labels" in d:
                 s["labels"] = torch.from_numpy(d["labels"]).cuda()
             if op in ("rmsnorm", "layernorm", "softmax",
@@ -108,16 +125,27 @@ class Workload:
                  "cross_entropy": (("x", "labels", "loss", "mean_loss"),
                                    False)}
         keys, has_eps = names[self.op]
-        args = [P(k) for k in keys] + [R, C] + ([eps] if has_eps else [])
-        args.append(st)
-        fname = f"mt_{self.op}_f32"
         if plan is not None:
-            fname += "_with_plan"
             self._plan_ref = plan if isinstance(plan, B.MtPlan) else \
                 B.MtPlan(**plan)
-            args.append(ctypes.byref(self._plan_ref))
+        if plan is not None and self.dtype != "f32":
+            # op, dtype, x, residual, weight, beta, labels, y, h_out, out,
+            # mean_loss, rows, cols, eps, stream, plan
+            fname = "mt_row_reduce_with_plan"
+            args = (B.OP_IDS[self.op], B.DTYPE_IDS[self.dtype], P("x"),
+                    P("residual"), P("weight") or P("gamma"), P("beta"),
+                    P("labels"), P("y"), P("h_out"),
+                    P("out") or P("loss"), P("mean_loss"), R, C, eps, st,
+                    ctypes.byref(self._plan_ref))
+        else:
+            args = [P(k) for k in keys] + [R, C] + ([eps] if has_eps else [])
+            args.append(st)
+            fname = f"mt_{self.op}_{self.dtype}"
+            if plan is not None:
+                fname += "_with_plan"
+                args.append(ctypes.byref(self._plan_ref))
+            args = tuple(args)
         f = getattr(L, fname)
-        args = tuple(args)
 
         def go():
             rc = f(*args)
@@ -252,7 +280,9 @@ def time_e2e(work, steps, warmup):
     host-to-device bytes per step, device-to-host bytes per step)."""
     import torch
     s0 = work.sets[0]
-    x_host = torch.from_numpy(work.host["x"]).pin_memory()
+    hx = work.host["x"]
+    x_host = (torch.from_numpy(hx.view("int16")).view(torch.bfloat16)
+              if work.dtype == "bf16" else torch.from_numpy(hx)).pin_memory()
     out_key = {"row_sum": "out", "cross_entropy": "loss"}.get(work.op, "y")
     out_host = torch.empty(s0[out_key].shape, dtype=s0[out_key].dtype,
                            pin_memory=True)
@@ -276,5 +306,6 @@ def time_e2e(work, steps, warmup):
             step()
         end.record(stream)
     end.synchronize()
-    return (start.elapsed_time(end) / 1e3, x_host.numel() * 4,
-            out_host.numel() * 4)
+    return (start.elapsed_time(end) / 1e3,
+            x_host.numel() * x_host.element_size(),
+            out_host.numel() * out_host.element_size())

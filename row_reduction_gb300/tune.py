@@ -38,6 +38,7 @@ from . import inputs
 from .timing import Workload, time_rounds
 
 CHUNKS = (1, 2, 4, 8, 16)
+VALUES = {"f32": (4, 2, 1), "f16": (8, 4, 2), "bf16": (8, 4, 2)}
 FLAG_SETS = (B.MT_PLAN_PDL, B.MT_PLAN_PDL | B.MT_PLAN_PREFETCH_NEXT, 0)
 
 
@@ -48,11 +49,11 @@ def pow2ceil(v):
     return p
 
 
-def candidates(op, rows, cols):
+def candidates(op, rows, cols, dtype="f32"):
     """Legal plans worth timing for one shape."""
     out = []
     op_id = B.OP_IDS[op]
-    for V in (4, 2, 1):
+    for V in VALUES[dtype]:
         W = V if V > 1 else 1
         while W <= 1024:
             if W * V <= 2 * pow2ceil(cols) or W <= 32:
@@ -76,7 +77,7 @@ def candidates(op, rows, cols):
         if key in seen:
             continue
         seen.add(key)
-        if B.mt_plan_check(op_id, cols, p) == B.MT_OK:
+        if B.mt_plan_check_dtype(op_id, dtype, cols, p) == B.MT_OK:
             legal.append(p)
     return legal
 
@@ -89,26 +90,31 @@ def _outputs(work, plan):
     return {k: v.clone() for k, v in work.outputs(0).items()}
 
 
-def _agrees(a, b):
+def _agrees(a, b, dtype="f32"):
+    """Two plans' outputs agree: within the FP32 tolerance, plus one unit of
+    the storage type's last place for 16-bit outputs (each plan rounds its
+    own FP32 result once)."""
     import torch
+    rel = {"f32": 0.0, "f16": 2.0 ** -10, "bf16": 2.0 ** -7}[dtype]
     for k in b:
         x, y = a[k].double(), b[k].double()
         nan = torch.isnan(x) & torch.isnan(y)
-        ok = ((x - y).abs() <= 1e-5 * (1 + y.abs())) | nan
+        r = rel if a[k].dtype != torch.float32 else 0.0
+        ok = ((x - y).abs() <= 1e-5 * (1 + y.abs()) + r * y.abs()) | nan
         if not bool(ok.all()):
             return False
     return True
 
 
-def tune_shape(op, rows, cols, l2, rounds=5, log=print):
+def tune_shape(op, rows, cols, l2, rounds=5, log=print, dtype="f32"):
     """Tunes one shape; returns a record with the winner and timings."""
     import torch
     outliers = op == "rmsnorm" and (rows, cols) in inputs.RMSNORM_SWEEP
     work = Workload(op, rows, cols, inputs.TUNE_SEED, outliers=outliers,
-                    l2_bytes=l2, max_pool_bytes=8 << 30)
-    default = B.mt_plan_query(op, rows, cols)
+                    l2_bytes=l2, max_pool_bytes=8 << 30, dtype=dtype)
+    default = B.mt_plan_query_dtype(op, dtype, rows, cols)
     ref = _outputs(work, default)
-    cands = candidates(op, rows, cols)
+    cands = candidates(op, rows, cols, dtype)
     timed = []
     rejected = 0
     for p in cands:
@@ -118,7 +124,7 @@ def tune_shape(op, rows, cols, l2, rounds=5, log=print):
             log(f"  reject {B.mt_describe_plan(p)}: {e}")
             rejected += 1
             continue
-        if not _agrees(got, ref):
+        if not _agrees(got, ref, dtype):
             log(f"  reject {B.mt_describe_plan(p)}: output differs")
             rejected += 1
             continue
@@ -139,21 +145,21 @@ def tune_shape(op, rows, cols, l2, rounds=5, log=print):
     torch.cuda.empty_cache()
     # Held-out validation of the winner.
     hold = Workload(op, rows, cols, inputs.HOLDOUT_SEED, outliers=outliers,
-                    l2_bytes=0, max_pool_bytes=0)
-    ok = _agrees(_outputs(hold, best), _outputs(hold, default))
+                    l2_bytes=0, max_pool_bytes=0, dtype=dtype)
+    ok = _agrees(_outputs(hold, best), _outputs(hold, default), dtype)
     del hold
     torch.cuda.empty_cache()
     if not ok:
         raise RuntimeError(f"{op} {rows}x{cols}: winner fails held-out "
                            "validation")
-    rec = {"op": op, "rows": rows, "cols": cols,
+    rec = {"op": op, "dtype": dtype, "rows": rows, "cols": cols,
            "winner": best.as_dict(), "winner_text": B.mt_describe_plan(best),
            "winner_us": best_us, "winner_rounds_us": best_rounds,
            "default": default.as_dict(),
            "default_us": statistics.median(d_rounds),
            "candidates": len(cands), "rejected": rejected,
            "top": [{"plan": p.as_dict(), "us": us} for us, p in timed[:8]]}
-    log(f"{op} {rows}x{cols}: {len(cands)} plans, winner "
+    log(f"{op} {dtype} {rows}x{cols}: {len(cands)} plans, winner "
         f"{rec['winner_text']} {best_us:.3f} us (default "
         f"{rec['default_us']:.3f} us)")
     return rec
@@ -231,6 +237,8 @@ def main(argv=None):
     ap.add_argument("--json", required=True)
     ap.add_argument("--table", default=None)
     ap.add_argument("--rounds", type=int, default=5)
+    ap.add_argument("--dtypes", default="f32",
+                    help="storage types, e.g. f32,bf16,f16")
     args = ap.parse_args(argv)
     import torch
     from . import build
@@ -246,13 +254,16 @@ def main(argv=None):
     records = []
     if os.path.exists(args.json):          # resume an interrupted run
         records = json.load(open(args.json))["records"]
-    done = {(r["op"], r["rows"], r["cols"]) for r in records}
+    done = {(r["op"], r.get("dtype", "f32"), r["rows"], r["cols"])
+            for r in records}
     t0 = time.time()
-    for op, rows, cols in shapes:
-        if (op, rows, cols) in done:
-            continue
-        records.append(tune_shape(op, rows, cols, l2, args.rounds,
-                                  log=lambda s: print(s, flush=True)))
+    for dt in [d for d in args.dtypes.split(",") if d]:
+        for op, rows, cols in shapes:
+            if (op, dt, rows, cols) in done:
+                continue
+            records.append(tune_shape(op, rows, cols, l2, args.rounds,
+                                      log=lambda s: print(s, flush=True),
+                                      dtype=dt))
         with open(args.json, "w") as f:
             json.dump({"device": torch.cuda.get_device_name(0),
                        "records": records}, f, indent=1)
