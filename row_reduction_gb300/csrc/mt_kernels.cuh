@@ -71,6 +71,16 @@ __device__ __forceinline__ void two_sum(float a, float b, float &s,
     err = __fadd_rn(__fsub_rn(a, ap), __fsub_rn(b, bp));
 }
 
+// e^d for d = x - max(row) <= 0, as 2^(d * log2(e)) with CUDA's exp2f.  The
+// difference d is formed first (exact when x is near the max), so the only
+// extra error is the rounding of the product: a relative error of at most
+// |d| * 2^-24 in the result.  A term's weight e^d makes its absolute error
+// at most max(e^d |d|) 2^-24 = 2^-24 / e, far below the FP32 tolerance of
+// every output that sums or normalises these terms.
+__device__ __forceinline__ float exp_shifted(float d) {
+    return exp2f(d * 1.4426950408889634f);
+}
+
 // ---- storage types ---------------------------------------------------------
 // Conversions between 32-bit words holding T values and FP32.
 template <typename T>
@@ -317,8 +327,8 @@ __device__ __forceinline__ void row_allreduce_compensated(float &s, float &c,
 __device__ __forceinline__ void lse_merge(float &m, float &s, float m2,
                                           float s2, bool self_first = true) {
     const float mm = nanmax(m, m2);
-    const float f1 = (m == mm) ? 1.f : expf(m - mm);
-    const float f2 = (m2 == mm) ? 1.f : expf(m2 - mm);
+    const float f1 = (m == mm) ? 1.f : exp_shifted(m - mm);
+    const float f2 = (m2 == mm) ? 1.f : exp_shifted(m2 - mm);
     s = self_first ? fmaf(s, f1, s2 * f2) : fmaf(s2, f2, s * f1);
     m = mm;
 }
@@ -687,12 +697,12 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
             for (int k = 0; k < K; ++k)
 #pragma unroll
                 for (int e = 0; e < V; ++e) {
-                    v[k][e] = expf(v[k][e] - m);
+                    v[k][e] = exp_shifted(v[k][e] - m);
                     acc[e] += v[k][e];
                 }
             float s = 0.f;
             if (head) {
-                hv = expf(hv - m);
+                hv = exp_shifted(hv - m);
                 s = hv;
             }
 #pragma unroll
@@ -740,8 +750,8 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
 #pragma unroll
             for (int k = 0; k < K; ++k)
 #pragma unroll
-                for (int e = 0; e < V; ++e) acc[e] += expf(v[k][e] - m);
-            float s = head ? expf(hv - m) : 0.f;
+                for (int e = 0; e < V; ++e) acc[e] += exp_shifted(v[k][e] - m);
+            float s = head ? exp_shifted(hv - m) : 0.f;
 #pragma unroll
             for (int e = 0; e < V; ++e) s += acc[e];
             s = row_allreduce<SumOp>(s, W, red, parity);
@@ -931,7 +941,7 @@ __global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
                                      float ps = 0.f;
 #pragma unroll
                                      for (int e = 0; e < V; ++e)
-                                         if (e < nv) ps += expf(t[e] - pm);
+                                         if (e < nv) ps += exp_shifted(t[e] - pm);
                                      lse_merge(m, s, pm, ps);
                                  });
             row_allreduce_lse(m, s, W, red, parity);
@@ -943,12 +953,12 @@ __global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
                     [&](const float *t, int nv, int off) {
                         if (off < 0) {
                             Y[base + column(off)] =
-                                from_f<T>(expf(t[0] - m) * inv);
+                                from_f<T>(exp_shifted(t[0] - m) * inv);
                             return;
                         }
                         float o[V];
 #pragma unroll
-                        for (int e = 0; e < V; ++e) o[e] = expf(t[e] - m) * inv;
+                        for (int e = 0; e < V; ++e) o[e] = exp_shifted(t[e] - m) * inv;
                         store_pack<T, V, AL>(yb, off, nb, true, yvec, o);
                     });
             } else {
