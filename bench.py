@@ -328,12 +328,12 @@ def run_sweep(l2, peak):
     from row_reduction_gb300 import inputs
     cases = [("rmsnorm", r, c, False, "f32") for r, c in inputs.RMSNORM_SHAPES]
     cases += [("rmsnorm", r, c, True, "f32") for r, c in inputs.RMSNORM_SWEEP]
-    cases += [(op, r, c, False, "f32") for op in inputs.OPS
+    cases += [(op, r, c, False, "f32") for op in inputs.ALL_OPS
               if op != "rmsnorm" for r, c in inputs.FAMILY_SHAPES]
     for dt in ("bf16", "f16"):
         cases += [("rmsnorm", r, c, True, dt)
                   for r, c in inputs.RMSNORM_SWEEP]
-        cases += [(op, 1024, 4096, False, dt) for op in inputs.OPS
+        cases += [(op, 1024, 4096, False, dt) for op in inputs.ALL_OPS
                   if op != "rmsnorm"]
     out = []
     import torch

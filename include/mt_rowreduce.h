@@ -79,8 +79,13 @@ typedef enum mt_op {
     MT_OP_RESIDUAL_LAYERNORM = 2,
     MT_OP_SOFTMAX = 3,
     MT_OP_ROW_SUM = 4,
-    MT_OP_CROSS_ENTROPY = 5
+    MT_OP_CROSS_ENTROPY = 5,
+    MT_OP_RESIDUAL_RMSNORM = 6,
+    MT_OP_LOG_SOFTMAX = 7
 } mt_op;
+
+/* ignore_index value meaning "no label is ignored". */
+#define MT_NO_IGNORE_INDEX INT32_MIN
 
 /* Storage type of the matrices and parameter vectors of a call.  All
  * arithmetic is FP32 whatever the storage type; per-row outputs (row sums,
@@ -210,6 +215,41 @@ MT_API mt_status mt_cross_entropy_f32_with_plan(const float *logits,
                                          int64_t cols, mt_stream_t stream,
                                          const mt_plan_t *plan);
 
+/* ---- fused variants (same engine, same conventions) --------------------- */
+
+/* Residual RMSNorm (pre-norm add-and-norm) per row: h = x + residual (FP32
+ * add); y = h / sqrt(mean(h^2) + eps) * weight; if h_out != NULL it
+ * receives h.  weight may be NULL (all ones). */
+MT_API mt_status mt_residual_rmsnorm_f32(const float *x, const float *residual,
+                                         const float *weight, float *y,
+                                         float *h_out, int64_t rows,
+                                         int64_t cols, float eps,
+                                         mt_stream_t stream);
+MT_API mt_status mt_residual_rmsnorm_f32_with_plan(
+    const float *x, const float *residual, const float *weight, float *y,
+    float *h_out, int64_t rows, int64_t cols, float eps, mt_stream_t stream,
+    const mt_plan_t *plan);
+
+/* Log-softmax per row: y = (x - max(x)) - log(sum(exp(x - max(x)))).  A row
+ * that holds a NaN gives an all-NaN output row. */
+MT_API mt_status mt_log_softmax_f32(const float *x, float *y, int64_t rows,
+                                    int64_t cols, mt_stream_t stream);
+MT_API mt_status mt_log_softmax_f32_with_plan(const float *x, float *y,
+                                              int64_t rows, int64_t cols,
+                                              mt_stream_t stream,
+                                              const mt_plan_t *plan);
+
+/* Cross-entropy with an ignore index: rows whose label equals ignore_index
+ * get loss 0 and are left out of the mean, which divides by the number of
+ * other rows (NaN when every row is ignored).  Any other label outside
+ * [0, cols) still gives loss NaN.  MT_NO_IGNORE_INDEX ignores nothing (same
+ * as mt_cross_entropy_f32). */
+MT_API mt_status mt_cross_entropy_ignore_f32(const float *logits,
+                                             const int32_t *labels,
+                                             int32_t ignore_index, float *loss,
+                                             float *mean_loss, int64_t rows,
+                                             int64_t cols, mt_stream_t stream);
+
 /* ---- FP16 / BF16 storage ------------------------------------------------
  * Same operators with 16-bit matrices and parameter vectors: every value is
  * widened to FP32 on load, all statistics and the epilogue (including the
@@ -257,18 +297,46 @@ MT_API mt_status mt_cross_entropy_bf16(const mt_bf16_t *logits,
                                        const int32_t *labels, float *loss,
                                        float *mean_loss, int64_t rows,
                                        int64_t cols, mt_stream_t stream);
+MT_API mt_status mt_cross_entropy_ignore_f16(
+    const mt_f16_t *logits, const int32_t *labels, int32_t ignore_index,
+    float *loss, float *mean_loss, int64_t rows, int64_t cols,
+    mt_stream_t stream);
+MT_API mt_status mt_cross_entropy_ignore_bf16(
+    const mt_bf16_t *logits, const int32_t *labels, int32_t ignore_index,
+    float *loss, float *mean_loss, int64_t rows, int64_t cols,
+    mt_stream_t stream);
+MT_API mt_status mt_residual_rmsnorm_f16(const mt_f16_t *x,
+                                         const mt_f16_t *residual,
+                                         const mt_f16_t *weight, mt_f16_t *y,
+                                         mt_f16_t *h_out, int64_t rows,
+                                         int64_t cols, float eps,
+                                         mt_stream_t stream);
+MT_API mt_status mt_residual_rmsnorm_bf16(const mt_bf16_t *x,
+                                          const mt_bf16_t *residual,
+                                          const mt_bf16_t *weight,
+                                          mt_bf16_t *y, mt_bf16_t *h_out,
+                                          int64_t rows, int64_t cols,
+                                          float eps, mt_stream_t stream);
+MT_API mt_status mt_log_softmax_f16(const mt_f16_t *x, mt_f16_t *y,
+                                    int64_t rows, int64_t cols,
+                                    mt_stream_t stream);
+MT_API mt_status mt_log_softmax_bf16(const mt_bf16_t *x, mt_bf16_t *y,
+                                     int64_t rows, int64_t cols,
+                                     mt_stream_t stream);
 
-/* Any operator and storage type with an explicit plan (NULL = the table's
- * plan).  Pointer arguments follow the typed calls above; pointers an
- * operator does not use must be NULL: x, weight (gamma), beta, residual, y,
- * h_out are of `dtype`; out (row sums / losses) and mean_loss are FP32;
- * labels are int32.  eps is ignored by softmax, row sum and
- * cross-entropy. */
+/* Any operator (mt_op) and storage type with an explicit plan (NULL = the
+ * table's plan).  Pointer arguments follow the typed calls above; pointers
+ * an operator does not take must be NULL: x, weight (gamma), beta,
+ * residual, y, h_out are of `dtype`; out (row sums / losses) and mean_loss
+ * are FP32; labels are int32.  ignore_index applies to cross-entropy only
+ * (MT_NO_IGNORE_INDEX for none); eps is ignored by the operators that have
+ * none. */
 MT_API mt_status mt_row_reduce_with_plan(
     int op, int dtype, const void *x, const void *residual,
-    const void *weight, const void *beta, const int32_t *labels, void *y,
-    void *h_out, float *out, float *mean_loss, int64_t rows, int64_t cols,
-    float eps, mt_stream_t stream, const mt_plan_t *plan);
+    const void *weight, const void *beta, const int32_t *labels,
+    int32_t ignore_index, void *y, void *h_out, float *out, float *mean_loss,
+    int64_t rows, int64_t cols, float eps, mt_stream_t stream,
+    const mt_plan_t *plan);
 
 /* ---- planning and introspection (host only; no CUDA call) ------------- */
 

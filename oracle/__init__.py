@@ -17,6 +17,8 @@ Definitions, per row of n = cols entries (see the header of ``oracle.c``):
   ``cross_entropy`` -- the operator coverage list of "Consecutive-worker
   reduction layout checkpoint", §Evidence and what remains; the pages name
   them without formulas, so the textbook definitions are used.
+* ``residual_rmsnorm``, ``log_softmax``, ``cross_entropy_ignore`` -- fused
+  variants on the same rows, the plain compositions of those definitions.
 
 Pins: ``tests/test_oracle_pins.py`` checks every function against closed
 forms, invariants, exactly-rounded sums and torch float64 library routines.
@@ -66,10 +68,18 @@ def _load():
             lib.oracle_softmax_f64.argtypes = [P, I, I, P]
             lib.oracle_row_sum_f64.argtypes = [P, I, I, P]
             lib.oracle_cross_entropy_f64.argtypes = [P, P, I, I, P, P]
+            lib.oracle_residual_rmsnorm_f64.argtypes = [P, P, P, I, I, D, P,
+                                                        P]
+            lib.oracle_log_softmax_f64.argtypes = [P, I, I, P]
+            lib.oracle_cross_entropy_ignore_f64.argtypes = [
+                P, P, ctypes.c_int32, I, I, P, P]
             for f in (lib.oracle_rmsnorm_f64, lib.oracle_layernorm_f64,
                       lib.oracle_residual_layernorm_f64,
                       lib.oracle_softmax_f64, lib.oracle_row_sum_f64,
-                      lib.oracle_cross_entropy_f64):
+                      lib.oracle_cross_entropy_f64,
+                      lib.oracle_residual_rmsnorm_f64,
+                      lib.oracle_log_softmax_f64,
+                      lib.oracle_cross_entropy_ignore_f64):
                 f.restype = None
             _lib = lib
     return _lib
@@ -169,6 +179,46 @@ def cross_entropy(logits, labels):
     return loss, float(mean[0])
 
 
+def residual_rmsnorm(x, residual, weight=None, eps=1e-6):
+    """Returns (y, h_out): y = rmsnorm(x + residual); h_out = fp32(x + r)."""
+    x = _f32(x, "x")
+    r = _f32(residual, "residual")
+    if r.shape != x.shape:
+        raise ValueError("residual must match x")
+    rows, cols = x.shape
+    w = _vec(weight, cols, "weight")
+    y = np.empty((rows, cols), dtype=np.float64)
+    h = np.empty((rows, cols), dtype=np.float32)
+    _load().oracle_residual_rmsnorm_f64(_p(x), _p(r), _p(w), rows, cols,
+                                        float(np.float32(eps)), _p(y), _p(h))
+    return y, h
+
+
+def log_softmax(x):
+    """y = (x - max) - log(sum(exp(x - max))), per row."""
+    x = _f32(x, "x")
+    rows, cols = x.shape
+    y = np.empty((rows, cols), dtype=np.float64)
+    _load().oracle_log_softmax_f64(_p(x), rows, cols, _p(y))
+    return y
+
+
+def cross_entropy_ignore(logits, labels, ignore_index):
+    """(loss, mean) with rows labelled `ignore_index` given loss 0 and left
+    out of the mean."""
+    x = _f32(logits, "logits")
+    rows, cols = x.shape
+    lab = np.ascontiguousarray(labels, dtype=np.int32).reshape(-1)
+    if lab.shape[0] != rows:
+        raise ValueError("labels must have rows entries")
+    loss = np.empty(rows, dtype=np.float64)
+    mean = np.empty(1, dtype=np.float64)
+    _load().oracle_cross_entropy_ignore_f64(_p(x), _p(lab),
+                                            int(ignore_index), rows, cols,
+                                            _p(loss), _p(mean))
+    return loss, float(mean[0])
+
+
 def run(op: str, inputs: dict):
     """Dispatch by operator name on a dict made by the input generators.
 
@@ -190,6 +240,16 @@ def run(op: str, inputs: dict):
     if op == "row_sum":
         return {"out": row_sum(inputs["x"])}
     if op == "cross_entropy":
-        loss, mean = cross_entropy(inputs["x"], inputs["labels"])
+        if inputs.get("ignore_index") is not None:
+            loss, mean = cross_entropy_ignore(inputs["x"], inputs["labels"],
+                                              inputs["ignore_index"])
+        else:
+            loss, mean = cross_entropy(inputs["x"], inputs["labels"])
         return {"loss": loss, "mean_loss": np.array([mean])}
+    if op == "residual_rmsnorm":
+        y, h = residual_rmsnorm(inputs["x"], inputs["residual"],
+                                inputs.get("weight"), inputs["eps"])
+        return {"y": y, "h_out": h}
+    if op == "log_softmax":
+        return {"y": log_softmax(inputs["x"])}
     raise ValueError(f"unknown op {op!r}")

@@ -21,6 +21,13 @@
  *   softmax     m = max(x); e = exp(x - m); y = e / sum(e)
  *   row sum     s = sum(x)
  *   cross-ent.  loss = m + log(sum(exp(x - m))) - x[label]; mean = sum(loss)/R
+ * Fused variants on the same rows (the pages name none of them; they are
+ * the plain compositions of the definitions above):
+ *   residual RMSNorm  h = x + r; y = rmsnorm(h); h_out = fl32(x + r)
+ *   log-softmax       y = (x - m) - log(sum(exp(x - m)))
+ *   cross-entropy with an ignore index: rows whose label equals it have
+ *                     loss 0 and are left out of the mean, which divides by
+ *                     the number of other rows (NaN when there are none)
  * The operator family is named in "Consecutive-worker reduction layout
  * checkpoint", §Evidence and what remains (the generic V=4 operator coverage
  * run: sum, softmax, RMSNorm, LayerNorm, residual LayerNorm, cross-entropy).
@@ -183,4 +190,81 @@ ORACLE_API void oracle_cross_entropy_f64(const float *logits,
     }
     if (mean)
         *mean = rows > 0 ? total / (double)rows : NAN;
+}
+
+ORACLE_API void oracle_residual_rmsnorm_f64(const float *x, const float *res,
+                                            const float *w, int64_t rows,
+                                            int64_t cols, double eps,
+                                            double *y, float *h_out)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *xr = x + r * cols;
+        const float *rr = res + r * cols;
+        double *yr = y + r * cols;
+        double ss = 0.0;
+        for (int64_t j = 0; j < cols; ++j) {
+            double h = (double)xr[j] + (double)rr[j];
+            yr[j] = h; /* keep h until the scale is known */
+            ss += h * h;
+            if (h_out)
+                h_out[r * cols + j] = (float)h;
+        }
+        double denom = sqrt(ss / (double)cols + eps);
+        for (int64_t j = 0; j < cols; ++j) {
+            double wj = w ? (double)w[j] : 1.0;
+            yr[j] = yr[j] / denom * wj;
+        }
+    }
+}
+
+ORACLE_API void oracle_log_softmax_f64(const float *x, int64_t rows,
+                                       int64_t cols, double *y)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *xr = x + r * cols;
+        double *yr = y + r * cols;
+        double m = -INFINITY;
+        int has_nan = 0;
+        for (int64_t j = 0; j < cols; ++j) {
+            double v = (double)xr[j];
+            if (v != v)
+                has_nan = 1;
+            if (v > m)
+                m = v;
+        }
+        if (has_nan) {
+            for (int64_t j = 0; j < cols; ++j)
+                yr[j] = NAN;
+            continue;
+        }
+        double s = 0.0;
+        for (int64_t j = 0; j < cols; ++j)
+            s += exp((double)xr[j] - m);
+        double ls = log(s);
+        for (int64_t j = 0; j < cols; ++j)
+            yr[j] = ((double)xr[j] - m) - ls;
+    }
+}
+
+ORACLE_API void oracle_cross_entropy_ignore_f64(const float *logits,
+                                                const int32_t *labels,
+                                                int32_t ignore_index,
+                                                int64_t rows, int64_t cols,
+                                                double *loss, double *mean)
+{
+    double total = 0.0;
+    int64_t counted = 0;
+    for (int64_t r = 0; r < rows; ++r) {
+        if (labels[r] == ignore_index) {
+            loss[r] = 0.0;
+            continue;
+        }
+        /* one row through the plain definition */
+        oracle_cross_entropy_f64(logits + r * cols, labels + r, 1, cols,
+                                 loss + r, NULL);
+        total += loss[r];
+        counted += 1;
+    }
+    if (mean)
+        *mean = counted > 0 ? total / (double)counted : NAN;
 }

@@ -20,7 +20,13 @@ from ._binding import (  # noqa: F401
     mt_rmsnorm_bf16, mt_layernorm_f16, mt_layernorm_bf16,
     mt_residual_layernorm_f16, mt_residual_layernorm_bf16, mt_softmax_f16,
     mt_softmax_bf16, mt_row_sum_f16, mt_row_sum_bf16, mt_cross_entropy_f16,
-    mt_cross_entropy_bf16,
+    mt_cross_entropy_bf16, MT_OP_RESIDUAL_RMSNORM, MT_OP_LOG_SOFTMAX,
+    MT_NO_IGNORE_INDEX, mt_residual_rmsnorm_f32,
+    mt_residual_rmsnorm_f32_with_plan, mt_residual_rmsnorm_f16,
+    mt_residual_rmsnorm_bf16, mt_log_softmax_f32,
+    mt_log_softmax_f32_with_plan, mt_log_softmax_f16, mt_log_softmax_bf16,
+    mt_cross_entropy_ignore_f32, mt_cross_entropy_ignore_f16,
+    mt_cross_entropy_ignore_bf16,
     lib, make_plan, mt_cross_entropy_f32, mt_cross_entropy_f32_with_plan,
     mt_describe_plan, mt_last_cuda_error, mt_layernorm_f32,
     mt_layernorm_f32_with_plan, mt_plan_check, mt_plan_query,
@@ -98,19 +104,48 @@ def row_sum(x, out=None, plan=None, stream=None):
     return o
 
 
-def cross_entropy(logits, labels, mean=True, plan=None, stream=None):
+def cross_entropy(logits, labels, mean=True, ignore_index=None, plan=None,
+                  stream=None):
     """Per-row loss logsumexp(row) - row[label] and, with mean, its mean
-    (both FP32).  Returns (loss, mean_loss) when mean is true (mean_loss a
-    1-element tensor), else loss."""
+    (both FP32).  Rows labelled `ignore_index` get loss 0 and leave the mean.
+    Returns (loss, mean_loss) when mean is true (mean_loss a 1-element
+    tensor), else loss."""
     import torch
     rows, cols = _shape(logits)
     loss = torch.empty(rows, dtype=torch.float32, device=logits.device)
     m = torch.empty(1, dtype=torch.float32, device=logits.device) if mean \
         else None
-    mt_row_reduce_with_plan("cross_entropy", dtype_of(logits), logits,
-                            labels=labels, out=loss, mean_loss=m, rows=rows,
-                            cols=cols, stream=stream, plan=plan)
+    mt_row_reduce_with_plan(
+        "cross_entropy", dtype_of(logits), logits, labels=labels, out=loss,
+        mean_loss=m, rows=rows, cols=cols, stream=stream, plan=plan,
+        ignore_index=(MT_NO_IGNORE_INDEX if ignore_index is None
+                      else ignore_index))
     return (loss, m) if mean else loss
+
+
+def residual_rmsnorm(x, residual, weight=None, eps=1e-6, out=None,
+                     h_out=None, return_h=False, plan=None, stream=None):
+    """y = rmsnorm(x + residual) * weight; with return_h also h = x + r."""
+    import torch
+    rows, cols = _shape(x)
+    y = torch.empty_like(x) if out is None else out
+    if return_h and h_out is None:
+        h_out = torch.empty_like(x)
+    mt_row_reduce_with_plan("residual_rmsnorm", dtype_of(x), x,
+                            residual=residual, weight=weight, y=y,
+                            h_out=h_out, rows=rows, cols=cols, eps=eps,
+                            stream=stream, plan=plan)
+    return (y, h_out) if return_h else y
+
+
+def log_softmax(x, out=None, plan=None, stream=None):
+    """Row-wise log-softmax."""
+    import torch
+    rows, cols = _shape(x)
+    y = torch.empty_like(x) if out is None else out
+    mt_row_reduce_with_plan("log_softmax", dtype_of(x), x, y=y, rows=rows,
+                            cols=cols, stream=stream, plan=plan)
+    return y
 
 
 def run(op: str, t: dict, plan=None, stream=None) -> dict:
@@ -133,7 +168,15 @@ def run(op: str, t: dict, plan=None, stream=None) -> dict:
     if op == "row_sum":
         return {"out": row_sum(t["x"], plan=plan, stream=stream)}
     if op == "cross_entropy":
-        loss, m = cross_entropy(t["x"], t["labels"], plan=plan,
-                                stream=stream)
+        loss, m = cross_entropy(t["x"], t["labels"],
+                                ignore_index=t.get("ignore_index"),
+                                plan=plan, stream=stream)
         return {"loss": loss, "mean_loss": m}
+    if op == "residual_rmsnorm":
+        y, h = residual_rmsnorm(t["x"], t["residual"], t.get("weight"),
+                                t["eps"], return_h=True, plan=plan,
+                                stream=stream)
+        return {"y": y, "h_out": h}
+    if op == "log_softmax":
+        return {"y": log_softmax(t["x"], plan=plan, stream=stream)}
     raise ValueError(f"unknown op {op!r}")

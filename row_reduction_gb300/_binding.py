@@ -30,8 +30,12 @@ MT_OP_RESIDUAL_LAYERNORM = 2
 MT_OP_SOFTMAX = 3
 MT_OP_ROW_SUM = 4
 MT_OP_CROSS_ENTROPY = 5
+MT_OP_RESIDUAL_RMSNORM = 6
+MT_OP_LOG_SOFTMAX = 7
 OP_IDS = {"rmsnorm": 0, "layernorm": 1, "residual_layernorm": 2,
-          "softmax": 3, "row_sum": 4, "cross_entropy": 5}
+          "softmax": 3, "row_sum": 4, "cross_entropy": 5,
+          "residual_rmsnorm": 6, "log_softmax": 7}
+MT_NO_IGNORE_INDEX = -(2 ** 31)
 
 MT_DTYPE_F32 = 0
 MT_DTYPE_F16 = 1
@@ -60,6 +64,12 @@ EXPORTS = (
     "mt_row_sum_f16", "mt_row_sum_bf16", "mt_cross_entropy_f16",
     "mt_cross_entropy_bf16", "mt_row_reduce_with_plan",
     "mt_plan_query_dtype", "mt_plan_check_dtype",
+    "mt_residual_rmsnorm_f32", "mt_residual_rmsnorm_f32_with_plan",
+    "mt_residual_rmsnorm_f16", "mt_residual_rmsnorm_bf16",
+    "mt_log_softmax_f32", "mt_log_softmax_f32_with_plan",
+    "mt_log_softmax_f16", "mt_log_softmax_bf16",
+    "mt_cross_entropy_ignore_f32", "mt_cross_entropy_ignore_f16",
+    "mt_cross_entropy_ignore_bf16",
 )
 
 
@@ -135,8 +145,14 @@ def lib() -> ctypes.CDLL:
                 "mt_plan_query": [ctypes.c_int, I64, I64, PP],
                 "mt_plan_check": [ctypes.c_int, I64, PP],
                 "mt_row_reduce_with_plan": [ctypes.c_int, ctypes.c_int, P, P,
-                                            P, P, P, P, P, P, P, I64, I64, F,
-                                            P, PP],
+                                            P, P, P, I32, P, P, P, P, I64,
+                                            I64, F, P, PP],
+                "mt_residual_rmsnorm_f32": [P, P, P, P, P, I64, I64, F, P],
+                "mt_residual_rmsnorm_f32_with_plan": [P, P, P, P, P, I64, I64,
+                                                      F, P, PP],
+                "mt_log_softmax_f32": [P, P, I64, I64, P],
+                "mt_log_softmax_f32_with_plan": [P, P, I64, I64, P, PP],
+                "mt_cross_entropy_ignore_f32": [P, P, I32, P, P, I64, I64, P],
                 "mt_plan_query_dtype": [ctypes.c_int, ctypes.c_int, I64, I64,
                                         PP],
                 "mt_plan_check_dtype": [ctypes.c_int, ctypes.c_int, I64, PP],
@@ -150,6 +166,11 @@ def lib() -> ctypes.CDLL:
                     f"mt_softmax_{dt}": [P, P, I64, I64, P],
                     f"mt_row_sum_{dt}": [P, P, I64, I64, P],
                     f"mt_cross_entropy_{dt}": [P, P, P, P, I64, I64, P],
+                    f"mt_cross_entropy_ignore_{dt}": [P, P, I32, P, P, I64,
+                                                      I64, P],
+                    f"mt_residual_rmsnorm_{dt}": [P, P, P, P, P, I64, I64, F,
+                                                  P],
+                    f"mt_log_softmax_{dt}": [P, P, I64, I64, P],
                 })
             for name, args in sig.items():
                 fn = getattr(L, name)
@@ -227,10 +248,6 @@ def _check(st, where):
 
 
 # ---- the C ABI, one function per entry point ---------------------------------
-def mt_rmsnorm_f32(x, weight, y, rows, cols, eps, stream=None):
-    _check(lib().mt_rmsnorm_f32(_ptr(x, "x"), _ptr(weight, "weight"),
-                                _ptr(y, "y"), rows, cols, eps,
-                                _stream(stream)), "mt_rmsnorm_f32")
 
 
 def mt_rmsnorm_f32_with_plan(x, weight, y, rows, cols, eps, stream=None,
@@ -240,11 +257,6 @@ def mt_rmsnorm_f32_with_plan(x, weight, y, rows, cols, eps, stream=None,
         _stream(stream), _plan(plan)), "mt_rmsnorm_f32_with_plan")
 
 
-def mt_layernorm_f32(x, gamma, beta, y, rows, cols, eps, stream=None):
-    _check(lib().mt_layernorm_f32(_ptr(x, "x"), _ptr(gamma, "gamma"),
-                                  _ptr(beta, "beta"), _ptr(y, "y"), rows,
-                                  cols, eps, _stream(stream)),
-           "mt_layernorm_f32")
 
 
 def mt_layernorm_f32_with_plan(x, gamma, beta, y, rows, cols, eps,
@@ -255,12 +267,6 @@ def mt_layernorm_f32_with_plan(x, gamma, beta, y, rows, cols, eps,
         "mt_layernorm_f32_with_plan")
 
 
-def mt_residual_layernorm_f32(x, residual, gamma, beta, y, h_out, rows, cols,
-                              eps, stream=None):
-    _check(lib().mt_residual_layernorm_f32(
-        _ptr(x, "x"), _ptr(residual, "residual"), _ptr(gamma, "gamma"),
-        _ptr(beta, "beta"), _ptr(y, "y"), _ptr(h_out, "h_out"), rows, cols,
-        eps, _stream(stream)), "mt_residual_layernorm_f32")
 
 
 def mt_residual_layernorm_f32_with_plan(x, residual, gamma, beta, y, h_out,
@@ -273,9 +279,6 @@ def mt_residual_layernorm_f32_with_plan(x, residual, gamma, beta, y, h_out,
         "mt_residual_layernorm_f32_with_plan")
 
 
-def mt_softmax_f32(x, y, rows, cols, stream=None):
-    _check(lib().mt_softmax_f32(_ptr(x, "x"), _ptr(y, "y"), rows, cols,
-                                _stream(stream)), "mt_softmax_f32")
 
 
 def mt_softmax_f32_with_plan(x, y, rows, cols, stream=None, plan=None):
@@ -284,9 +287,6 @@ def mt_softmax_f32_with_plan(x, y, rows, cols, stream=None, plan=None):
            "mt_softmax_f32_with_plan")
 
 
-def mt_row_sum_f32(x, out, rows, cols, stream=None):
-    _check(lib().mt_row_sum_f32(_ptr(x, "x"), _ptr(out, "out"), rows, cols,
-                                _stream(stream)), "mt_row_sum_f32")
 
 
 def mt_row_sum_f32_with_plan(x, out, rows, cols, stream=None, plan=None):
@@ -296,12 +296,6 @@ def mt_row_sum_f32_with_plan(x, out, rows, cols, stream=None, plan=None):
            "mt_row_sum_f32_with_plan")
 
 
-def mt_cross_entropy_f32(logits, labels, loss, mean_loss, rows, cols,
-                         stream=None):
-    _check(lib().mt_cross_entropy_f32(
-        _ptr(logits, "logits"), _ptr(labels, "labels", "int32"),
-        _ptr(loss, "loss"), _ptr(mean_loss, "mean_loss"), rows, cols,
-        _stream(stream)), "mt_cross_entropy_f32")
 
 
 def mt_cross_entropy_f32_with_plan(logits, labels, loss, mean_loss, rows,
@@ -348,21 +342,61 @@ def _half_entry_points(dt):
             _ptr(logits, "logits", dt), _ptr(labels, "labels", "int32"),
             _ptr(loss, "loss"), _ptr(mean_loss, "mean_loss"), rows, cols,
             _stream(stream)), f"mt_cross_entropy_{dt}")
-    return rmsnorm, layernorm, residual_layernorm, softmax, row_sum, \
-        cross_entropy
+    def cross_entropy_ignore(logits, labels, ignore_index, loss, mean_loss,
+                             rows, cols, stream=None):
+        _check(getattr(lib(), f"mt_cross_entropy_ignore_{dt}")(
+            _ptr(logits, "logits", dt), _ptr(labels, "labels", "int32"),
+            ignore_index, _ptr(loss, "loss"), _ptr(mean_loss, "mean_loss"),
+            rows, cols, _stream(stream)), f"mt_cross_entropy_ignore_{dt}")
+
+    def residual_rmsnorm(x, residual, weight, y, h_out, rows, cols, eps,
+                         stream=None):
+        _check(getattr(lib(), f"mt_residual_rmsnorm_{dt}")(
+            _ptr(x, "x", dt), _ptr(residual, "residual", dt),
+            _ptr(weight, "weight", dt), _ptr(y, "y", dt),
+            _ptr(h_out, "h_out", dt), rows, cols, eps, _stream(stream)),
+            f"mt_residual_rmsnorm_{dt}")
+
+    def log_softmax(x, y, rows, cols, stream=None):
+        _check(getattr(lib(), f"mt_log_softmax_{dt}")(
+            _ptr(x, "x", dt), _ptr(y, "y", dt), rows, cols,
+            _stream(stream)), f"mt_log_softmax_{dt}")
+    return (rmsnorm, layernorm, residual_layernorm, softmax, row_sum,
+            cross_entropy, cross_entropy_ignore, residual_rmsnorm,
+            log_softmax)
 
 
+(mt_rmsnorm_f32, mt_layernorm_f32, mt_residual_layernorm_f32, mt_softmax_f32,
+ mt_row_sum_f32, mt_cross_entropy_f32, mt_cross_entropy_ignore_f32,
+ mt_residual_rmsnorm_f32, mt_log_softmax_f32) = _half_entry_points("f32")
 (mt_rmsnorm_f16, mt_layernorm_f16, mt_residual_layernorm_f16, mt_softmax_f16,
- mt_row_sum_f16, mt_cross_entropy_f16) = _half_entry_points("f16")
+ mt_row_sum_f16, mt_cross_entropy_f16, mt_cross_entropy_ignore_f16,
+ mt_residual_rmsnorm_f16, mt_log_softmax_f16) = _half_entry_points("f16")
 (mt_rmsnorm_bf16, mt_layernorm_bf16, mt_residual_layernorm_bf16,
- mt_softmax_bf16, mt_row_sum_bf16,
- mt_cross_entropy_bf16) = _half_entry_points("bf16")
+ mt_softmax_bf16, mt_row_sum_bf16, mt_cross_entropy_bf16,
+ mt_cross_entropy_ignore_bf16, mt_residual_rmsnorm_bf16,
+ mt_log_softmax_bf16) = _half_entry_points("bf16")
+
+
+def mt_residual_rmsnorm_f32_with_plan(x, residual, weight, y, h_out, rows,
+                                      cols, eps, stream=None, plan=None):
+    _check(lib().mt_residual_rmsnorm_f32_with_plan(
+        _ptr(x, "x"), _ptr(residual, "residual"), _ptr(weight, "weight"),
+        _ptr(y, "y"), _ptr(h_out, "h_out"), rows, cols, eps, _stream(stream),
+        _plan(plan)), "mt_residual_rmsnorm_f32_with_plan")
+
+
+def mt_log_softmax_f32_with_plan(x, y, rows, cols, stream=None, plan=None):
+    _check(lib().mt_log_softmax_f32_with_plan(
+        _ptr(x, "x"), _ptr(y, "y"), rows, cols, _stream(stream),
+        _plan(plan)), "mt_log_softmax_f32_with_plan")
 
 
 def mt_row_reduce_with_plan(op, dtype, x, residual=None, weight=None,
                             beta=None, labels=None, y=None, h_out=None,
                             out=None, mean_loss=None, rows=0, cols=0, eps=0.0,
-                            stream=None, plan=None):
+                            stream=None, plan=None,
+                            ignore_index=MT_NO_IGNORE_INDEX):
     """Any operator, any storage type, optional explicit plan."""
     op_id = OP_IDS.get(op, op)
     dt = dtype if isinstance(dtype, str) else \
@@ -371,7 +405,8 @@ def mt_row_reduce_with_plan(op, dtype, x, residual=None, weight=None,
         op_id, DTYPE_IDS[dt], _ptr(x, "x", dt),
         _ptr(residual, "residual", dt), _ptr(weight, "weight", dt),
         _ptr(beta, "beta", dt), _ptr(labels, "labels", "int32"),
-        _ptr(y, "y", dt), _ptr(h_out, "h_out", dt), _ptr(out, "out"),
+        ignore_index, _ptr(y, "y", dt), _ptr(h_out, "h_out", dt),
+        _ptr(out, "out"),
         _ptr(mean_loss, "mean_loss"), rows, cols, eps, _stream(stream),
         _plan(plan)), "mt_row_reduce_with_plan")
 

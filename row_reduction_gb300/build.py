@@ -22,7 +22,7 @@ LIB = os.path.join(OUT, "libmt_rowreduce.so")
 HEADER = os.path.join(ROOT, "include", "mt_rowreduce.h")
 
 OPS = ("rmsnorm", "layernorm", "residual_layernorm", "softmax", "row_sum",
-       "cross_entropy")
+       "cross_entropy", "residual_rmsnorm", "log_softmax")
 DTYPES = ("f32", "f16", "bf16")
 SOURCES = (["api.cpp", "planner.cpp", "mean.cu"] +
            [f"ops_{op}_{dt}.cu" for op in OPS for dt in DTYPES])

@@ -58,12 +58,15 @@ typedef cudaError_t (*OccFn)(const mt_plan_t &, bool, int *);
     {launch_##op##_f32_occupancy, launch_##op##_f16_occupancy,               \
      launch_##op##_bf16_occupancy}
 const LaunchFn kLaunch[OP_COUNT][DT_COUNT] = {
-    MT_ROW(rmsnorm), MT_ROW(layernorm), MT_ROW(residual_layernorm),
-    MT_ROW(softmax), MT_ROW(row_sum),   MT_ROW(cross_entropy)};
+    MT_ROW(rmsnorm),       MT_ROW(layernorm),
+    MT_ROW(residual_layernorm), MT_ROW(softmax),
+    MT_ROW(row_sum),       MT_ROW(cross_entropy),
+    MT_ROW(residual_rmsnorm), MT_ROW(log_softmax)};
 const OccFn kOcc[OP_COUNT][DT_COUNT] = {
-    MT_OCC_ROW(rmsnorm), MT_OCC_ROW(layernorm),
+    MT_OCC_ROW(rmsnorm),       MT_OCC_ROW(layernorm),
     MT_OCC_ROW(residual_layernorm), MT_OCC_ROW(softmax),
-    MT_OCC_ROW(row_sum), MT_OCC_ROW(cross_entropy)};
+    MT_OCC_ROW(row_sum),       MT_OCC_ROW(cross_entropy),
+    MT_OCC_ROW(residual_rmsnorm), MT_OCC_ROW(log_softmax)};
 #undef MT_ROW
 #undef MT_OCC_ROW
 
@@ -105,6 +108,7 @@ struct Call {
     float *out = nullptr, *mean = nullptr;
     int64_t rows = 0, cols = 0;
     float eps = 0.f;
+    int32_t ignore_index = MT_NO_IGNORE_INDEX;
 };
 
 // Which pointers each operator takes (the others must be NULL), and which
@@ -121,6 +125,8 @@ unsigned uses(int op) {
         case OP_SOFTMAX: return U_Y;
         case OP_ROW_SUM: return U_OUT;
         case OP_CROSS_ENTROPY: return U_LABELS | U_OUT | U_MEAN;
+        case OP_RESIDUAL_RMSNORM: return U_RES | U_W | U_Y | U_H;
+        case OP_LOG_SOFTMAX: return U_Y;
     }
     return 0;
 }
@@ -128,8 +134,10 @@ unsigned required(int op) {
     switch (op) {
         case OP_RMSNORM:
         case OP_LAYERNORM:
-        case OP_SOFTMAX: return U_Y;
-        case OP_RESIDUAL_LAYERNORM: return U_RES | U_Y;
+        case OP_SOFTMAX:
+        case OP_LOG_SOFTMAX: return U_Y;
+        case OP_RESIDUAL_LAYERNORM:
+        case OP_RESIDUAL_RMSNORM: return U_RES | U_Y;
         case OP_ROW_SUM: return U_OUT;
         case OP_CROSS_ENTROPY: return U_LABELS | U_OUT;
     }
@@ -184,6 +192,8 @@ mt_status run(const Call &c, const mt_plan_t *forced, cudaStream_t stream) {
     a.rows = c.rows;
     a.cols = (int32_t)c.cols;
     a.eps = c.eps;
+    a.ignore_index = c.ignore_index;
+    a.has_ignore = c.ignore_index != MT_NO_IGNORE_INDEX;
 
     // Alignment mode: the "aligned" kernels need every row of every
     // vector-accessed pointer to start on a V*element-size boundary.  A
@@ -237,7 +247,8 @@ mt_status run(const Call &c, const mt_plan_t *forced, cudaStream_t stream) {
             cuda_status(kLaunch[c.op][c.dtype](p, a, aligned, stream)))
         return st;
     if (c.op == OP_CROSS_ENTROPY && c.mean != nullptr)
-        return cuda_status(launch_mean(c.out, c.mean, c.rows, stream));
+        return cuda_status(launch_mean(c.out, c.mean, c.rows, c.labels,
+                                       a.ignore_index, a.has_ignore, stream));
     return MT_OK;
 }
 
@@ -302,11 +313,33 @@ mt_status row_sum_call(int dt, const void *x, float *out, int64_t rows,
 
 mt_status ce_call(int dt, const void *x, const int32_t *labels, float *loss,
                   float *mean, int64_t rows, int64_t cols, mt_stream_t s,
-                  const mt_plan_t *plan) {
+                  const mt_plan_t *plan,
+                  int32_t ignore_index = MT_NO_IGNORE_INDEX) {
     Call c = make_call(OP_CROSS_ENTROPY, dt, x, rows, cols);
     c.labels = labels;
     c.out = loss;
     c.mean = mean;
+    c.ignore_index = ignore_index;
+    return run(c, plan, (cudaStream_t)s);
+}
+
+mt_status res_rms_call(int dt, const void *x, const void *r, const void *w,
+                       void *y, void *h, int64_t rows, int64_t cols,
+                       float eps, mt_stream_t s, const mt_plan_t *plan) {
+    Call c = make_call(OP_RESIDUAL_RMSNORM, dt, x, rows, cols);
+    c.res = r;
+    c.w = w;
+    c.y = y;
+    c.h = h;
+    c.eps = eps;
+    return run(c, plan, (cudaStream_t)s);
+}
+
+mt_status log_softmax_call(int dt, const void *x, void *y, int64_t rows,
+                           int64_t cols, mt_stream_t s,
+                           const mt_plan_t *plan) {
+    Call c = make_call(OP_LOG_SOFTMAX, dt, x, rows, cols);
+    c.y = y;
     return run(c, plan, (cudaStream_t)s);
 }
 
@@ -393,6 +426,42 @@ mt_status mt_cross_entropy_f32(const float *logits, const int32_t *labels,
                    stream, nullptr);
 }
 
+mt_status mt_residual_rmsnorm_f32_with_plan(const float *x,
+                                            const float *residual,
+                                            const float *weight, float *y,
+                                            float *h_out, int64_t rows,
+                                            int64_t cols, float eps,
+                                            mt_stream_t stream,
+                                            const mt_plan_t *plan) {
+    return res_rms_call(MT_DTYPE_F32, x, residual, weight, y, h_out, rows,
+                        cols, eps, stream, plan);
+}
+mt_status mt_residual_rmsnorm_f32(const float *x, const float *residual,
+                                  const float *weight, float *y, float *h_out,
+                                  int64_t rows, int64_t cols, float eps,
+                                  mt_stream_t stream) {
+    return res_rms_call(MT_DTYPE_F32, x, residual, weight, y, h_out, rows,
+                        cols, eps, stream, nullptr);
+}
+mt_status mt_log_softmax_f32_with_plan(const float *x, float *y,
+                                       int64_t rows, int64_t cols,
+                                       mt_stream_t stream,
+                                       const mt_plan_t *plan) {
+    return log_softmax_call(MT_DTYPE_F32, x, y, rows, cols, stream, plan);
+}
+mt_status mt_log_softmax_f32(const float *x, float *y, int64_t rows,
+                             int64_t cols, mt_stream_t stream) {
+    return log_softmax_call(MT_DTYPE_F32, x, y, rows, cols, stream, nullptr);
+}
+mt_status mt_cross_entropy_ignore_f32(const float *logits,
+                                      const int32_t *labels,
+                                      int32_t ignore_index, float *loss,
+                                      float *mean_loss, int64_t rows,
+                                      int64_t cols, mt_stream_t stream) {
+    return ce_call(MT_DTYPE_F32, logits, labels, loss, mean_loss, rows, cols,
+                   stream, nullptr, ignore_index);
+}
+
 // ---- FP16 / BF16 ------------------------------------------------------------
 #define MT_HALF_ENTRY_POINTS(suffix, DT, TY)                                  \
     mt_status mt_rmsnorm_##suffix(const TY *x, const TY *weight, TY *y,      \
@@ -428,6 +497,23 @@ mt_status mt_cross_entropy_f32(const float *logits, const int32_t *labels,
         float *mean_loss, int64_t rows, int64_t cols, mt_stream_t stream) {  \
         return ce_call(DT, logits, labels, loss, mean_loss, rows, cols,      \
                        stream, nullptr);                                     \
+    }                                                                        \
+    mt_status mt_cross_entropy_ignore_##suffix(                              \
+        const TY *logits, const int32_t *labels, int32_t ignore_index,       \
+        float *loss, float *mean_loss, int64_t rows, int64_t cols,           \
+        mt_stream_t stream) {                                                \
+        return ce_call(DT, logits, labels, loss, mean_loss, rows, cols,      \
+                       stream, nullptr, ignore_index);                       \
+    }                                                                        \
+    mt_status mt_residual_rmsnorm_##suffix(                                  \
+        const TY *x, const TY *residual, const TY *weight, TY *y, TY *h_out, \
+        int64_t rows, int64_t cols, float eps, mt_stream_t stream) {         \
+        return res_rms_call(DT, x, residual, weight, y, h_out, rows, cols,   \
+                            eps, stream, nullptr);                           \
+    }                                                                        \
+    mt_status mt_log_softmax_##suffix(const TY *x, TY *y, int64_t rows,      \
+                                      int64_t cols, mt_stream_t stream) {    \
+        return log_softmax_call(DT, x, y, rows, cols, stream, nullptr);      \
     }
 MT_HALF_ENTRY_POINTS(f16, MT_DTYPE_F16, mt_f16_t)
 MT_HALF_ENTRY_POINTS(bf16, MT_DTYPE_BF16, mt_bf16_t)
@@ -436,8 +522,8 @@ MT_HALF_ENTRY_POINTS(bf16, MT_DTYPE_BF16, mt_bf16_t)
 mt_status mt_row_reduce_with_plan(int op, int dtype, const void *x,
                                   const void *residual, const void *weight,
                                   const void *beta, const int32_t *labels,
-                                  void *y, void *h_out, float *out,
-                                  float *mean_loss, int64_t rows,
+                                  int32_t ignore_index, void *y, void *h_out,
+                                  float *out, float *mean_loss, int64_t rows,
                                   int64_t cols, float eps, mt_stream_t stream,
                                   const mt_plan_t *plan) {
     Call c = make_call(op, dtype, x, rows, cols);
@@ -445,6 +531,7 @@ mt_status mt_row_reduce_with_plan(int op, int dtype, const void *x,
     c.w = weight;
     c.b = beta;
     c.labels = labels;
+    c.ignore_index = ignore_index;
     c.y = y;
     c.h = h_out;
     c.out = out;

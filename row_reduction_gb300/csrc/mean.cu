@@ -4,32 +4,49 @@
 
 namespace mt {
 
-// mean = (sum of loss[0..rows)) / rows.  One CTA; each thread sums a strided
-// subset in index order with compensated arithmetic, then the block combines
-// the partials in a fixed shuffle/shared-memory order, so the result does not
-// depend on timing (no atomics).
+// mean = (sum of loss[0..rows)) / n, n = rows, or with an ignore index the
+// number of rows whose label is not it (ignored rows hold loss 0; no such
+// row gives 0/0 = NaN).  One CTA; each thread sums a strided subset in index
+// order with compensated arithmetic, then the block combines the partials in
+// a fixed shuffle/shared-memory order, so the result does not depend on
+// timing (no atomics).
 __global__ void __launch_bounds__(1024)
-    mean_kernel(const float *loss, float *mean, int64_t rows) {
+    mean_kernel(const float *loss, float *mean, int64_t rows,
+                const int32_t *labels, int32_t ignore_index,
+                int32_t has_ignore) {
     // Launched as a programmatic dependent of the loss kernel: wait until
     // that grid has completed and its losses are visible.
     grid_wait_prerequisites();
     grid_launch_dependents();
     __shared__ RedScratch red;
     int parity = 0;
+    __shared__ long long ignored_part[32];
     float s = 0.f, c = 0.f;
+    long long ignored = 0;
     for (int64_t i = threadIdx.x; i < rows; i += blockDim.x) {
         float t, err;
         two_sum(s, loss[i], t, err);
         s = t;
         c += err;
+        if (has_ignore && labels[i] == ignore_index) ++ignored;
     }
     row_allreduce_compensated(s, c, (int)blockDim.x, red, parity);
-    if (threadIdx.x == 0)
-        *mean = (float)((double)(s + c) / (double)rows);
+    // Exact count of ignored rows: warp sums, then warp 0 adds the warps'.
+    for (int off = 16; off > 0; off >>= 1)
+        ignored += __shfl_xor_sync(kFull, ignored, off);
+    if ((threadIdx.x & 31) == 0) ignored_part[threadIdx.x >> 5] = ignored;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        long long total = 0;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) total += ignored_part[w];
+        const double n = (double)(rows - total);
+        *mean = (float)((double)(s + c) / n);
+    }
 }
 
 cudaError_t launch_mean(const float *loss, float *mean, int64_t rows,
-                        cudaStream_t stream) {
+                        const int32_t *labels, int32_t ignore_index,
+                        int32_t has_ignore, cudaStream_t stream) {
     // Programmatic dependent launch lets this one-CTA kernel start while the
     // loss kernel finishes; it waits for that grid before reading.
     cudaLaunchAttribute attr[1];
@@ -41,7 +58,8 @@ cudaError_t launch_mean(const float *loss, float *mean, int64_t rows,
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, mean_kernel, loss, mean, rows);
+    return cudaLaunchKernelEx(&cfg, mean_kernel, loss, mean, rows, labels,
+                              ignore_index, has_ignore);
 }
 
 }  // namespace mt

@@ -16,7 +16,9 @@ enum : int {
     OP_SOFTMAX = MT_OP_SOFTMAX,
     OP_ROW_SUM = MT_OP_ROW_SUM,
     OP_CROSS_ENTROPY = MT_OP_CROSS_ENTROPY,
-    OP_COUNT = 6
+    OP_RESIDUAL_RMSNORM = MT_OP_RESIDUAL_RMSNORM,
+    OP_LOG_SOFTMAX = MT_OP_LOG_SOFTMAX,
+    OP_COUNT = 8
 };
 
 enum : int {
@@ -46,6 +48,10 @@ struct KArgs {
     int32_t log2W;
     int32_t B;             // rows per CTA
     float eps;
+    // Cross-entropy: rows whose label equals ignore_index (when has_ignore)
+    // get loss 0 and leave the mean.
+    int32_t ignore_index;
+    int32_t has_ignore;
     // Unaligned mode only: 1 when the pointer keeps x's 16-byte phase, so
     // its row body can use vector accesses too.
     int32_t y_vec, h_vec, r_vec;
@@ -86,12 +92,16 @@ MT_DECLARE_OP(residual_layernorm)
 MT_DECLARE_OP(softmax)
 MT_DECLARE_OP(row_sum)
 MT_DECLARE_OP(cross_entropy)
+MT_DECLARE_OP(residual_rmsnorm)
+MT_DECLARE_OP(log_softmax)
 #undef MT_DECLARE_OP
 #undef MT_DECLARE_LAUNCHER
 
-// One-CTA fixed-order mean of `rows` per-row losses.
+// One-CTA fixed-order mean of `rows` per-row losses; with has_ignore, rows
+// whose label is ignore_index are left out of the count (their loss is 0).
 cudaError_t launch_mean(const float *loss, float *mean, int64_t rows,
-                        cudaStream_t stream);
+                        const int32_t *labels, int32_t ignore_index,
+                        int32_t has_ignore, cudaStream_t stream);
 
 // Planner (planner.cpp).
 mt_status plan_lookup(int op, int dtype, int64_t rows, int64_t cols,

@@ -81,6 +81,26 @@ __device__ __forceinline__ float exp_shifted(float d) {
     return exp2f(d * 1.4426950408889634f);
 }
 
+// Operators that add a residual to x before normalising.
+template <int OP>
+__host__ __device__ constexpr bool has_residual() {
+    return OP == OP_RESIDUAL_LAYERNORM || OP == OP_RESIDUAL_RMSNORM;
+}
+
+// Cross-entropy label handling: the logit of the label, 0-loss rows for the
+// ignore index, NaN for any other label outside [0, cols).
+struct LabelInfo {
+    bool ignored;
+    bool valid;
+};
+__device__ __forceinline__ LabelInfo label_info(const KArgs &a, int32_t lab,
+                                                int cols) {
+    LabelInfo li;
+    li.ignored = a.has_ignore && lab == a.ignore_index;
+    li.valid = lab >= 0 && lab < cols;
+    return li;
+}
+
 // ---- storage types ---------------------------------------------------------
 // Conversions between 32-bit words holding T values and FP32.
 template <typename T>
@@ -408,7 +428,7 @@ __device__ __forceinline__ void prefetch_group(const KArgs &a, int64_t g) {
     const int64_t nr = a.rows - r0 < a.B ? a.rows - r0 : a.B;
     const int64_t bytes = nr * (int64_t)a.cols * (int64_t)sizeof(T);
     prefetch_l2(static_cast<const T *>(a.x) + r0 * a.cols, bytes);
-    if constexpr (OP == OP_RESIDUAL_LAYERNORM)
+    if constexpr (has_residual<OP>())
         prefetch_l2(static_cast<const T *>(a.res) + r0 * a.cols, bytes);
 }
 
@@ -539,7 +559,8 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
     const int slot = threadIdx.x >> a.log2W;
     const int cols = a.cols;
     const int64_t ngroups = (a.rows + a.B - 1) / a.B;
-    constexpr bool kMaxFill = (OP == OP_SOFTMAX || OP == OP_CROSS_ENTROPY);
+    constexpr bool kMaxFill = (OP == OP_SOFTMAX || OP == OP_CROSS_ENTROPY ||
+                               OP == OP_LOG_SOFTMAX);
     const float fill = kMaxFill ? -INFINITY : 0.f;
     constexpr bool kHead = !AL && V > 1;
     const bool yvec = AL || a.y_vec;
@@ -562,7 +583,7 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
                                 fill, v[k]);
         if (head) hv = to_f(X[geo.base + worker]);
 
-        if constexpr (OP == OP_RESIDUAL_LAYERNORM) {
+        if constexpr (has_residual<OP>()) {
             const T *R = static_cast<const T *>(a.res);
             const T *rb = R + geo.base + geo.hd;
             const bool rvec = AL || a.r_vec;
@@ -590,15 +611,18 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
         // Cross-entropy: fetch the label and its logit while the row loads
         // are in flight.
         float xl = 0.f;
+        bool ignored = false;
         if constexpr (OP == OP_CROSS_ENTROPY) {
             if (active && worker == 0) {
                 const int32_t lab = __ldg(a.labels + row);
-                xl = (lab >= 0 && lab < cols) ? to_f(X[geo.base + lab]) : NAN;
+                const LabelInfo li = label_info(a, lab, cols);
+                ignored = li.ignored;
+                xl = li.valid ? to_f(X[geo.base + lab]) : NAN;
             }
         }
 
         // ---- per-operator reduction and epilogue ----------------------
-        if constexpr (OP == OP_RMSNORM) {
+        if constexpr (OP == OP_RMSNORM || OP == OP_RESIDUAL_RMSNORM) {
             float acc[V];
 #pragma unroll
             for (int e = 0; e < V; ++e) acc[e] = 0.f;
@@ -755,7 +779,42 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
 #pragma unroll
             for (int e = 0; e < V; ++e) s += acc[e];
             s = row_allreduce<SumOp>(s, W, red, parity);
-            if (active && worker == 0) a.out[row] = (m + logf(s)) - xl;
+            if (active && worker == 0)
+                a.out[row] = ignored ? 0.f : (m + logf(s)) - xl;
+        } else if constexpr (OP == OP_LOG_SOFTMAX) {
+            float mx[V];
+#pragma unroll
+            for (int e = 0; e < V; ++e) mx[e] = hv;
+#pragma unroll
+            for (int k = 0; k < K; ++k)
+#pragma unroll
+                for (int e = 0; e < V; ++e) mx[e] = nanmax(mx[e], v[k][e]);
+            float m = mx[0];
+#pragma unroll
+            for (int e = 1; e < V; ++e) m = nanmax(m, mx[e]);
+            m = row_allreduce<MaxOp>(m, W, red, parity);
+            float acc[V];
+#pragma unroll
+            for (int e = 0; e < V; ++e) acc[e] = 0.f;
+#pragma unroll
+            for (int k = 0; k < K; ++k)
+#pragma unroll
+                for (int e = 0; e < V; ++e) acc[e] += exp_shifted(v[k][e] - m);
+            float s = head ? exp_shifted(hv - m) : 0.f;
+#pragma unroll
+            for (int e = 0; e < V; ++e) s += acc[e];
+            s = row_allreduce<SumOp>(s, W, red, parity);
+            const float ls = logf(s);
+            T *yb = Y + geo.base + geo.hd;
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                float o[V];
+#pragma unroll
+                for (int e = 0; e < V; ++e) o[e] = (v[k][e] - m) - ls;
+                store_pack<T, V, AL>(yb, (k * W + worker) * V, nb, active,
+                                     yvec, o);
+            }
+            if (head) Y[geo.base + worker] = from_f<T>((hv - m) - ls);
         }
     }
 }
@@ -827,7 +886,7 @@ __global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
         auto load_x = [&](int off, int nv, float *t) {
             if (off < 0) {
                 t[0] = to_f(xrow[-1 - off]);
-                if constexpr (OP == OP_RESIDUAL_LAYERNORM)
+                if constexpr (has_residual<OP>())
                     t[0] = __fadd_rn(
                         t[0], to_f(static_cast<const T *>(a.res)[base - 1 - off]));
                 return;
@@ -839,7 +898,7 @@ __global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
                 for (int e = 0; e < V; ++e)
                     t[e] = e < nv ? to_f(xb[off + e]) : 0.f;
             }
-            if constexpr (OP == OP_RESIDUAL_LAYERNORM) {
+            if constexpr (has_residual<OP>()) {
                 const T *rb = static_cast<const T *>(a.res) + base + hd;
                 float r[V];
                 if (nv == V && (AL || a.r_vec)) {
@@ -856,7 +915,7 @@ __global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
         // Column of a head element (off < 0).
         auto column = [&](int off) { return -1 - off; };
 
-        if constexpr (OP == OP_RMSNORM) {
+        if constexpr (OP == OP_RMSNORM || OP == OP_RESIDUAL_RMSNORM) {
             float ss = 0.f;
             stream_row<V, AL, U>(worker, W, hd, nb, active, load_x,
                                  [&](const float *t, int nv, int) {
@@ -867,12 +926,17 @@ __global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
             ss = row_allreduce<SumOp>(ss, W, red, parity);
             const float r = rsqrtf(ss / (float)cols + a.eps);
             T *yb = Y + base + hd;
+            T *H = static_cast<T *>(a.h);
+            T *hb = H ? H + base + hd : nullptr;
+            const bool hvec = AL || a.h_vec;
             stream_row<V, AL, U>(
                 worker, W, hd, nb, active, load_x,
                 [&](const float *t, int nv, int off) {
                     if (off < 0) {
                         const int c = column(off);
                         Y[base + c] = from_f<T>(t[0] * r * param_at(Wt, c, 1.f));
+                        if (OP == OP_RESIDUAL_RMSNORM && H)
+                            H[base + c] = from_f<T>(t[0]);
                         return;
                     }
                     float wv[V], o[V];
@@ -880,6 +944,8 @@ __global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
 #pragma unroll
                     for (int e = 0; e < V; ++e) o[e] = t[e] * r * wv[e];
                     store_pack<T, V, AL>(yb, off, nb, true, yvec, o);
+                    if (OP == OP_RESIDUAL_RMSNORM && hb)
+                        store_pack<T, V, AL>(hb, off, nb, true, hvec, t);
                 });
         } else if constexpr (OP == OP_LAYERNORM ||
                              OP == OP_RESIDUAL_LAYERNORM) {
@@ -930,7 +996,8 @@ __global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
                     if (OP == OP_RESIDUAL_LAYERNORM && hb)
                         store_pack<T, V, AL>(hb, off, nb, true, hvec, t);
                 });
-        } else if constexpr (OP == OP_SOFTMAX || OP == OP_CROSS_ENTROPY) {
+        } else if constexpr (OP == OP_SOFTMAX || OP == OP_CROSS_ENTROPY ||
+                             OP == OP_LOG_SOFTMAX) {
             float m = -INFINITY, s = 0.f;
             stream_row<V, AL, U>(worker, W, hd, nb, active, load_x,
                                  [&](const float *t, int nv, int) {
@@ -961,12 +1028,27 @@ __global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
                         for (int e = 0; e < V; ++e) o[e] = exp_shifted(t[e] - m) * inv;
                         store_pack<T, V, AL>(yb, off, nb, true, yvec, o);
                     });
+            } else if constexpr (OP == OP_LOG_SOFTMAX) {
+                const float ls = logf(s);
+                T *yb = Y + base + hd;
+                stream_row<V, AL, U>(
+                    worker, W, hd, nb, active, load_x,
+                    [&](const float *t, int nv, int off) {
+                        if (off < 0) {
+                            Y[base + column(off)] = from_f<T>((t[0] - m) - ls);
+                            return;
+                        }
+                        float o[V];
+#pragma unroll
+                        for (int e = 0; e < V; ++e) o[e] = (t[e] - m) - ls;
+                        store_pack<T, V, AL>(yb, off, nb, true, yvec, o);
+                    });
             } else {
                 if (active && worker == 0) {
                     const int32_t lab = __ldg(a.labels + row);
-                    const float xl =
-                        (lab >= 0 && lab < cols) ? to_f(X[base + lab]) : NAN;
-                    a.out[row] = (m + logf(s)) - xl;
+                    const LabelInfo li = label_info(a, lab, cols);
+                    const float xl = li.valid ? to_f(X[base + lab]) : NAN;
+                    a.out[row] = li.ignored ? 0.f : (m + logf(s)) - xl;
                 }
             }
         } else if constexpr (OP == OP_ROW_SUM) {

@@ -30,6 +30,9 @@ HOLDOUT_SEED = 20261202
 
 OPS = ("rmsnorm", "layernorm", "residual_layernorm", "softmax", "row_sum",
        "cross_entropy")
+# Fused variants built on the same engine.
+FUSED_OPS = ("residual_rmsnorm", "log_softmax")
+ALL_OPS = OPS + FUSED_OPS
 
 RMS_EPS = 1e-6
 LN_EPS = 1e-5
@@ -61,7 +64,7 @@ def make(op: str, rows: int, cols: int, seed: int, outliers: bool = False,
     """
     rng = np.random.default_rng(seed)
     shape = (rows, cols)
-    if op in ("softmax", "cross_entropy"):
+    if op in ("softmax", "cross_entropy", "log_softmax"):
         x = _normal(rng, shape, 2.0)
     else:
         x = _normal(rng, shape)
@@ -69,8 +72,10 @@ def make(op: str, rows: int, cols: int, seed: int, outliers: bool = False,
         mask = rng.random(shape, dtype=np.float32) < np.float32(0.01)
         x[mask] *= np.float32(100.0)
     d = {"x": x}
-    if op == "rmsnorm":
+    if op in ("rmsnorm", "residual_rmsnorm"):
         d["eps"] = RMS_EPS
+        if op == "residual_rmsnorm":
+            d["residual"] = _normal(rng, shape)
         if affine:
             d["weight"] = np.float32(1.0) + _normal(rng, (cols,), 0.1)
     elif op in ("layernorm", "residual_layernorm"):
@@ -82,7 +87,7 @@ def make(op: str, rows: int, cols: int, seed: int, outliers: bool = False,
             d["beta"] = _normal(rng, (cols,), 0.1)
     elif op == "cross_entropy":
         d["labels"] = rng.integers(0, cols, rows, dtype=np.int32)
-    elif op in ("softmax", "row_sum"):
+    elif op in ("softmax", "row_sum", "log_softmax"):
         pass
     else:
         raise ValueError(f"unknown op {op!r}")

@@ -43,6 +43,10 @@ def algorithmic_bytes(op, rows, cols, h_out=False, mean=False, dtype="f32"):
         return e * rc + 4 * rows
     if op == "cross_entropy":
         return e * rc + 8 * rows + (4 if mean else 0)
+    if op == "residual_rmsnorm":
+        return 3 * e * rc + e * cols + (e * rc if h_out else 0)
+    if op == "log_softmax":
+        return 2 * e * rc
     raise ValueError(op)
 
 
@@ -68,7 +72,7 @@ class Workload:
         self.host = d
         self.eps = float(d.get("eps", 0.0))
         self.mean = op == "cross_entropy"
-        self.h_out = op == "residual_layernorm"
+        self.h_out = op in ("residual_layernorm", "residual_rmsnorm")
         self.bytes = algorithmic_bytes(op, rows, cols, self.h_out, self.mean,
                                        dtype)
         params = {k: _device(d[k], dtype) for k in
@@ -85,8 +89,8 @@ class Workload:
                 s["residual"] = _device(d["residual"], dtype)
             if "labels" in d:
                 s["labels"] = torch.from_numpy(d["labels"]).cuda()
-            if op in ("rmsnorm", "layernorm", "softmax",
-                      "residual_layernorm"):
+            if op in ("rmsnorm", "layernorm", "softmax", "log_softmax",
+                      "residual_layernorm", "residual_rmsnorm"):
                 s["y"] = torch.empty_like(x0)
             if self.h_out:
                 s["h_out"] = torch.empty_like(x0)
@@ -123,7 +127,10 @@ class Workload:
                  "softmax": (("x", "y"), False),
                  "row_sum": (("x", "out"), False),
                  "cross_entropy": (("x", "labels", "loss", "mean_loss"),
-                                   False)}
+                                   False),
+                 "residual_rmsnorm": (("x", "residual", "weight", "y",
+                                       "h_out"), True),
+                 "log_softmax": (("x", "y"), False)}
         keys, has_eps = names[self.op]
         if plan is not None:
             self._plan_ref = plan if isinstance(plan, B.MtPlan) else \
@@ -134,7 +141,7 @@ class Workload:
             fname = "mt_row_reduce_with_plan"
             args = (B.OP_IDS[self.op], B.DTYPE_IDS[self.dtype], P("x"),
                     P("residual"), P("weight") or P("gamma"), P("beta"),
-                    P("labels"), P("y"), P("h_out"),
+                    P("labels"), B.MT_NO_IGNORE_INDEX, P("y"), P("h_out"),
                     P("out") or P("loss"), P("mean_loss"), R, C, eps, st,
                     ctypes.byref(self._plan_ref))
         else:

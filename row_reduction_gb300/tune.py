@@ -219,6 +219,8 @@ def write_table(records, path):
 
 
 def published_shapes(ops):
+    """RMSNorm: the published shapes and bandwidth sweep; every other
+    operator (the fused variants included): the family shapes."""
     shapes = []
     for op in ops:
         if op == "rmsnorm":
@@ -231,7 +233,7 @@ def published_shapes(ops):
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description="measured plan search")
-    ap.add_argument("--ops", default=",".join(inputs.OPS))
+    ap.add_argument("--ops", default=",".join(inputs.ALL_OPS))
     ap.add_argument("--shapes", default="published",
                     help="'published' or a list like 1024x4096,64x4096")
     ap.add_argument("--json", required=True)

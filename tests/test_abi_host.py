@@ -33,7 +33,7 @@ def header_symbols():
 
 def test_library_exports_every_declared_symbol():
     declared = header_symbols()
-    assert len(declared) == 33
+    assert len(declared) == 44
     L = mt.lib()
     for name in declared:
         assert hasattr(L, name), name
@@ -120,7 +120,7 @@ def test_plan_check(plan, cols, want):
     p = mt.make_plan(plan["W"], plan["V"], plan.get("chunks", 0),
                      plan.get("rows_per_block", 1), plan.get("path", REG),
                      plan.get("grid", 0))
-    for op in range(6):
+    for op in range(8):
         assert mt.mt_plan_check(op, cols, p) == want
 
 
@@ -159,7 +159,7 @@ def test_plan_check_per_storage_type():
 
 def test_plan_query_errors_and_describe():
     with pytest.raises(mt.MTError):
-        mt.mt_plan_query(6, 1, 1)
+        mt.mt_plan_query(8, 1, 1)
     with pytest.raises(mt.MTError):
         mt.mt_plan_query(0, -1, 1)
     with pytest.raises(mt.MTError):
@@ -224,20 +224,25 @@ def test_generic_and_half_entry_points_validate_before_launch():
     L = mt.lib()
     f = L.mt_row_reduce_with_plan
     # op, dtype, x, res, w, b, labels, y, h, out, mean, rows, cols, eps, s, plan
-    assert f(0, 2, A, None, None, None, None, A, None, None, None, 0, 8, 0.0,
-             None, None) == OK
+    NI = mt.MT_NO_IGNORE_INDEX
+    assert f(0, 2, A, None, None, None, None, NI, A, None, None, None, 0, 8,
+             0.0, None, None) == OK
     # a pointer the operator does not take
-    assert f(0, 2, A, None, None, None, None, A, None, A, None, 4, 8, 0.0,
-             None, None) == INV
-    assert f(3, 0, A, None, A, None, None, A, None, None, None, 4, 8, 0.0,
-             None, None) == INV
-    # a missing required pointer / unknown op or dtype
-    assert f(4, 1, A, None, None, None, None, None, None, None, None, 4, 8,
+    assert f(0, 2, A, None, None, None, None, NI, A, None, A, None, 4, 8,
              0.0, None, None) == INV
-    assert f(6, 0, A, None, None, None, None, A, None, None, None, 4, 8, 0.0,
-             None, None) == INV
-    assert f(0, 3, A, None, None, None, None, A, None, None, None, 4, 8, 0.0,
-             None, None) == INV
+    assert f(3, 0, A, None, A, None, None, NI, A, None, None, None, 4, 8,
+             0.0, None, None) == INV
+    assert f(7, 0, A, A, None, None, None, NI, A, None, None, None, 4, 8,
+             0.0, None, None) == INV
+    # a missing required pointer / unknown op or dtype
+    assert f(4, 1, A, None, None, None, None, NI, None, None, None, None, 4,
+             8, 0.0, None, None) == INV
+    assert f(6, 0, A, None, None, None, None, NI, A, None, None, None, 4, 8,
+             0.0, None, None) == INV      # residual RMSNorm needs residual
+    assert f(8, 0, A, None, None, None, None, NI, A, None, None, None, 4, 8,
+             0.0, None, None) == INV
+    assert f(0, 3, A, None, None, None, None, NI, A, None, None, None, 4, 8,
+             0.0, None, None) == INV
     # 16-bit storage needs 2-byte alignment; FP32 outputs need 4
     assert L.mt_rmsnorm_bf16(A + 1, None, A, 4, 8, 1e-6, None) == INV
     assert L.mt_rmsnorm_bf16(A + 2, None, A + 6, 0, 8, 1e-6, None) == OK

@@ -273,3 +273,65 @@ def test_generator_recipe():
     b = inputs.make("layernorm", 2, 8, seed=4)
     assert np.array_equal(a["x"], b["x"]) and np.array_equal(a["beta"],
                                                              b["beta"])
+
+
+# ------------------------------------------------------ fused variants
+def test_residual_rmsnorm_matches_torch_and_reduces_to_rmsnorm(oracle_mod):
+    d = inputs.make("residual_rmsnorm", 4, 333, seed=21)
+    y, h = oracle_mod.residual_rmsnorm(d["x"], d["residual"], d["weight"],
+                                       d["eps"])
+    hs = torch.from_numpy(d["x"]).double() + torch.from_numpy(
+        d["residual"]).double()
+    t = F.rms_norm(hs, (333,), torch.from_numpy(d["weight"]).double(),
+                   f32(d["eps"]))
+    assert np.allclose(y, t.numpy(), rtol=1e-12, atol=1e-14)
+    assert np.array_equal(h.view(np.uint32),
+                          (d["x"] + d["residual"]).view(np.uint32))
+    y0, h0 = oracle_mod.residual_rmsnorm(d["x"], np.zeros_like(d["x"]),
+                                         d["weight"], d["eps"])
+    assert np.array_equal(y0, oracle_mod.rmsnorm(d["x"], d["weight"],
+                                                 d["eps"]))
+    # hand case: x + r = [3, 4]
+    yh, _ = oracle_mod.residual_rmsnorm(rows_of([1.0, 5.0]),
+                                        rows_of([2.0, -1.0]), None, 0.0)
+    assert np.allclose(yh[0], [3 / math.sqrt(12.5), 4 / math.sqrt(12.5)],
+                       rtol=1e-15)
+
+
+def test_log_softmax_hand_cases_and_torch(oracle_mod):
+    y = oracle_mod.log_softmax(rows_of([0.0, f32(math.log(2)),
+                                        f32(math.log(3))]))
+    assert np.allclose(y[0], [math.log(1 / 6), math.log(1 / 3),
+                              math.log(1 / 2)], atol=1e-7)
+    y = oracle_mod.log_softmax(rows_of([1000.0, 1000.0]))
+    assert np.allclose(y, -math.log(2), rtol=1e-15)
+    assert oracle_mod.log_softmax(rows_of([7.0]))[0, 0] == 0.0
+    d = inputs.make("log_softmax", 6, 500, seed=22)
+    y = oracle_mod.log_softmax(d["x"])
+    t = torch.log_softmax(torch.from_numpy(d["x"]).double(), dim=1)
+    assert np.allclose(y, t.numpy(), rtol=1e-12, atol=1e-12)
+    assert np.allclose(np.exp(y).sum(axis=1), 1.0, atol=1e-12)
+    assert np.isnan(oracle_mod.log_softmax(rows_of([1.0, np.nan]))).all()
+
+
+def test_cross_entropy_ignore_index(oracle_mod):
+    d = inputs.make("cross_entropy", 12, 300, seed=23)
+    lab = d["labels"].copy()
+    lab[[1, 4, 5]] = -100
+    loss, mean = oracle_mod.cross_entropy_ignore(d["x"], lab, -100)
+    xt = torch.from_numpy(d["x"]).double()
+    lt = torch.from_numpy(lab).long()
+    t = F.cross_entropy(xt, lt, ignore_index=-100, reduction="none")
+    assert np.allclose(loss, t.numpy(), rtol=1e-12)
+    assert loss[1] == 0.0 and loss[4] == 0.0
+    tm = F.cross_entropy(xt, lt, ignore_index=-100, reduction="mean")
+    assert math.isclose(mean, float(tm), rel_tol=1e-12)
+    # an in-range ignore index; every row ignored gives a NaN mean
+    lab2 = np.zeros(12, np.int32)
+    loss2, mean2 = oracle_mod.cross_entropy_ignore(d["x"], lab2, 0)
+    assert (loss2 == 0).all() and math.isnan(mean2)
+    # a label out of range that is not the ignore index is still NaN
+    lab3 = d["labels"].copy()
+    lab3[0] = 300
+    loss3, mean3 = oracle_mod.cross_entropy_ignore(d["x"], lab3, -100)
+    assert math.isnan(loss3[0]) and math.isnan(mean3)

@@ -22,7 +22,7 @@ from gpu_util import Guarded, assert_close, to_dev
 
 pytestmark = pytest.mark.gpu
 
-OPS = list(inputs.OPS)
+OPS = list(inputs.ALL_OPS)
 SEED = inputs.TUNE_SEED
 
 
@@ -55,14 +55,22 @@ def call(op, p, rows, cols, eps=None, plan=None, stream=None):
         mt.mt_cross_entropy_f32_with_plan(p["x"], p["labels"], p["loss"],
                                           p.get("mean_loss"), rows, cols,
                                           stream, plan)
+    elif op == "residual_rmsnorm":
+        mt.mt_residual_rmsnorm_f32_with_plan(p["x"], p["residual"],
+                                             p.get("weight"), p["y"],
+                                             p.get("h_out"), rows, cols, eps,
+                                             stream, plan)
+    elif op == "log_softmax":
+        mt.mt_log_softmax_f32_with_plan(p["x"], p["y"], rows, cols, stream,
+                                        plan)
     else:
         raise ValueError(op)
 
 
 def outputs_of(op, rows, cols):
-    if op in ("rmsnorm", "layernorm", "softmax"):
+    if op in ("rmsnorm", "layernorm", "softmax", "log_softmax"):
         return {"y": rows * cols}
-    if op == "residual_layernorm":
+    if op in ("residual_layernorm", "residual_rmsnorm"):
         return {"y": rows * cols, "h_out": rows * cols}
     if op == "row_sum":
         return {"out": rows}
@@ -437,3 +445,55 @@ def test_cross_entropy_mean_on_concurrent_streams():
         got = outs[k][1].cpu().numpy()
         assert_close(got, np.full(20, ref_mean), f"stream {k}")
         assert len(set(got.tolist())) == 1     # deterministic per stream
+
+
+# ------------------------------------------------------ ignore index
+@pytest.mark.parametrize("ignore_index", [-100, 0, 7])
+def test_cross_entropy_ignore_index(ignore_index):
+    rows, cols = 1024, 4096
+    d = inputs.make("cross_entropy", rows, cols, SEED + 11)
+    lab = d["labels"].copy()
+    lab[::3] = ignore_index
+    lab[5] = cols + 3                 # out of range, not ignored: NaN
+    t = to_dev(d)
+    lt = torch.from_numpy(lab).cuda()
+    loss = torch.empty(rows, device="cuda")
+    mean = torch.empty(1, device="cuda")
+    mt.mt_cross_entropy_ignore_f32(t["x"], lt, ignore_index, loss, mean,
+                                   rows, cols)
+    ref_loss, ref_mean = oracle.cross_entropy_ignore(d["x"], lab,
+                                                     ignore_index)
+    assert_close(loss.cpu().numpy(), ref_loss, "loss")
+    assert np.isnan(mean.item()) and np.isnan(ref_mean)
+    lab[5] = 1
+    lt = torch.from_numpy(lab).cuda()
+    for plan in (None, mt.make_plan(128, 4, 8, 1),
+                 mt.make_plan(256, 4, 0, 1, mt.MT_PATH_LOOP)):
+        l2, m2 = mt.cross_entropy(t["x"], lt, ignore_index=ignore_index,
+                                  plan=plan)
+        ref_loss, ref_mean = oracle.cross_entropy_ignore(d["x"], lab,
+                                                         ignore_index)
+        assert_close(l2.cpu().numpy(), ref_loss, f"loss {plan}")
+        assert_close(m2.cpu().numpy(), np.array([ref_mean]), f"mean {plan}")
+    # every row ignored: NaN mean, zero losses
+    allig = torch.full((rows,), ignore_index, dtype=torch.int32,
+                       device="cuda")
+    l3, m3 = mt.cross_entropy(t["x"], allig, ignore_index=ignore_index)
+    assert (l3 == 0).all() and np.isnan(m3.item())
+
+
+def test_residual_rmsnorm_aliasing_and_zero_residual():
+    rows, cols = 64, 4096
+    d = inputs.make("residual_rmsnorm", rows, cols, SEED + 12)
+    t = to_dev(d)
+    y, h = mt.residual_rmsnorm(t["x"], t["residual"], t["weight"], d["eps"],
+                               return_h=True)
+    assert torch.equal(h, t["x"] + t["residual"])
+    x2, r2 = t["x"].clone(), t["residual"].clone()
+    mt.mt_residual_rmsnorm_f32(x2, r2, t["weight"], x2, r2, rows, cols,
+                               d["eps"])
+    assert torch.equal(x2, y) and torch.equal(r2, h)
+    y0 = mt.residual_rmsnorm(t["x"], torch.zeros_like(t["x"]), t["weight"],
+                             d["eps"])
+    assert_close(y0.cpu().numpy(), oracle.rmsnorm(d["x"], d["weight"],
+                                                  d["eps"]), "r = 0")

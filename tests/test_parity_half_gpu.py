@@ -19,11 +19,12 @@ from gpu_util import Guarded, assert_close
 pytestmark = pytest.mark.gpu
 
 DTYPES = ["f16", "bf16"]
-OPS = list(inputs.OPS)
+OPS = list(inputs.ALL_OPS)
 SEED = inputs.TUNE_SEED + 100
 MATRIX_OUT = {"rmsnorm": ["y"], "layernorm": ["y"], "softmax": ["y"],
               "residual_layernorm": ["y", "h_out"], "row_sum": [],
-              "cross_entropy": []}
+              "cross_entropy": [], "residual_rmsnorm": ["y", "h_out"],
+              "log_softmax": ["y"]}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -77,9 +78,10 @@ def run(op, st, dt, rows, cols, plan=None, typed=False):
     eps = st.get("eps", 0.0)
     tdt = torch.bfloat16 if dt == "bf16" else torch.float16
     outs = {}
-    if op in ("rmsnorm", "layernorm", "softmax", "residual_layernorm"):
+    if op in ("rmsnorm", "layernorm", "softmax", "residual_layernorm",
+              "residual_rmsnorm", "log_softmax"):
         outs["y"] = torch.full((rows, cols), -7.0, dtype=tdt, device="cuda")
-    if op == "residual_layernorm":
+    if op in ("residual_layernorm", "residual_rmsnorm"):
         outs["h_out"] = torch.full((rows, cols), -7.0, dtype=tdt,
                                    device="cuda")
     if op == "row_sum":
@@ -103,7 +105,13 @@ def run(op, st, dt, rows, cols, plan=None, typed=False):
                  t["x"], outs["out"], rows, cols),
              "cross_entropy": lambda: getattr(mt, f"mt_cross_entropy_{dt}")(
                  t["x"], t["labels"], outs["loss"], outs["mean_loss"], rows,
-                 cols)}[op]
+                 cols),
+             "residual_rmsnorm": lambda: getattr(
+                 mt, f"mt_residual_rmsnorm_{dt}")(
+                 t["x"], t["residual"], t.get("weight"), outs["y"],
+                 outs["h_out"], rows, cols, eps),
+             "log_softmax": lambda: getattr(mt, f"mt_log_softmax_{dt}")(
+                 t["x"], outs["y"], rows, cols)}[op]
         f()
     else:
         mt.mt_row_reduce_with_plan(
@@ -268,3 +276,19 @@ def test_in_place_and_determinism(dt, op):
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
     f(x, out=x, **kw)
     assert torch.equal(x.view(torch.int16), a.view(torch.int16))
+
+
+@pytest.mark.parametrize("dt", DTYPES)
+def test_cross_entropy_ignore_index_half(dt):
+    rows, cols = 512, 1000
+    st, wide = case("cross_entropy", rows, cols, dt, SEED + 9)
+    lab = st["labels"].copy()
+    lab[1::4] = -100
+    x = dev(st["x"], dt)
+    loss = torch.empty(rows, device="cuda")
+    mean = torch.empty(1, device="cuda")
+    getattr(mt, f"mt_cross_entropy_ignore_{dt}")(
+        x, torch.from_numpy(lab).cuda(), -100, loss, mean, rows, cols)
+    ref_loss, ref_mean = oracle.cross_entropy_ignore(wide["x"], lab, -100)
+    assert_close(loss.cpu().numpy(), ref_loss, "loss")
+    assert_close(mean.cpu().numpy(), np.array([ref_mean]), "mean")
