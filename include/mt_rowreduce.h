@@ -131,6 +131,14 @@ typedef struct mt_plan {
                                   resident on the device), the CTAs then loop
                                   over row groups (grid-stride) */
     int32_t flags;             /* MT_PLAN_* bits */
+    int32_t cluster;           /* CTAs sharing one row: 0 or 1 = none; 2, 4
+                                  or 8 = a thread-block cluster of that many
+                                  CTAs splits every row (then
+                                  rows_per_block = 1, W >= 32, 16-byte packs
+                                  (V*element size = 16), the ownership map
+                                  spans cluster*W workers, and an explicit
+                                  grid counts CTAs, a multiple of the
+                                  cluster size) */
 } mt_plan_t;
 
 /* Plan flag: launch as a programmatic dependent of the previous kernel on

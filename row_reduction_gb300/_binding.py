@@ -81,7 +81,8 @@ class MtPlan(ctypes.Structure):
                 ("rows_per_block", ctypes.c_int32),
                 ("path", ctypes.c_int32),
                 ("grid", ctypes.c_int32),
-                ("flags", ctypes.c_int32)]
+                ("flags", ctypes.c_int32),
+                ("cluster", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {f: getattr(self, f) for f, _ in self._fields_}
@@ -91,8 +92,8 @@ class MtPlan(ctypes.Structure):
 
 
 def make_plan(W, V, chunks=0, rows_per_block=1, path=MT_PATH_REGISTERS,
-              grid=0, flags=0) -> MtPlan:
-    return MtPlan(W, V, chunks, rows_per_block, path, grid, flags)
+              grid=0, flags=0, cluster=0) -> MtPlan:
+    return MtPlan(W, V, chunks, rows_per_block, path, grid, flags, cluster)
 
 
 class MTError(RuntimeError):

@@ -224,9 +224,12 @@ mt_status run(const Call &c, const mt_plan_t *forced, cudaStream_t stream) {
     a.B = p.rows_per_block;
     a.pdl = (p.flags & MT_PLAN_PDL) ? 1 : 0;
     a.prefetch_next = (p.flags & MT_PLAN_PREFETCH_NEXT) ? 1 : 0;
+    a.csize = p.cluster > 1 ? p.cluster : 1;
+    const int64_t C = a.csize;
 
+    // Row groups are processed by CTAs, or by clusters of C CTAs.
     const int64_t ngroups = (a.rows + a.B - 1) / a.B;
-    int64_t grid = p.grid;
+    int64_t grid = p.grid / C;  // in units of row-group workers
     if (grid == 0) {
         int dev = 0;
         cudaError_t e = cudaGetDevice(&dev);
@@ -237,11 +240,12 @@ mt_status run(const Call &c, const mt_plan_t *forced, cudaStream_t stream) {
         e = blocks_per_sm(dev, c.op, c.dtype, p, aligned, &bps);
         if (e != cudaSuccess) return cuda_status(e);
         if (bps < 1) return MT_ERR_OUT_OF_RESOURCES;
-        grid = (int64_t)sms * bps;
+        grid = (int64_t)sms * bps / C;
+        if (grid < 1) grid = 1;
     }
     if (grid > ngroups) grid = ngroups;
-    if (grid > 0x7fffffff) grid = 0x7fffffff;
-    p.grid = (int32_t)grid;
+    if (grid * C > 0x7fffffff) grid = 0x7fffffff / C;
+    p.grid = (int32_t)(grid * C);
 
     if (mt_status st =
             cuda_status(kLaunch[c.op][c.dtype](p, a, aligned, stream)))

@@ -60,6 +60,8 @@ struct KArgs {
     int32_t pdl;
     // Persistent CTAs prefetch their next row group into L2.
     int32_t prefetch_next;
+    // CTAs per row (thread-block cluster size; 1 = no cluster).
+    int32_t csize;
 };
 
 // Instantiated register-path chunk counts.

@@ -259,6 +259,7 @@ struct MaxOp {
 
 struct RedScratch {
     float buf[2][2][32];  // [alternating buffer][component][warp]
+    float cl[2][2];       // cluster exchange: [alternating buffer][component]
 };
 
 // All-reduce of one value over the W threads of each row; every thread of
@@ -392,6 +393,125 @@ __device__ __forceinline__ void row_allreduce_lse(float &m, float &s, int W,
     s = __shfl_sync(kFull, ts, 0);
 }
 
+// ---- split rows: thread-block clusters -------------------------------------
+// With a cluster of `csize` CTAs per row, each CTA reduces its slice of the
+// row as above, thread 0 publishes the CTA total in its own shared memory,
+// one cluster barrier (release/acquire) makes the totals visible, and every
+// CTA reads all csize totals through distributed shared memory and combines
+// them in rank order -- the same single-barrier, private-scratch scheme as
+// the cross-warp stage, one level up.  Consecutive cluster reductions
+// alternate between two slots, so the next cluster barrier keeps a slot from
+// being rewritten before every peer has read it; a last cluster barrier
+// before exit keeps each CTA's shared memory alive until its peers are done.
+// Every CTA of a cluster runs the same number of loop iterations and hence
+// the same number of cluster barriers.
+__device__ __forceinline__ unsigned cluster_ctarank() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ unsigned cluster_id_x() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ unsigned num_clusters_x() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile(
+        "barrier.cluster.arrive.release.aligned;\n\t"
+        "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Reads a float at the same shared-memory offset in the CTA of cluster rank
+// `rank`.
+__device__ __forceinline__ float ld_cluster(const float *p, unsigned rank) {
+    const unsigned la = (unsigned)__cvta_generic_to_shared(p);
+    unsigned ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                 : "=r"(ra)
+                 : "r"(la), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];"
+                 : "=f"(v)
+                 : "r"(ra)
+                 : "memory");
+    return v;
+}
+
+// Row all-reduces over a team: the W threads of this CTA, then (csize > 1)
+// the csize CTAs of the cluster.  `cpar` alternates the cluster slots.
+template <class Op>
+__device__ __forceinline__ float team_allreduce(float v, int W, int csize,
+                                                RedScratch &red, int &parity,
+                                                int &cpar) {
+    v = row_allreduce<Op>(v, W, red, parity);
+    if (csize > 1) {
+        Op op;
+        if (threadIdx.x == 0) red.cl[cpar][0] = v;
+        cluster_sync();
+        const int lane = threadIdx.x & 31;
+        float t = lane < csize ? ld_cluster(&red.cl[cpar][0], lane)
+                               : Op::ident();
+        for (int off = csize >> 1; off > 0; off >>= 1)
+            t = op(t, __shfl_xor_sync(kFull, t, off));
+        v = __shfl_sync(kFull, t, 0);
+        cpar ^= 1;
+    }
+    return v;
+}
+
+__device__ __forceinline__ void team_allreduce_compensated(
+    float &s, float &c, int W, int csize, RedScratch &red, int &parity,
+    int &cpar) {
+    row_allreduce_compensated(s, c, W, red, parity);
+    if (csize > 1) {
+        if (threadIdx.x == 0) {
+            red.cl[cpar][0] = s;
+            red.cl[cpar][1] = c;
+        }
+        cluster_sync();
+        const int lane = threadIdx.x & 31;
+        float ts = lane < csize ? ld_cluster(&red.cl[cpar][0], lane) : 0.f;
+        float tc = lane < csize ? ld_cluster(&red.cl[cpar][1], lane) : 0.f;
+        for (int off = csize >> 1; off > 0; off >>= 1) {
+            const float s2 = __shfl_xor_sync(kFull, ts, off);
+            const float c2 = __shfl_xor_sync(kFull, tc, off);
+            pair_add(ts, tc, s2, c2);
+        }
+        s = __shfl_sync(kFull, ts, 0);
+        c = __shfl_sync(kFull, tc, 0);
+        cpar ^= 1;
+    }
+}
+
+__device__ __forceinline__ void team_allreduce_lse(float &m, float &s, int W,
+                                                   int csize, RedScratch &red,
+                                                   int &parity, int &cpar) {
+    row_allreduce_lse(m, s, W, red, parity);
+    if (csize > 1) {
+        if (threadIdx.x == 0) {
+            red.cl[cpar][0] = m;
+            red.cl[cpar][1] = s;
+        }
+        cluster_sync();
+        const int lane = threadIdx.x & 31;
+        float tm = lane < csize ? ld_cluster(&red.cl[cpar][0], lane)
+                                : -INFINITY;
+        float ts = lane < csize ? ld_cluster(&red.cl[cpar][1], lane) : 0.f;
+        for (int off = csize >> 1; off > 0; off >>= 1) {
+            const float m2 = __shfl_xor_sync(kFull, tm, off);
+            const float s2 = __shfl_xor_sync(kFull, ts, off);
+            lse_merge(tm, ts, m2, s2, (lane & off) == 0);
+        }
+        m = __shfl_sync(kFull, tm, 0);
+        s = __shfl_sync(kFull, ts, 0);
+        cpar ^= 1;
+    }
+}
+
 // ---- launch overlap ---------------------------------------------------------
 // Programmatic dependent launch: the next kernel on the stream may start as
 // soon as every CTA of this one has started; griddepcontrol.wait then holds
@@ -432,23 +552,33 @@ __device__ __forceinline__ void prefetch_group(const KArgs &a, int64_t g) {
         prefetch_l2(static_cast<const T *>(a.res) + r0 * a.cols, bytes);
 }
 
-// Persistent CTAs: with `prefetch_next`, thread 0 asks L2 for the row group
-// the CTA will process after `g`, so its DRAM reads overlap this one.
+// Persistent CTAs: with `prefetch_next`, thread 0 (of cluster rank 0) asks
+// L2 for the row group processed after `g`, so its DRAM reads overlap this
+// one.
 template <int OP, typename T>
 __device__ __forceinline__ void prefetch_next_group(const KArgs &a,
                                                     int64_t g,
-                                                    int64_t ngroups) {
-    const int64_t gn = g + gridDim.x;
-    if (!a.prefetch_next || threadIdx.x != 0 || gn >= ngroups) return;
+                                                    int64_t ngroups,
+                                                    int64_t gstride,
+                                                    int rank) {
+    const int64_t gn = g + gstride;
+    if (!a.prefetch_next || threadIdx.x != 0 || rank != 0 || gn >= ngroups)
+        return;
     prefetch_group<OP, T>(a, gn);
 }
 
-// Kernel prologue: with `pdl`, thread 0 prefetches the CTA's first row group
-// into L2; then every thread lets dependents launch and waits for the
-// previous grid.
-template <int OP, typename T>
+// Kernel prologue: with `pdl`, thread 0 (of cluster rank 0) prefetches the
+// first row group into L2; then every thread lets dependents launch and
+// waits for the previous grid.
+template <int OP, typename T, bool CL>
 __device__ __forceinline__ void kernel_prologue(const KArgs &a) {
-    if (a.pdl && threadIdx.x == 0) prefetch_group<OP, T>(a, blockIdx.x);
+    if (a.pdl && threadIdx.x == 0) {
+        if (CL && a.csize > 1) {
+            if (cluster_ctarank() == 0) prefetch_group<OP, T>(a, cluster_id_x());
+        } else {
+            prefetch_group<OP, T>(a, blockIdx.x);
+        }
+    }
     grid_launch_dependents();
     grid_wait_prerequisites();
 }
@@ -544,19 +674,28 @@ __device__ __forceinline__ void param_row_pack(const T *p, int col,
 // =========================================================================
 // Register path
 // =========================================================================
-template <int OP, typename T, int V, int K, bool AL>
+template <int OP, typename T, int V, int K, bool AL, bool CL>
 __global__ void __launch_bounds__(reg_max_threads(V * K))
     reg_kernel(const KArgs a) {
-    kernel_prologue<OP, T>(a);
+    kernel_prologue<OP, T, CL>(a);
     __shared__ RedScratch red;
     int parity = 0;
     const T *X = static_cast<const T *>(a.x);
     const T *Wt = static_cast<const T *>(a.w);
     const T *Bt = static_cast<const T *>(a.b);
     T *Y = static_cast<T *>(a.y);
-    const int W = a.W;
-    const int worker = threadIdx.x & (W - 1);
+    const int W = a.W;             // threads of this CTA per row
+    // CTAs per row (thread-block cluster); the CL=false kernels fold every
+    // cluster step away.
+    const int csize = CL ? a.csize : 1;
+    const int rank = csize > 1 ? (int)cluster_ctarank() : 0;
+    const int WT = W * csize;      // workers per row
+    const int worker = rank * W + (int)(threadIdx.x & (W - 1));
     const int slot = threadIdx.x >> a.log2W;
+    const int64_t g0 = csize > 1 ? (int64_t)cluster_id_x() : blockIdx.x;
+    const int64_t gstride =
+        csize > 1 ? (int64_t)num_clusters_x() : (int64_t)gridDim.x;
+    int cpar = 0;
     const int cols = a.cols;
     const int64_t ngroups = (a.rows + a.B - 1) / a.B;
     constexpr bool kMaxFill = (OP == OP_SOFTMAX || OP == OP_CROSS_ENTROPY ||
@@ -565,8 +704,8 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
     constexpr bool kHead = !AL && V > 1;
     const bool yvec = AL || a.y_vec;
 
-    for (int64_t g = blockIdx.x; g < ngroups; g += gridDim.x) {
-        prefetch_next_group<OP, T>(a, g, ngroups);
+    for (int64_t g = g0; g < ngroups; g += gstride) {
+        prefetch_next_group<OP, T>(a, g, ngroups, gstride, rank);
         const int64_t row = g * a.B + slot;
         const bool active = row < a.rows;
         const RowGeom<T, V, AL> geo(X, active ? row : 0, cols);
@@ -579,7 +718,7 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
         float hv = fill;
 #pragma unroll
         for (int k = 0; k < K; ++k)
-            load_pack<T, V, AL>(xb, (k * W + worker) * V, nb, active, true,
+            load_pack<T, V, AL>(xb, (k * WT + worker) * V, nb, active, true,
                                 fill, v[k]);
         if (head) hv = to_f(X[geo.base + worker]);
 
@@ -590,7 +729,7 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
 #pragma unroll
             for (int k = 0; k < K; ++k) {
                 float t[V];
-                load_pack<T, V, AL>(rb, (k * W + worker) * V, nb, active,
+                load_pack<T, V, AL>(rb, (k * WT + worker) * V, nb, active,
                                     rvec, 0.f, t);
 #pragma unroll
                 for (int e = 0; e < V; ++e) v[k][e] = __fadd_rn(v[k][e], t[e]);
@@ -602,7 +741,7 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
                 const bool hvec = AL || a.h_vec;
 #pragma unroll
                 for (int k = 0; k < K; ++k)
-                    store_pack<T, V, AL>(hb, (k * W + worker) * V, nb, active,
+                    store_pack<T, V, AL>(hb, (k * WT + worker) * V, nb, active,
                                          hvec, v[k]);
                 if (head) H[geo.base + worker] = from_f<T>(hv);
             }
@@ -634,12 +773,12 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
             float ss = hv * hv;
 #pragma unroll
             for (int e = 0; e < V; ++e) ss += acc[e];
-            ss = row_allreduce<SumOp>(ss, W, red, parity);
+            ss = team_allreduce<SumOp>(ss, W, csize, red, parity, cpar);
             const float r = rsqrtf(ss / (float)cols + a.eps);
             T *yb = Y + geo.base + geo.hd;
 #pragma unroll
             for (int k = 0; k < K; ++k) {
-                const int off = (k * W + worker) * V;
+                const int off = (k * WT + worker) * V;
                 float wv[V], o[V];
                 param_row_pack<T, V, AL>(Wt, geo.hd + off, off, nb, active,
                                          1.f, wv);
@@ -662,13 +801,13 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
             float s = hv;
 #pragma unroll
             for (int e = 0; e < V; ++e) s += acc[e];
-            s = row_allreduce<SumOp>(s, W, red, parity);
+            s = team_allreduce<SumOp>(s, W, csize, red, parity, cpar);
             const float mean = s / (float)cols;
 #pragma unroll
             for (int e = 0; e < V; ++e) acc[e] = 0.f;
 #pragma unroll
             for (int k = 0; k < K; ++k) {
-                const int off = (k * W + worker) * V;
+                const int off = (k * WT + worker) * V;
 #pragma unroll
                 for (int e = 0; e < V; ++e) {
                     const float d = v[k][e] - mean;
@@ -682,12 +821,12 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
             }
 #pragma unroll
             for (int e = 0; e < V; ++e) q += acc[e];
-            q = row_allreduce<SumOp>(q, W, red, parity);
+            q = team_allreduce<SumOp>(q, W, csize, red, parity, cpar);
             const float rstd = rsqrtf(q / (float)cols + a.eps);
             T *yb = Y + geo.base + geo.hd;
 #pragma unroll
             for (int k = 0; k < K; ++k) {
-                const int off = (k * W + worker) * V;
+                const int off = (k * WT + worker) * V;
                 float gv[V], bv[V], o[V];
                 param_row_pack<T, V, AL>(Wt, geo.hd + off, off, nb, active,
                                          1.f, gv);
@@ -713,7 +852,7 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
             float m = mx[0];
 #pragma unroll
             for (int e = 1; e < V; ++e) m = nanmax(m, mx[e]);
-            m = row_allreduce<MaxOp>(m, W, red, parity);
+            m = team_allreduce<MaxOp>(m, W, csize, red, parity, cpar);
             float acc[V];
 #pragma unroll
             for (int e = 0; e < V; ++e) acc[e] = 0.f;
@@ -731,7 +870,7 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
             }
 #pragma unroll
             for (int e = 0; e < V; ++e) s += acc[e];
-            s = row_allreduce<SumOp>(s, W, red, parity);
+            s = team_allreduce<SumOp>(s, W, csize, red, parity, cpar);
             const float inv = 1.f / s;
             T *yb = Y + geo.base + geo.hd;
 #pragma unroll
@@ -739,7 +878,7 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
                 float o[V];
 #pragma unroll
                 for (int e = 0; e < V; ++e) o[e] = v[k][e] * inv;
-                store_pack<T, V, AL>(yb, (k * W + worker) * V, nb, active,
+                store_pack<T, V, AL>(yb, (k * WT + worker) * V, nb, active,
                                      yvec, o);
             }
             if (head) Y[geo.base + worker] = from_f<T>(hv * inv);
@@ -754,7 +893,7 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
                     s = t;
                     c += err;
                 }
-            row_allreduce_compensated(s, c, W, red, parity);
+            team_allreduce_compensated(s, c, W, csize, red, parity, cpar);
             if (active && worker == 0) a.out[row] = s + c;
         } else if constexpr (OP == OP_CROSS_ENTROPY) {
             float mx[V];
@@ -767,7 +906,7 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
             float m = mx[0];
 #pragma unroll
             for (int e = 1; e < V; ++e) m = nanmax(m, mx[e]);
-            m = row_allreduce<MaxOp>(m, W, red, parity);
+            m = team_allreduce<MaxOp>(m, W, csize, red, parity, cpar);
             float acc[V];
 #pragma unroll
             for (int e = 0; e < V; ++e) acc[e] = 0.f;
@@ -778,7 +917,7 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
             float s = head ? exp_shifted(hv - m) : 0.f;
 #pragma unroll
             for (int e = 0; e < V; ++e) s += acc[e];
-            s = row_allreduce<SumOp>(s, W, red, parity);
+            s = team_allreduce<SumOp>(s, W, csize, red, parity, cpar);
             if (active && worker == 0)
                 a.out[row] = ignored ? 0.f : (m + logf(s)) - xl;
         } else if constexpr (OP == OP_LOG_SOFTMAX) {
@@ -792,7 +931,7 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
             float m = mx[0];
 #pragma unroll
             for (int e = 1; e < V; ++e) m = nanmax(m, mx[e]);
-            m = row_allreduce<MaxOp>(m, W, red, parity);
+            m = team_allreduce<MaxOp>(m, W, csize, red, parity, cpar);
             float acc[V];
 #pragma unroll
             for (int e = 0; e < V; ++e) acc[e] = 0.f;
@@ -803,7 +942,7 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
             float s = head ? exp_shifted(hv - m) : 0.f;
 #pragma unroll
             for (int e = 0; e < V; ++e) s += acc[e];
-            s = row_allreduce<SumOp>(s, W, red, parity);
+            s = team_allreduce<SumOp>(s, W, csize, red, parity, cpar);
             const float ls = logf(s);
             T *yb = Y + geo.base + geo.hd;
 #pragma unroll
@@ -811,12 +950,14 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
                 float o[V];
 #pragma unroll
                 for (int e = 0; e < V; ++e) o[e] = (v[k][e] - m) - ls;
-                store_pack<T, V, AL>(yb, (k * W + worker) * V, nb, active,
+                store_pack<T, V, AL>(yb, (k * WT + worker) * V, nb, active,
                                      yvec, o);
             }
             if (head) Y[geo.base + worker] = from_f<T>((hv - m) - ls);
         }
     }
+    // Peers may still read this CTA's cluster slots.
+    if (csize > 1) cluster_sync();
 }
 
 // =========================================================================
@@ -854,9 +995,9 @@ __device__ __forceinline__ void stream_row(int worker, int W, int hd, int nb,
     }
 }
 
-template <int OP, typename T, int V, bool AL>
+template <int OP, typename T, int V, bool AL, bool CL>
 __global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
-    kernel_prologue<OP, T>(a);
+    kernel_prologue<OP, T, CL>(a);
     // Packs in flight per thread: 4, or 2 for 8-value packs (keeps the
     // residual LayerNorm variants within the register budget).
     constexpr int U = V >= 8 ? 2 : 4;
@@ -866,15 +1007,24 @@ __global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
     const T *Wt = static_cast<const T *>(a.w);
     const T *Bt = static_cast<const T *>(a.b);
     T *Y = static_cast<T *>(a.y);
-    const int W = a.W;
-    const int worker = threadIdx.x & (W - 1);
+    const int W = a.W;             // threads of this CTA per row
+    // CTAs per row (thread-block cluster); the CL=false kernels fold every
+    // cluster step away.
+    const int csize = CL ? a.csize : 1;
+    const int rank = csize > 1 ? (int)cluster_ctarank() : 0;
+    const int WT = W * csize;      // workers per row
+    const int worker = rank * W + (int)(threadIdx.x & (W - 1));
     const int slot = threadIdx.x >> a.log2W;
+    const int64_t g0 = csize > 1 ? (int64_t)cluster_id_x() : blockIdx.x;
+    const int64_t gstride =
+        csize > 1 ? (int64_t)num_clusters_x() : (int64_t)gridDim.x;
+    int cpar = 0;
     const int cols = a.cols;
     const int64_t ngroups = (a.rows + a.B - 1) / a.B;
     const bool yvec = AL || a.y_vec;
 
-    for (int64_t g = blockIdx.x; g < ngroups; g += gridDim.x) {
-        prefetch_next_group<OP, T>(a, g, ngroups);
+    for (int64_t g = g0; g < ngroups; g += gstride) {
+        prefetch_next_group<OP, T>(a, g, ngroups, gstride, rank);
         const int64_t row = g * a.B + slot;
         const bool active = row < a.rows;
         const RowGeom<T, V, AL> geo(X, active ? row : 0, cols);
@@ -917,20 +1067,20 @@ __global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
 
         if constexpr (OP == OP_RMSNORM || OP == OP_RESIDUAL_RMSNORM) {
             float ss = 0.f;
-            stream_row<V, AL, U>(worker, W, hd, nb, active, load_x,
+            stream_row<V, AL, U>(worker, WT, hd, nb, active, load_x,
                                  [&](const float *t, int nv, int) {
 #pragma unroll
                                      for (int e = 0; e < V; ++e)
                                          if (e < nv) ss = fmaf(t[e], t[e], ss);
                                  });
-            ss = row_allreduce<SumOp>(ss, W, red, parity);
+            ss = team_allreduce<SumOp>(ss, W, csize, red, parity, cpar);
             const float r = rsqrtf(ss / (float)cols + a.eps);
             T *yb = Y + base + hd;
             T *H = static_cast<T *>(a.h);
             T *hb = H ? H + base + hd : nullptr;
             const bool hvec = AL || a.h_vec;
             stream_row<V, AL, U>(
-                worker, W, hd, nb, active, load_x,
+                worker, WT, hd, nb, active, load_x,
                 [&](const float *t, int nv, int off) {
                     if (off < 0) {
                         const int c = column(off);
@@ -950,16 +1100,16 @@ __global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
         } else if constexpr (OP == OP_LAYERNORM ||
                              OP == OP_RESIDUAL_LAYERNORM) {
             float s = 0.f;
-            stream_row<V, AL, U>(worker, W, hd, nb, active, load_x,
+            stream_row<V, AL, U>(worker, WT, hd, nb, active, load_x,
                                  [&](const float *t, int nv, int) {
 #pragma unroll
                                      for (int e = 0; e < V; ++e)
                                          if (e < nv) s += t[e];
                                  });
-            s = row_allreduce<SumOp>(s, W, red, parity);
+            s = team_allreduce<SumOp>(s, W, csize, red, parity, cpar);
             const float mean = s / (float)cols;
             float q = 0.f;
-            stream_row<V, AL, U>(worker, W, hd, nb, active, load_x,
+            stream_row<V, AL, U>(worker, WT, hd, nb, active, load_x,
                                  [&](const float *t, int nv, int) {
 #pragma unroll
                                      for (int e = 0; e < V; ++e)
@@ -968,14 +1118,14 @@ __global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
                                              q = fmaf(d, d, q);
                                          }
                                  });
-            q = row_allreduce<SumOp>(q, W, red, parity);
+            q = team_allreduce<SumOp>(q, W, csize, red, parity, cpar);
             const float rstd = rsqrtf(q / (float)cols + a.eps);
             T *yb = Y + base + hd;
             T *H = static_cast<T *>(a.h);
             T *hb = H ? H + base + hd : nullptr;
             const bool hvec = AL || a.h_vec;
             stream_row<V, AL, U>(
-                worker, W, hd, nb, active, load_x,
+                worker, WT, hd, nb, active, load_x,
                 [&](const float *t, int nv, int off) {
                     if (off < 0) {
                         const int c = column(off);
@@ -999,7 +1149,7 @@ __global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
         } else if constexpr (OP == OP_SOFTMAX || OP == OP_CROSS_ENTROPY ||
                              OP == OP_LOG_SOFTMAX) {
             float m = -INFINITY, s = 0.f;
-            stream_row<V, AL, U>(worker, W, hd, nb, active, load_x,
+            stream_row<V, AL, U>(worker, WT, hd, nb, active, load_x,
                                  [&](const float *t, int nv, int) {
                                      float pm = -INFINITY;
 #pragma unroll
@@ -1011,12 +1161,12 @@ __global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
                                          if (e < nv) ps += exp_shifted(t[e] - pm);
                                      lse_merge(m, s, pm, ps);
                                  });
-            row_allreduce_lse(m, s, W, red, parity);
+            team_allreduce_lse(m, s, W, csize, red, parity, cpar);
             if constexpr (OP == OP_SOFTMAX) {
                 const float inv = 1.f / s;
                 T *yb = Y + base + hd;
                 stream_row<V, AL, U>(
-                    worker, W, hd, nb, active, load_x,
+                    worker, WT, hd, nb, active, load_x,
                     [&](const float *t, int nv, int off) {
                         if (off < 0) {
                             Y[base + column(off)] =
@@ -1032,7 +1182,7 @@ __global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
                 const float ls = logf(s);
                 T *yb = Y + base + hd;
                 stream_row<V, AL, U>(
-                    worker, W, hd, nb, active, load_x,
+                    worker, WT, hd, nb, active, load_x,
                     [&](const float *t, int nv, int off) {
                         if (off < 0) {
                             Y[base + column(off)] = from_f<T>((t[0] - m) - ls);
@@ -1053,7 +1203,7 @@ __global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
             }
         } else if constexpr (OP == OP_ROW_SUM) {
             float s = 0.f, c = 0.f;
-            stream_row<V, AL, U>(worker, W, hd, nb, active, load_x,
+            stream_row<V, AL, U>(worker, WT, hd, nb, active, load_x,
                                  [&](const float *t, int nv, int) {
 #pragma unroll
                                      for (int e = 0; e < V; ++e)
@@ -1064,10 +1214,12 @@ __global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
                                              c += err;
                                          }
                                  });
-            row_allreduce_compensated(s, c, W, red, parity);
+            team_allreduce_compensated(s, c, W, csize, red, parity, cpar);
             if (active && worker == 0) a.out[row] = s + c;
         }
     }
+    // Peers may still read this CTA's cluster slots.
+    if (csize > 1) cluster_sync();
 }
 
 // =========================================================================
@@ -1075,30 +1227,39 @@ __global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
 // =========================================================================
 using KernelFn = void (*)(KArgs);
 
-template <int OP, typename T, int V, bool AL>
+template <int OP, typename T, int V, bool AL, bool CL>
 __host__ KernelFn reg_kernel_for_chunks(int K) {
     switch (K) {
-        case 1: return reg_kernel<OP, T, V, 1, AL>;
-        case 2: return reg_kernel<OP, T, V, 2, AL>;
-        case 4: return reg_kernel<OP, T, V, 4, AL>;
-        case 8: return reg_kernel<OP, T, V, 8, AL>;
-        case 16: return reg_kernel<OP, T, V, 16, AL>;
+        case 1: return reg_kernel<OP, T, V, 1, AL, CL>;
+        case 2: return reg_kernel<OP, T, V, 2, AL, CL>;
+        case 4: return reg_kernel<OP, T, V, 4, AL, CL>;
+        case 8: return reg_kernel<OP, T, V, 8, AL, CL>;
+        case 16: return reg_kernel<OP, T, V, 16, AL, CL>;
         default: return nullptr;
     }
 }
 
 // A pack of one FP32 value needs no alignment head, so it has only the
-// aligned kernels.
-template <int OP, typename T, int V>
-__host__ KernelFn kernel_for(const mt_plan_t &p, bool aligned) {
+// aligned kernels.  Cluster (split-row) kernels exist for 16-byte packs.
+template <int OP, typename T, int V, bool CL>
+__host__ KernelFn kernel_for_cl(const mt_plan_t &p, bool aligned) {
     constexpr bool kOnlyAligned = (V == 1 && sizeof(T) == 4);
     if (p.path == MT_PATH_LOOP) {
-        if (kOnlyAligned || aligned) return loop_kernel<OP, T, V, true>;
-        return loop_kernel<OP, T, V, kOnlyAligned>;
+        if (kOnlyAligned || aligned) return loop_kernel<OP, T, V, true, CL>;
+        return loop_kernel<OP, T, V, kOnlyAligned, CL>;
     }
     if (kOnlyAligned || aligned)
-        return reg_kernel_for_chunks<OP, T, V, true>(p.chunks);
-    return reg_kernel_for_chunks<OP, T, V, kOnlyAligned>(p.chunks);
+        return reg_kernel_for_chunks<OP, T, V, true, CL>(p.chunks);
+    return reg_kernel_for_chunks<OP, T, V, kOnlyAligned, CL>(p.chunks);
+}
+
+template <int OP, typename T, int V>
+__host__ KernelFn kernel_for(const mt_plan_t &p, bool aligned) {
+    if constexpr (V * sizeof(T) == 16) {
+        if (p.cluster > 1) return kernel_for_cl<OP, T, V, true>(p, aligned);
+    }
+    if (p.cluster > 1) return nullptr;
+    return kernel_for_cl<OP, T, V, false>(p, aligned);
 }
 
 // Instantiated values per thread per chunk: FP32 V = 1, 2, 4 (4-, 8- and
@@ -1126,16 +1287,27 @@ __host__ cudaError_t launch_op(const mt_plan_t &p, const KArgs &a,
                                bool aligned, cudaStream_t stream) {
     KernelFn k = select_kernel<OP, T>(p, aligned);
     if (k == nullptr) return cudaErrorInvalidValue;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    if (a.pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (a.csize > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = (unsigned)a.csize;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.grid);
     cfg.blockDim = dim3((unsigned)(p.threads_per_row * p.rows_per_block));
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
-    cfg.attrs = a.pdl ? attr : nullptr;
-    cfg.numAttrs = a.pdl ? 1 : 0;
+    cfg.attrs = n ? attr : nullptr;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, k, a);
 }
 

@@ -100,14 +100,22 @@ mt_status plan_check(int op, int dtype, int64_t cols, const mt_plan_t &p) {
     if (p.grid < 0) return MT_ERR_INVALID_ARGUMENT;
     if (p.flags & ~(MT_PLAN_PDL | MT_PLAN_PREFETCH_NEXT))
         return MT_ERR_INVALID_ARGUMENT;
+    const int64_t C = p.cluster <= 1 ? 1 : p.cluster;
+    if (p.cluster < 0 || (C != 1 && C != 2 && C != 4 && C != 8))
+        return MT_ERR_INVALID_ARGUMENT;
+    // Split rows (clusters) are built for 16-byte packs only.
+    if (C > 1 && (B != 1 || W < 32 || p.grid % C != 0 ||
+                  V * dtype_size(dtype) != 16))
+        return MT_ERR_INVALID_ARGUMENT;
     const int64_t threads = W * B;
     if (threads % 32 != 0) return MT_ERR_INVALID_ARGUMENT;
     if (p.path == MT_PATH_REGISTERS) {
         if (!chunk_instantiated(p.chunks)) return MT_ERR_INVALID_ARGUMENT;
         if (threads > reg_max_threads((int)(V * p.chunks)))
             return MT_ERR_OUT_OF_RESOURCES;
-        // Every worker's private slots must hold its share of the row.
-        if (mt_private_slot_bound(cols, (int32_t)W, (int32_t)V) >
+        // Every worker's private slots must hold its share of the row; a
+        // cluster's CTAs together provide C*W workers.
+        if (mt_private_slot_bound(cols, (int32_t)(W * C), (int32_t)V) >
             V * p.chunks)
             return MT_ERR_OUT_OF_RESOURCES;
     } else if (p.path == MT_PATH_LOOP) {
@@ -181,12 +189,14 @@ size_t mt_describe_plan(const mt_plan_t *p, char *buf, size_t n) {
         const char *path = p->path == MT_PATH_REGISTERS ? "registers"
                            : p->path == MT_PATH_LOOP    ? "loop"
                                                         : "invalid";
+        char cl[32] = "";
+        if (p->cluster > 1) snprintf(cl, sizeof(cl), " cluster=%d", p->cluster);
         len = snprintf(tmp, sizeof(tmp),
                        "path=%s W=%d V=%d chunks=%d rows_per_block=%d "
-                       "threads=%d grid=%s%s%s",
+                       "threads=%d grid=%s%s%s%s",
                        path, p->threads_per_row, p->values_per_thread,
                        p->chunks, p->rows_per_block,
-                       p->threads_per_row * p->rows_per_block, grid,
+                       p->threads_per_row * p->rows_per_block, grid, cl,
                        (p->flags & MT_PLAN_PDL) ? " pdl" : "",
                        (p->flags & MT_PLAN_PREFETCH_NEXT) ? " prefetch_next"
                                                           : "");

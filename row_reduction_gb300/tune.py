@@ -187,9 +187,9 @@ def write_table(records, path):
         "// (row_reduction_gb300/tune.py) from timings on the GPU; do not "
         "edit by",
         "// hand.  Entry: {op, dtype, cols_min, cols_max, rows_min, rows_max,",
-        "// {W, V, chunks, rows_per_block, path, grid, flags}}.  The last "
-        "entry",
-        "// (op -1) only terminates the list.",
+        "// {W, V, chunks, rows_per_block, path, grid, flags, cluster}}.  The "
+        "last",
+        "// entry (op -1) only terminates the list.",
         "static const PlanEntry kPlanTable[] = {",
     ]
     by = {}
@@ -209,10 +209,11 @@ def write_table(records, path):
                 f"{lo}, {hi}, "
                 f"{{{w['threads_per_row']}, {w['values_per_thread']}, "
                 f"{w['chunks']}, {w['rows_per_block']}, {w['path']}, "
-                f"{w['grid']}, {w.get('flags', 0)}}}}},  "
+                f"{w['grid']}, {w.get('flags', 0)}, {w.get('cluster', 0)}"
+                f"}}}},  "
                 f"// {op} {dt} {r['rows']}x{cols}: "
                 f"{r['winner_us']:.3f} us")
-    lines.append("    {-1, 0, 0, 0, 0, 0, {0, 0, 0, 0, 0, 0, 0}},")
+    lines.append("    {-1, 0, 0, 0, 0, 0, {0, 0, 0, 0, 0, 0, 0, 0}},")
     lines.append("};")
     with open(path, "w") as f:
         f.write("\n".join(lines) + "\n")

@@ -250,3 +250,28 @@ def test_generic_and_half_entry_points_validate_before_launch():
     assert L.mt_cross_entropy_bf16(A, None, A, None, 4, 8, None) == INV
     assert L.mt_residual_layernorm_f16(A, None, None, None, A, None, 4, 8,
                                        1e-5, None) == INV
+
+
+def test_cluster_plan_legality():
+    ok = dict(W=256, V=4, chunks=4, rows_per_block=1)
+    def chk(cols, dtype="f32", **kw):
+        d = dict(ok, **kw)
+        p = mt.make_plan(d["W"], d["V"], d["chunks"], d["rows_per_block"],
+                         d.get("path", REG), d.get("grid", 0), 0,
+                         d.get("cluster", 0))
+        return mt.mt_plan_check_dtype(0, dtype, cols, p)
+    assert chk(16384, cluster=4) == OK          # 4 * 256 * 4 * 4 = 16384
+    assert chk(16384, cluster=2) == OOR         # half the row does not fit
+    assert chk(16384, cluster=3) == INV
+    assert chk(16384, cluster=16) == INV
+    assert chk(16384, cluster=-1) == INV
+    assert chk(16384, cluster=4, rows_per_block=2) == INV
+    assert chk(4096, cluster=2, W=16, chunks=16, rows_per_block=2) == INV
+    assert chk(16384, cluster=4, V=2, chunks=8) == INV   # not 16-byte packs
+    assert chk(16384, cluster=4, grid=6) == INV          # not a multiple
+    assert chk(16384, cluster=4, grid=8) == OK
+    assert chk(16384, "bf16", cluster=4, V=8, chunks=2) == OK
+    assert chk(16384, "bf16", cluster=4, V=4, chunks=4) == INV
+    assert chk(10 ** 6, cluster=8, chunks=0, path=LOOP) == OK
+    s = mt.mt_describe_plan(mt.make_plan(256, 4, 4, 1, cluster=4))
+    assert "cluster=4" in s

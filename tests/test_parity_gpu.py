@@ -497,3 +497,44 @@ def test_residual_rmsnorm_aliasing_and_zero_residual():
                              d["eps"])
     assert_close(y0.cpu().numpy(), oracle.rmsnorm(d["x"], d["weight"],
                                                   d["eps"]), "r = 0")
+
+
+# ------------------------------------------ split rows (thread-block clusters)
+def cluster_plans(cols, V=4):
+    plans = []
+    for C in (2, 4, 8):
+        for W in (32, 128, 512):
+            for K in (1, 2, 4, 8, 16):
+                p = mt.make_plan(W, V, K, 1, cluster=C,
+                                 flags=mt.MT_PLAN_PDL)
+                if mt.mt_plan_check(0, cols, p) == mt.MT_OK:
+                    plans.append(p)
+                    break
+            p = mt.make_plan(W, V, 0, 1, mt.MT_PATH_LOOP, cluster=C,
+                             flags=mt.MT_PLAN_PDL | mt.MT_PLAN_PREFETCH_NEXT)
+            if mt.mt_plan_check(0, cols, p) == mt.MT_OK:
+                plans.append(p)
+    return plans
+
+
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("shape", [(1, 65536), (3, 100003), (64, 4096),
+                                   (5, 33), (7, 4103)])
+def test_cluster_split_rows(op, shape):
+    """Rows split across a cluster of 2, 4 or 8 CTAs (partials exchanged
+    through distributed shared memory), against the oracle, with guards;
+    x is shifted by one element on the odd shapes (alignment heads)."""
+    rows, cols = shape
+    d = inputs.make(op, rows, cols, SEED + cols + 17)
+    ref = oracle.run(op, d)
+    offs = {"x": 1, "y": 1, "h_out": 1, "residual": 1} if cols % 4 else {}
+    plans = cluster_plans(cols)
+    assert plans
+    for p in plans:
+        got = run_guarded(op, d, rows, cols, plan=p, offsets=offs)
+        compare(op, got, ref, f"{op} {shape} {mt.mt_describe_plan(p)}")
+    # a grid smaller than the row count: clusters loop over rows
+    if rows > 2:
+        p = mt.make_plan(128, 4, 0, 1, mt.MT_PATH_LOOP, grid=4, cluster=2)
+        got = run_guarded(op, d, rows, cols, plan=p, offsets=offs)
+        compare(op, got, ref, f"{op} {shape} persistent clusters")

@@ -292,3 +292,15 @@ def test_cross_entropy_ignore_index_half(dt):
     ref_loss, ref_mean = oracle.cross_entropy_ignore(wide["x"], lab, -100)
     assert_close(loss.cpu().numpy(), ref_loss, "loss")
     assert_close(mean.cpu().numpy(), np.array([ref_mean]), "mean")
+
+
+@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("op", OPS)
+def test_cluster_split_rows_half(dt, op):
+    rows, cols = 3, 50003
+    st, wide = case(op, rows, cols, dt, SEED + 31)
+    for p in (mt.make_plan(512, 8, 4, 1, cluster=4),
+              mt.make_plan(256, 8, 0, 1, mt.MT_PATH_LOOP, cluster=8)):
+        assert mt.mt_plan_check_dtype(op, dt, cols, p) == mt.MT_OK
+        outs = run(op, st, dt, rows, cols, plan=p)
+        check(op, dt, outs, st, wide, f"{op} {dt} {mt.mt_describe_plan(p)}")
