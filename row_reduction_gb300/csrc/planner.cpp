@@ -1,10 +1,14 @@
 // planner.cpp -- launch-plan choice and legality (host only, no CUDA call).
 //
 // A plan fixes W (threads per row), V (consecutive values per thread per
-// chunk), the register chunk count K, the rows per CTA B, the path and the
-// grid.  The operators take the plan from a table of winners measured on the
-// GPU (plan_table.inc, written by the package's tuner), keyed by operator and
-// a (cols, rows) range; shapes outside the table fall back to a heuristic.
+// chunk), the register chunk count K, the rows per CTA B, the path, the
+// grid, launch flags and the cluster size.  The operators take the plan from
+// a table of winners measured on the GPU (plan_table.inc, written by the
+// package's tuner), keyed by operator, storage type and a (cols, rows)
+// range.  A shape outside the table takes the measured winner of the
+// nearest tuned shape -- nearest in log2(cols), then log2(rows) -- with its
+// chunk count (and if need be its width, or its path) re-fitted to the new
+// row length; the heuristic below is the last resort.
 //
 // The legality rules follow the fail-closed contract of the pages: a plan is
 // checked before dispatch and an illegal one is rejected, never remapped
@@ -14,6 +18,7 @@
 // overflow fail closed), and the private-slot bound is enforced before a plan
 // is used ("Consecutive-worker reduction layout checkpoint", §Implementation
 // and semantics).
+#include <math.h>
 #include <stdio.h>
 #include <string.h>
 
@@ -27,6 +32,7 @@ struct PlanEntry {
     int dtype;
     int64_t cols_min, cols_max;  // inclusive
     int64_t rows_min, rows_max;  // inclusive
+    int64_t rows_tuned;          // the row count the plan was measured at
     mt_plan_t plan;
 };
 
@@ -38,6 +44,13 @@ int64_t pow2_ceil(int64_t v) {
     int64_t p = 1;
     while (p < v) p <<= 1;
     return p;
+}
+
+// CTAs per row for a row count: rows are split across a cluster only while
+// there are too few rows to give each SM work (152 SMs: 8 CTAs per row up to
+// 19 rows, 4 up to 38, 2 up to 76).
+int64_t cluster_for(int64_t rows) {
+    return rows <= 19 ? 8 : rows <= 38 ? 4 : rows <= 76 ? 2 : 1;
 }
 
 bool chunk_instantiated(int k) {
@@ -53,41 +66,161 @@ bool v_instantiated(int dtype, int64_t V) {
     return V == 2 || V == 4 || V == 8;
 }
 
-// Heuristic plan for shapes the measured table does not cover: 16-byte
-// packs (V = 16 / element size), about `per_thread` values per thread,
-// blocks of about 256 threads; register path while one of the instantiated
-// chunk counts holds the row, else the loop path.
+// Heuristic plan for shapes far from every measured one.  It follows what
+// the measured winners have in common:
+//  * 16-byte packs (V = 16 / element size) unless the row is tiny;
+//  * short rows (<= 32 packs): a warp or less per row, several rows per CTA;
+//  * rows that fit in registers at about 16 values per thread (up to 64 KiB
+//    of FP32 data): one row per CTA of W = row/16 threads (at most 1024),
+//    two rows per CTA when that leaves fewer than 256 threads;
+//  * wider rows, many of them: the loop path with 256 threads per row and
+//    two rows per CTA, so several rows stream through each SM at once;
+//  * wider rows, fewer rows than SMs: a cluster of 8 CTAs per row.
+// All launches use the programmatic-dependent prologue, and persistent
+// CTAs prefetch their next row group.
 mt_plan_t heuristic_plan(int op, int dtype, int64_t rows, int64_t cols) {
     (void)op;
     mt_plan_t p;
     memset(&p, 0, sizeof(p));
-    const int vmax = 16 / dtype_size(dtype);
+    const int es = dtype_size(dtype);
+    const int vmax = 16 / es;
     const int vmin = dtype == DT_F32 ? 1 : 2;
-    p.values_per_thread = cols >= 16 ? vmax : vmin;
-    const int V = p.values_per_thread;
-    const int64_t per_thread = rows >= 2048 ? 16 : 8;
-    int64_t W = pow2_ceil((cols + per_thread - 1) / per_thread);
-    if (W < V) W = V;
-    if (W > 1024) W = 1024;
-    p.threads_per_row = (int)W;
-    int64_t K = pow2_ceil((cols + W * V - 1) / (W * V));
-    if (K <= 16 && W <= reg_max_threads((int)(V * K))) {
+    const int V = cols >= 4 * vmax ? vmax : vmin;
+    p.values_per_thread = V;
+    p.flags = MT_PLAN_PDL | MT_PLAN_PREFETCH_NEXT;
+    const int64_t packs = (cols + V - 1) / V;
+    if (packs <= 32) {
+        int64_t W = pow2_ceil(packs);
+        if (W < V) W = V;
+        if (W < 1) W = 1;
+        p.threads_per_row = (int)W;
+        p.chunks = 1;
+        p.rows_per_block = (int)(256 / W);
         p.path = MT_PATH_REGISTERS;
-        p.chunks = (int)K;
-    } else {
+        return p;
+    }
+    const int64_t reg_cap = 16384;  // FP32 values a row may keep in registers
+    if (cols <= reg_cap) {
+        int64_t W = pow2_ceil((packs + 3) / 4);  // about 4 packs per thread
+        if (W > 1024) W = 1024;
+        if (W < 32) W = 32;
+        int64_t K = pow2_ceil((cols + W * V - 1) / (W * V));
+        while (K > 16 || W > reg_max_threads((int)(V * K))) {
+            if (W >= 1024) break;
+            W *= 2;
+            K = pow2_ceil((cols + W * V - 1) / (W * V));
+        }
+        if (K <= 16 && W <= reg_max_threads((int)(V * K))) {
+            p.threads_per_row = (int)W;
+            p.chunks = (int)K;
+            p.rows_per_block = W >= 256 ? 1 : (int)(256 / W);
+            p.path = MT_PATH_REGISTERS;
+            return p;
+        }
+    }
+    const int64_t C = cluster_for(rows);
+    if (C > 1 && V * es == 16) {
+        // A cluster of C CTAs per row: registers while the row fits.
+        p.cluster = (int)C;
+        p.rows_per_block = 1;
+        for (int64_t W = 32; W <= 1024; W *= 2) {
+            for (int i = 0; i < kNumChunkSet; ++i) {
+                const int64_t K = kChunkSet[i];
+                if (K > 4 || C * W * V * K < cols ||
+                    W > reg_max_threads((int)(V * K)))
+                    continue;
+                p.threads_per_row = (int)W;
+                p.chunks = (int)K;
+                p.path = MT_PATH_REGISTERS;
+                return p;
+            }
+        }
         p.path = MT_PATH_LOOP;
         p.chunks = 0;
-        if (W > kLoopMaxThreads) p.threads_per_row = (int)(W = kLoopMaxThreads);
+        p.threads_per_row = 512;
+        return p;
     }
-    p.rows_per_block = W >= 256 ? 1 : (int)(256 / W);
-    p.grid = 0;
-    p.flags = MT_PLAN_PDL;
+    p.path = MT_PATH_LOOP;
+    p.chunks = 0;
+    // Two rows per CTA once there are enough rows for two CTAs per SM.
+    p.threads_per_row = rows >= 304 ? 256 : 512;
+    p.rows_per_block = rows >= 304 ? 2 : 1;
     return p;
 }
 
 }  // namespace
 
+namespace {
+double log2d(double v) { return log2(v < 1.0 ? 1.0 : v); }
+
+mt_status plan_check_impl(int op, int dtype, int64_t cols, const mt_plan_t &p);
+
+// Re-fits the measured plan of shape (rows_src, cols_src) to (rows, cols).
+// The source plan says how many threads the device wanted in flight
+// (rows_src * W * cluster) and how they were grouped (threads per CTA,
+// flags, V); the re-fit keeps those and recomputes the rest:
+//  * cluster: cluster_for(rows) for wide rows (>= 8192) of 16-byte packs;
+//  * W = the source's threads in flight / rows / cluster (a power of two),
+//    raised until the row fits in at most 8 chunks, capped at 1024;
+//  * chunks: the smallest instantiated count that holds the row, the loop
+//    path when none does;
+//  * rows per CTA: what keeps the source's CTA size.
+// Returns false when nothing legal is left.
+bool refit(int op, int dtype, int64_t rows_src, int64_t rows, int64_t cols,
+           mt_plan_t *p) {
+    const int64_t V = p->values_per_thread;
+    const int64_t cta = (int64_t)p->threads_per_row * p->rows_per_block;
+    const int64_t c_src = p->cluster > 1 ? p->cluster : 1;
+    // Split rows when there are few of them and they are wide.
+    const int64_t C = (V * dtype_size(dtype) == 16 && cols >= 8192)
+                          ? cluster_for(rows)
+                          : 1;
+    p->cluster = C > 1 ? (int32_t)C : 0;
+    p->grid = 0;
+    const double inflight = (double)(rows_src < 1 ? 1 : rows_src) *
+                            p->threads_per_row * c_src;
+    int64_t W = pow2_ceil((int64_t)(inflight / (double)(rows < 1 ? 1 : rows) /
+                                    (double)C / 1.414));
+    const int64_t wmin = C > 1 ? 32 : (V > 1 ? V : 1);
+    if (W < wmin) W = wmin;
+    while (W < 1024 && C * W * V * 8 < cols) W *= 2;
+    if (W > 1024) W = 1024;
+    if (p->path == MT_PATH_REGISTERS) {
+        int64_t K = 0;
+        for (int i = 0; i < kNumChunkSet; ++i)
+            if (C * W * V * kChunkSet[i] >= cols) {
+                K = kChunkSet[i];
+                break;
+            }
+        int64_t B = C > 1 ? 1 : (cta / W < 1 ? 1 : cta / W);
+        while (K > 0 && B > 1 && W * B > reg_max_threads((int)(V * K))) B /= 2;
+        if (K > 0 && (W * B) % 32 == 0 &&
+            W * B <= reg_max_threads((int)(V * K))) {
+            p->threads_per_row = (int32_t)W;
+            p->chunks = (int32_t)K;
+            p->rows_per_block = (int32_t)B;
+            if (plan_check_impl(op, dtype, cols, *p) == MT_OK) return true;
+        }
+        p->path = MT_PATH_LOOP;
+    }
+    p->chunks = 0;
+    if (W > kLoopMaxThreads) W = kLoopMaxThreads;
+    int64_t B = C > 1 ? 1 : (cta / W < 1 ? 1 : cta / W);
+    while (W * B > kLoopMaxThreads) B /= 2;
+    while ((W * B) % 32 != 0) B *= 2;
+    p->threads_per_row = (int32_t)W;
+    p->rows_per_block = (int32_t)(B < 1 ? 1 : B);
+    return plan_check_impl(op, dtype, cols, *p) == MT_OK;
+}
+
+}  // namespace
+
 mt_status plan_check(int op, int dtype, int64_t cols, const mt_plan_t &p) {
+    return plan_check_impl(op, dtype, cols, p);
+}
+
+namespace {
+mt_status plan_check_impl(int op, int dtype, int64_t cols, const mt_plan_t &p) {
     if (op < 0 || op >= OP_COUNT || cols < 1) return MT_ERR_INVALID_ARGUMENT;
     if (dtype < 0 || dtype >= DT_COUNT) return MT_ERR_INVALID_ARGUMENT;
     const int64_t W = p.threads_per_row, V = p.values_per_thread;
@@ -125,6 +258,7 @@ mt_status plan_check(int op, int dtype, int64_t cols, const mt_plan_t &p) {
     }
     return MT_OK;
 }
+}  // namespace
 
 mt_status plan_lookup(int op, int dtype, int64_t rows, int64_t cols,
                       mt_plan_t *out) {
@@ -137,6 +271,30 @@ mt_status plan_lookup(int op, int dtype, int64_t rows, int64_t cols,
             continue;
         if (plan_check(op, dtype, cols, e.plan) == MT_OK) {
             *out = e.plan;
+            return MT_OK;
+        }
+    }
+    // Nearest measured shape of the same operator and storage type.
+    const PlanEntry *best = nullptr;
+    double best_d = 0.0;
+    for (const PlanEntry &e : kPlanTable) {
+        if (e.op != op || e.dtype != dtype) continue;
+        const double d =
+            fabs(log2d((double)cols) - log2d((double)e.cols_min)) +
+            0.5 * fabs(log2d((double)rows) - log2d((double)e.rows_tuned));
+        if (best == nullptr || d < best_d) {
+            best = &e;
+            best_d = d;
+        }
+    }
+    // A measured plan transfers to rows within a factor 2 in length and 16
+    // in count; farther shapes take the heuristic.
+    if (best != nullptr &&
+        fabs(log2d((double)cols) - log2d((double)best->cols_min)) <= 2.0 &&
+        fabs(log2d((double)rows) - log2d((double)best->rows_tuned)) <= 4.0) {
+        mt_plan_t p = best->plan;
+        if (refit(op, dtype, best->rows_tuned, rows, cols, &p)) {
+            *out = p;
             return MT_OK;
         }
     }

@@ -71,6 +71,21 @@ def candidates(op, rows, cols, dtype="f32"):
                             out.append(B.make_plan(W, V, 0, Bk,
                                                    B.MT_PATH_LOOP, flags=fl))
             W *= 2
+    # Split rows (clusters of CTAs per row) when rows are too few to give
+    # every SM work: 16-byte packs, one row per CTA.
+    vmax = VALUES[dtype][0]
+    if rows < 304 and cols >= 1024:
+        for C in (2, 4, 8):
+            for W in (128, 256, 512, 1024):
+                K = next((k for k in CHUNKS if C * W * vmax * k >= cols),
+                         None)
+                for fl in FLAG_SETS:
+                    if K is not None:
+                        out.append(B.make_plan(W, vmax, K, 1, flags=fl,
+                                               cluster=C))
+                    if cols >= 8192:
+                        out.append(B.make_plan(W, vmax, 0, 1, B.MT_PATH_LOOP,
+                                               flags=fl, cluster=C))
     seen, legal = set(), []
     for p in out:
         key = tuple(p.as_dict().values())
@@ -165,6 +180,37 @@ def tune_shape(op, rows, cols, l2, rounds=5, log=print, dtype="f32"):
     return rec
 
 
+def evaluate(records, l2, rounds=7, log=print):
+    """Regret of the planner's own choice on tuned shapes: times the plan
+    mt_plan_query_dtype returns and compares it with each record's measured
+    winner.  Used on held-out shapes (records not in the table) to check
+    the fallback of the planner."""
+    import torch
+    out = []
+    for r in records:
+        dt = r.get("dtype", "f32")
+        outliers = r["op"] == "rmsnorm" and \
+            (r["rows"], r["cols"]) in inputs.RMSNORM_SWEEP
+        work = Workload(r["op"], r["rows"], r["cols"], inputs.TUNE_SEED,
+                        outliers=outliers, l2_bytes=l2,
+                        max_pool_bytes=8 << 30, dtype=dt)
+        p = B.mt_plan_query_dtype(r["op"], dt, r["rows"], r["cols"])
+        us = statistics.median(time_rounds(work, p, rounds=rounds,
+                                           min_round_s=0.01))
+        best = statistics.median(time_rounds(work, B.MtPlan(**r["winner"]),
+                                             rounds=rounds, min_round_s=0.01))
+        rec = {"op": r["op"], "dtype": dt, "rows": r["rows"],
+               "cols": r["cols"], "plan": B.mt_describe_plan(p),
+               "plan_us": us, "best_us": best, "regret": us / best - 1.0}
+        log(f"{r['op']} {dt} {r['rows']}x{r['cols']}: planner {us:.3f} us "
+            f"vs best {best:.3f} us (regret {100 * rec['regret']:.1f}%) "
+            f"[{rec['plan']}]")
+        out.append(rec)
+        del work
+        torch.cuda.empty_cache()
+    return out
+
+
 # ------------------------------------------------------------ the table
 def _rows_ranges(rows_list):
     """Splits [1, inf) between the tuned row counts at geometric
@@ -187,9 +233,8 @@ def write_table(records, path):
         "// (row_reduction_gb300/tune.py) from timings on the GPU; do not "
         "edit by",
         "// hand.  Entry: {op, dtype, cols_min, cols_max, rows_min, rows_max,",
-        "// {W, V, chunks, rows_per_block, path, grid, flags, cluster}}.  The "
-        "last",
-        "// entry (op -1) only terminates the list.",
+        "// rows tuned, {W, V, chunks, rows_per_block, path, grid, flags,",
+        "// cluster}}.  The last entry (op -1) only terminates the list.",
         "static const PlanEntry kPlanTable[] = {",
     ]
     by = {}
@@ -206,14 +251,14 @@ def write_table(records, path):
             w = r["winner"]
             lines.append(
                 f"    {{{B.OP_IDS[op]}, {B.DTYPE_IDS[dt]}, {cols}, {cols}, "
-                f"{lo}, {hi}, "
+                f"{lo}, {hi}, {r['rows']}, "
                 f"{{{w['threads_per_row']}, {w['values_per_thread']}, "
                 f"{w['chunks']}, {w['rows_per_block']}, {w['path']}, "
                 f"{w['grid']}, {w.get('flags', 0)}, {w.get('cluster', 0)}"
                 f"}}}},  "
                 f"// {op} {dt} {r['rows']}x{cols}: "
                 f"{r['winner_us']:.3f} us")
-    lines.append("    {-1, 0, 0, 0, 0, 0, {0, 0, 0, 0, 0, 0, 0, 0}},")
+    lines.append("    {-1, 0, 0, 0, 0, 0, 0, {0, 0, 0, 0, 0, 0, 0, 0}},")
     lines.append("};")
     with open(path, "w") as f:
         f.write("\n".join(lines) + "\n")
@@ -242,10 +287,22 @@ def main(argv=None):
     ap.add_argument("--rounds", type=int, default=5)
     ap.add_argument("--dtypes", default="f32",
                     help="storage types, e.g. f32,bf16,f16")
+    ap.add_argument("--evaluate", default=None,
+                    help="tuning records (JSON) to measure the planner's "
+                         "regret on, instead of tuning")
     args = ap.parse_args(argv)
     import torch
     from . import build
     build.build()
+    if args.evaluate:
+        props = torch.cuda.get_device_properties(0)
+        l2 = int(getattr(props, "L2_cache_size", 126 << 20)) or (126 << 20)
+        recs = json.load(open(args.evaluate))["records"]
+        res = evaluate(recs, l2, log=lambda s: print(s, flush=True))
+        with open(args.json, "w") as f:
+            json.dump({"device": torch.cuda.get_device_name(0),
+                       "evaluation": res}, f, indent=1)
+        return 0
     ops = [o for o in args.ops.split(",") if o]
     if args.shapes == "published":
         shapes = published_shapes(ops)
