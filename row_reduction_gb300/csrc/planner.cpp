@@ -287,7 +287,7 @@ mt_status plan_lookup(int op, int dtype, int64_t rows, int64_t cols,
             best_d = d;
         }
     }
-    // A measured plan transfers to rows within a factor 2 in length and 16
+    // A measured plan transfers to rows within a factor 4 in length and 16
     // in count; farther shapes take the heuristic.
     if (best != nullptr &&
         fabs(log2d((double)cols) - log2d((double)best->cols_min)) <= 2.0 &&
