@@ -47,6 +47,23 @@ from row_reduction_gb300.timing import (  # noqa: E402
 METRIC = ("RMSNorm FP32 µs/op and HBM GB/s (% of GB300 peak), "
           "1×127 … 1024×4096")
 FALLBACK_HBM_GBS = 6800.0
+H_OUT_OPS = ("residual_layernorm", "residual_rmsnorm")
+_OUTL = "with 1% x100 outliers"
+INPUT_RECIPE = {
+    "rmsnorm": f"x~N(0,1) {_OUTL}, weight~1+0.1N(0,1), eps=1e-6",
+    "residual_rmsnorm": f"x~N(0,1) {_OUTL}, residual~N(0,1), "
+                        "weight~1+0.1N(0,1), eps=1e-6, h_out written",
+    "layernorm": f"x~N(0,1) {_OUTL}, gamma~1+0.1N(0,1), beta~0.1N(0,1), "
+                 "eps=1e-5",
+    "residual_layernorm": f"x~N(0,1) {_OUTL}, residual~N(0,1), "
+                          "gamma~1+0.1N(0,1), beta~0.1N(0,1), eps=1e-5, "
+                          "h_out written",
+    "softmax": f"x~N(0,4) {_OUTL}",
+    "log_softmax": f"x~N(0,4) {_OUTL}",
+    "row_sum": f"x~N(0,1) {_OUTL}",
+    "cross_entropy": f"logits~N(0,4) {_OUTL}, labels uniform in [0, cols), "
+                     "per-row loss and mean",
+}
 
 
 # ---------------------------------------------------------------- helpers
@@ -79,20 +96,21 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_sources_sha(op="rmsnorm", plan=None):
+def kernel_sources_sha(op="rmsnorm", plan=None, dtype="f32"):
     """Hash of what defines one operator's kernel: the kernel templates, the
-    launch code, that operator's translation unit and its plan."""
+    launch code, that operator's translation unit for the storage type and
+    its plan."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "row_reduction_gb300", "csrc")
     for name in ("mt_kernels.cuh", "mt_internal.h", "api.cpp",
-                 f"ops_{op}_f32.cu"):
+                 f"ops_{op}_{dtype}.cu"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + b"\0" + f.read())
     h.update((plan or "").encode())
     return h.hexdigest()
 
 
-def profiled_traffic(workload_key, op, plan):
+def profiled_traffic(workload_key, op, plan, dtype="f32"):
     """DRAM bytes per launch from the committed ncu summary of this
     workload, if it was taken on the current kernel code and plan."""
     path = os.path.join(ROOT, "profiles", f"{workload_key}.ncu.txt")
@@ -103,7 +121,8 @@ def profiled_traffic(workload_key, op, plan):
         if ":" in line:
             k, v = line.split(":", 1)
             fields[k.strip()] = v.strip()
-    if fields.get("kernel_sources_sha256") != kernel_sources_sha(op, plan):
+    if fields.get("kernel_sources_sha256") != kernel_sources_sha(op, plan,
+                                                                 dtype):
         return None
     try:
         return int(fields["dram_bytes_per_launch"])
@@ -169,11 +188,14 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sms)}
 
 
-def cpu_baseline(op, d, rows, cols, budget_s=10.0):
-    """The CPU oracle as it stands, single-threaded, on the same inputs,
-    repeated for about `budget_s` seconds."""
+def cpu_baseline(op, d, rows, cols, budget_s=10.0, dtype="f32"):
+    """The CPU oracle as it stands, single-threaded, on the same inputs
+    (`d` in `dtype` storage, handed to the oracle as their exact FP32
+    values), repeated for about `budget_s` seconds."""
     import oracle
+    from row_reduction_gb300 import inputs
     oracle.build()
+    d = inputs.widen_all(d, dtype)
     reps, t0 = 0, time.perf_counter()
     while True:
         oracle.run(op, d)
@@ -181,11 +203,11 @@ def cpu_baseline(op, d, rows, cols, budget_s=10.0):
         el = time.perf_counter() - t0
         if el >= budget_s or (reps >= 1 and el * (reps + 1) / reps > 3 * budget_s):
             break
-    b = algorithmic_bytes(op, rows, cols, op == "residual_layernorm",
-                          op == "cross_entropy")
+    b = algorithmic_bytes(op, rows, cols, op in H_OUT_OPS,
+                          op == "cross_entropy", dtype)
     return {"value": b * reps / el / 1e9, "unit": "GB/s", "cores": 1,
             "kind": "oracle",
-            "sample": f"{op} {rows}x{cols} (the full workload) x {reps} "
+            "sample": f"{op} {dtype} {rows}x{cols} (the full workload) x {reps} "
                       f"repetitions, {el:.1f} s, one thread",
             "us_per_op": el / reps * 1e6}
 
@@ -198,7 +220,10 @@ def run_reference(args, rank, world):
     from row_reduction_gb300 import inputs
     oracle.build()
     rows, cols = args.rows, args.cols
-    d = inputs.make(args.op, rows, cols, inputs.TUNE_SEED, outliers=True)
+    d = inputs.widen_all(
+        inputs.as_storage(inputs.make(args.op, rows, cols, inputs.TUNE_SEED,
+                                      outliers=True), args.dtype),
+        args.dtype)
     # Size the per-step row sample so the whole run stays near 60 s.
     def rows_of(n):
         return {k: (v[:n] if isinstance(v, np.ndarray) and
@@ -216,7 +241,8 @@ def run_reference(args, rank, world):
     for _ in range(args.steps):
         oracle.run(args.op, sub)
     el = time.perf_counter() - t0
-    b = algorithmic_bytes(args.op, sample_rows, cols)
+    b = algorithmic_bytes(args.op, sample_rows, cols, args.op in H_OUT_OPS,
+                          args.op == "cross_entropy", args.dtype)
     value = b * args.steps / el / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
@@ -224,7 +250,8 @@ def run_reference(args, rank, world):
         "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": f"{args.op}_f32 {rows}x{cols}", "op": args.op,
+        "config": {"workload": f"{args.op}_{args.dtype} {rows}x{cols}",
+                   "op": args.op, "storage": args.dtype,
                    "rows": rows, "cols": cols,
                    "sample_rows_per_step": sample_rows},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1,
@@ -252,7 +279,7 @@ def run_ours(args, rank, world, local_rank):
     barrier = (lambda: dist.barrier()) if world > 1 else None
 
     work = Workload(args.op, args.rows, args.cols, inputs.TUNE_SEED,
-                    outliers=True, l2_bytes=l2)
+                    outliers=True, l2_bytes=l2, dtype=args.dtype)
     sampler = ClockSampler(local_rank)
     elapsed = time_graph_steps(work, args.steps, args.warmup,
                                barrier=barrier, sampler=sampler)
@@ -264,12 +291,12 @@ def run_ours(args, rank, world, local_rank):
         return 0
 
     peak, peak_kind = measured_peak()
-    key = f"{args.op}_f32_{args.rows}x{args.cols}"
+    key = f"{args.op}_{args.dtype}_{args.rows}x{args.cols}"
+    plan = plan_text(args.op, args.rows, args.cols, args.dtype)
     achieved = work.bytes / per_step / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak,
                 "unit": "GB/s", "frac": achieved / peak,
-                "traffic": profiled_traffic(
-                    key, args.op, plan_text(args.op, args.rows, args.cols)),
+                "traffic": profiled_traffic(key, args.op, plan, args.dtype),
                 "peak_source": f"{peak_kind} HBM copy bandwidth "
                                "(MEASURED_PEAKS.json hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s"}
@@ -290,11 +317,10 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
         "config": {
-            "workload": f"{args.op}_f32 rows={args.rows} cols={args.cols}, "
-                        "x~N(0,1) with 1% x100 outliers, "
-                        "weight~1+0.1N(0,1), eps=1e-6",
-            "op": args.op, "rows": args.rows, "cols": args.cols,
-            "plan": plan_text(args.op, args.rows, args.cols),
+            "workload": f"{args.op}_{args.dtype} rows={args.rows} "
+                        f"cols={args.cols}, {INPUT_RECIPE[args.op]}",
+            "op": args.op, "storage": args.dtype, "rows": args.rows,
+            "cols": args.cols, "plan": plan,
             "l2": f"inputs larger than L2: rotating pool of "
                   f"{len(work.sets)} buffer sets, "
                   f"{work.pool_bytes / 2**20:.0f} MiB >= 4x L2 "
@@ -314,7 +340,8 @@ def run_ours(args, rank, world, local_rank):
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.op, work.host, args.rows,
-                                            args.cols, args.cpu_seconds)
+                                            args.cols, args.cpu_seconds,
+                                            args.dtype)
     if world == 1 and not args.no_sweep:
         line["sweep"] = run_sweep(l2, peak)
     print(json.dumps(line))
@@ -366,6 +393,9 @@ def main():
     ap.add_argument("--op", default="rmsnorm")
     ap.add_argument("--rows", type=int, default=1024)
     ap.add_argument("--cols", type=int, default=4096)
+    ap.add_argument("--dtype", choices=["f32", "f16", "bf16"], default="f32",
+                    help="storage type of matrices and parameter vectors "
+                         "(arithmetic is FP32 for all)")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
