@@ -281,38 +281,58 @@ def time_plain_steps(work, steps, warmup):
     return start.elapsed_time(end) / 1e3
 
 
-def time_e2e(work, steps, warmup):
-    """Each step copies x from pinned host memory, calls the library and
-    copies the result back to pinned host memory.  Returns (seconds,
-    host-to-device bytes per step, device-to-host bytes per step)."""
+def _e2e_host_buffers(work):
     import torch
-    s0 = work.sets[0]
     hx = work.host["x"]
     x_host = (torch.from_numpy(hx.view("int16")).view(torch.bfloat16)
               if work.dtype == "bf16" else torch.from_numpy(hx)).pin_memory()
     out_key = {"row_sum": "out", "cross_entropy": "loss"}.get(work.op, "y")
-    out_host = torch.empty(s0[out_key].shape, dtype=s0[out_key].dtype,
-                           pin_memory=True)
-    stream = torch.cuda.Stream()
-    fn = work.call_fn(0, stream.cuda_stream)
+    return x_host, out_key
 
-    def step():
-        s0["x"].copy_(x_host, non_blocking=True)
-        fn()
-        out_host.copy_(s0[out_key], non_blocking=True)
 
-    with torch.cuda.stream(stream):
-        for _ in range(warmup):
-            step()
-    stream.synchronize()
+def time_e2e(work, steps, warmup, depth=1):
+    """Each step copies x from pinned host memory, calls the library and
+    copies the result back to pinned host memory.  Returns (seconds,
+    host-to-device bytes per step, device-to-host bytes per step).
+
+    depth = 1 runs the steps one after another on one stream.  depth = 2
+    alternates two device buffer sets, two pinned result buffers and two
+    streams, so one step's upload overlaps the previous step's kernel and
+    download (the two copy directions use separate copy engines); each step
+    still moves its own input and result inside the timed region."""
+    import torch
+    depth = max(1, min(depth, len(work.sets)))
+    x_host, out_key = _e2e_host_buffers(work)
+    s0 = work.sets[0]
+    outs = [torch.empty(s0[out_key].shape, dtype=s0[out_key].dtype,
+                        pin_memory=True) for _ in range(depth)]
+    streams = [torch.cuda.Stream() for _ in range(depth)]
+    fns = [work.call_fn(b, streams[b].cuda_stream) for b in range(depth)]
+
+    def step(k):
+        b = k % depth
+        s = work.sets[b]
+        with torch.cuda.stream(streams[b]):
+            s["x"].copy_(x_host, non_blocking=True)
+            fns[b]()
+            outs[b].copy_(s[out_key], non_blocking=True)
+
+    for k in range(max(warmup, depth)):
+        step(k)
+    torch.cuda.synchronize()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        start.record(stream)
-        for _ in range(steps):
-            step()
-        end.record(stream)
+    done = [torch.cuda.Event() for _ in range(depth)]
+    start.record(streams[0])
+    for st in streams[1:]:
+        st.wait_event(start)
+    for k in range(steps):
+        step(k)
+    for b in range(1, depth):
+        done[b].record(streams[b])
+        streams[0].wait_event(done[b])
+    end.record(streams[0])
     end.synchronize()
     return (start.elapsed_time(end) / 1e3,
             x_host.numel() * x_host.element_size(),
-            out_host.numel() * out_host.element_size())
+            outs[0].numel() * outs[0].element_size())

@@ -97,6 +97,25 @@ def candidates(op, rows, cols, dtype="f32"):
     return legal
 
 
+def grid_variants(rows, plans, sms):
+    """Second-stage candidates: the given plans again with persistent grids
+    of one to three CTAs per SM (fewer CTAs than row groups, so each loops
+    over several), with and without the next-group prefetch."""
+    flag_sets = (B.MT_PLAN_PDL, B.MT_PLAN_PDL | B.MT_PLAN_PREFETCH_NEXT)
+    out = []
+    for p in plans:
+        d = p.as_dict()
+        C = max(1, d.get("cluster", 0))
+        ngroups = -(-rows // d["rows_per_block"])
+        for mult in (1, 2, 3):
+            G = sms * mult
+            if G % C or G // C >= ngroups:
+                continue
+            for fl in flag_sets:
+                out.append(B.MtPlan(**dict(d, grid=G, flags=fl)))
+    return out
+
+
 def _outputs(work, plan):
     import torch
     stream = torch.cuda.current_stream()
@@ -132,21 +151,38 @@ def tune_shape(op, rows, cols, l2, rounds=5, log=print, dtype="f32"):
     cands = candidates(op, rows, cols, dtype)
     timed = []
     rejected = 0
-    for p in cands:
-        try:
-            got = _outputs(work, p)
-        except B.MTError as e:
-            log(f"  reject {B.mt_describe_plan(p)}: {e}")
-            rejected += 1
-            continue
-        if not _agrees(got, ref, dtype):
-            log(f"  reject {B.mt_describe_plan(p)}: output differs")
-            rejected += 1
-            continue
-        us = statistics.median(time_rounds(work, p, rounds=rounds,
-                                           min_round_s=0.004))
-        timed.append((us, p))
-    timed.sort(key=lambda t: t[0])
+    seen = set()
+
+    def run_stage(plans):
+        nonlocal rejected
+        for p in plans:
+            key = tuple(p.as_dict().values())
+            if key in seen:
+                continue
+            seen.add(key)
+            try:
+                got = _outputs(work, p)
+            except B.MTError as e:
+                log(f"  reject {B.mt_describe_plan(p)}: {e}")
+                rejected += 1
+                continue
+            if not _agrees(got, ref, dtype):
+                log(f"  reject {B.mt_describe_plan(p)}: output differs")
+                rejected += 1
+                continue
+            us = statistics.median(time_rounds(work, p, rounds=rounds,
+                                               min_round_s=0.004))
+            timed.append((us, p))
+        timed.sort(key=lambda t: t[0])
+
+    run_stage(cands)
+    # Second stage: persistent grids and prefetch depth for the best plans.
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    stage2 = grid_variants(rows, [p for _, p in timed[:4]], sms)
+    stage2 = [p for p in stage2 if B.mt_plan_check_dtype(
+        B.OP_IDS[op], dtype, cols, p) == B.MT_OK]
+    run_stage(stage2)
+    cands = cands + stage2
     # Re-measure the three fastest (and the default) with more rounds.
     finals = []
     for us, p in timed[:3]:

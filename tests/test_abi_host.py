@@ -173,6 +173,18 @@ def test_plan_query_errors_and_describe():
     assert mt.status_string(99) == "MT_ERR_UNKNOWN"
 
 
+def test_plan_flags():
+    both = mt.MT_PLAN_PDL | mt.MT_PLAN_PREFETCH_NEXT
+    for fl in range(both + 1):
+        p = mt.make_plan(128, 4, 8, 2, grid=152, flags=fl)
+        assert mt.mt_plan_check(0, 4096, p) == OK
+    for fl in (4, 8, -1, both | 4):
+        p = mt.make_plan(128, 4, 8, 2, flags=fl)
+        assert mt.mt_plan_check(0, 4096, p) == INV
+    s = mt.mt_describe_plan(mt.make_plan(128, 4, 8, 2, grid=152, flags=both))
+    assert s.endswith("grid=152 pdl prefetch_next")
+
+
 # ------------------------------------------------------ argument validation
 # These return before any CUDA call, so they run without a GPU.  Addresses
 # are arbitrary 16-byte aligned integers that are never dereferenced.

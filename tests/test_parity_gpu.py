@@ -371,6 +371,52 @@ def test_forced_plan_errors_on_gpu():
         assert torch.allclose(y, torch.ones_like(y), rtol=1e-5)
 
 
+# ------------------------------- persistent grids with L2 prefetches
+PDL_NEXT = mt.MT_PLAN_PDL | mt.MT_PLAN_PREFETCH_NEXT
+
+
+@pytest.mark.parametrize("op", OPS)
+def test_persistent_grids_with_prefetch(op):
+    """Grids smaller than the row-group count (CTAs loop over row groups),
+    with the first row group prefetched into L2 before the wait on the
+    previous kernel and the next one prefetched during the current one,
+    against the oracle, with guards; the second shape is unaligned and
+    ragged."""
+    for rows, cols, K, offs in ((1000, 4096, 8, {}),
+                                (517, 1000, 2, {"x": 1, "y": 1, "h_out": 1,
+                                                "residual": 1})):
+        d = inputs.make(op, rows, cols, SEED + rows)
+        ref = oracle.run(op, d)
+        for grid in (7, 152, 304):
+            for fl in (mt.MT_PLAN_PDL, PDL_NEXT):
+                p = mt.make_plan(128, 4, K, 2, grid=grid, flags=fl)
+                got = run_guarded(op, d, rows, cols, plan=p, offsets=offs)
+                compare(op, got, ref,
+                        f"{op} {rows}x{cols} {mt.mt_describe_plan(p)}")
+
+
+def test_prefetched_call_reads_the_previous_kernels_output():
+    """A call whose input the previous call on the stream writes: the L2
+    prefetch issued before the wait must not let it read the old contents
+    (here NaN)."""
+    rows, cols = 4096, 4096
+    x = torch.randn(rows, cols, device="cuda")
+    w = torch.ones(cols, device="cuda")
+    z = torch.empty_like(x)
+    s = torch.empty(rows, device="cuda")
+    pa = mt.make_plan(128, 4, 8, 2, grid=152, flags=PDL_NEXT)
+    for _ in range(3):
+        z.fill_(float("nan"))
+        mt.softmax(x, out=z, plan=pa)
+        mt.row_sum(z, out=s, plan=pa)
+        mt.rmsnorm(z, w, eps=0.0, out=z, plan=pa)
+        torch.cuda.synchronize()
+        assert torch.allclose(s, torch.ones_like(s), atol=1e-5)
+        assert bool(torch.isfinite(z).all())
+        ms = (z.double() ** 2).mean(dim=1)
+        assert torch.allclose(ms, torch.ones_like(ms), atol=1e-3)
+
+
 # ------------------------------------------- cross-entropy mean paths
 def _ce_case(rows, cols, seed):
     d = inputs.make("cross_entropy", rows, cols, seed)
