@@ -1,7 +1,9 @@
 /*
- * mt_rowreduce.h -- C ABI of a GB300 (sm_103a) library of per-row FP32
- * reductions: RMSNorm, LayerNorm, residual LayerNorm, softmax, row sum and
- * cross-entropy.
+ * mt_rowreduce.h -- C ABI of a GB300 (sm_103a) library of per-row
+ * reductions with FP32 arithmetic: RMSNorm, LayerNorm, residual LayerNorm,
+ * softmax, row sum and cross-entropy, plus the fused residual RMSNorm,
+ * log-softmax and cross-entropy with an ignore index; FP32, FP16 or BF16
+ * storage.
  *
  * Operator family: "Consecutive-worker reduction layout checkpoint",
  * §Evidence and what remains (generic V=4 operator coverage: sum, softmax,
@@ -14,27 +16,30 @@
  *
  * Conventions shared by every call below
  * -------------------------------------
- * Layout     every matrix is rows x cols, FP32, contiguous row-major (row r
- *            starts at element r*cols); vectors (weight, gamma, beta) hold
- *            cols FP32 values; per-row outputs hold rows FP32 values; labels
- *            hold rows int32 values.
+ * Layout     every matrix is rows x cols in the call's storage type (FP32
+ *            for the *_f32 calls, FP16 for *_f16, BF16 for *_bf16),
+ *            contiguous row-major (row r starts at element r*cols); vectors
+ *            (weight, gamma, beta) hold cols values of the same type;
+ *            per-row outputs (row sums, losses, the mean) hold FP32 values;
+ *            labels hold rows int32 values.
  * Memory     every data pointer is a DEVICE pointer owned by the caller and
  *            must be aligned to its element size (4 bytes for FP32, labels
- *            and per-row outputs; 2 bytes for FP16/BF16).  Calls allocate no device
- *            memory and never synchronise the host; work is enqueued on
- *            `stream` (NULL = the legacy default stream) on the current
- *            device, and device-side faults surface at the caller's next
- *            synchronisation.  16-byte aligned pointers and cols a multiple
- *            of V get the fully vectorised path; other alignments are
- *            handled by a per-row scalar head before the vector body.
+ *            and per-row outputs; 2 bytes for FP16/BF16).  Calls allocate
+ *            no device memory and never synchronise the host; work is
+ *            enqueued on `stream` (NULL = the legacy default stream) on the
+ *            current device, and device-side faults surface at the
+ *            caller's next synchronisation.  16-byte aligned pointers and
+ *            cols a multiple of V get the fully vectorised path; other
+ *            alignments are handled by a per-row scalar head before the
+ *            vector body.
  * Aliasing   y == x (in place) is allowed; so are h_out == x and
  *            h_out == residual.  Any other (partial) overlap between an
  *            output and an input is undefined.
  * Errors     arguments are checked before anything is enqueued: a NULL
  *            required pointer (rows > 0), a pointer not aligned to its
- *            element size,
- *            rows < 0, cols < 1, cols > INT32_MAX or rows*cols overflowing
- *            int64 give MT_ERR_INVALID_ARGUMENT and enqueue nothing.
+ *            element size, a pointer the operator does not take, rows < 0,
+ *            cols < 1, cols > INT32_MAX or rows*cols overflowing int64 give
+ *            MT_ERR_INVALID_ARGUMENT and enqueue nothing.
  *            rows == 0 returns MT_OK without a launch (outputs untouched).
  *            A failed launch gives MT_ERR_CUDA (mt_last_cuda_error() has the
  *            cudaError_t value).  A forced plan that is malformed gives
@@ -349,9 +354,12 @@ MT_API mt_status mt_row_reduce_with_plan(
 /* ---- planning and introspection (host only; no CUDA call) ------------- */
 
 /* The plan the operators use for (op, rows, cols): a lookup in the table of
- * measured winners, else the built-in heuristic.  grid is left 0 (resolved
- * at launch from the device's SM count and occupancy).  Returns
- * MT_ERR_INVALID_ARGUMENT for an unknown op, rows < 0 or cols < 1. */
+ * measured winners, else the nearest measured shape re-fitted, else the
+ * built-in heuristic.  grid is 0 (resolved at launch from the device's SM
+ * count and occupancy) unless the measured winner had an explicit
+ * persistent grid (a multiple of the SM count it was measured on).
+ * Returns MT_ERR_INVALID_ARGUMENT for an unknown op, rows < 0 or
+ * cols < 1. */
 MT_API mt_status mt_plan_query(int op, int64_t rows, int64_t cols, mt_plan_t *out);
 
 /* Legality of a plan for (op, cols) without launching anything: MT_OK, or

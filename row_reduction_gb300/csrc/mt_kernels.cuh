@@ -56,9 +56,22 @@ namespace mt {
 
 constexpr unsigned kFull = 0xffffffffu;
 
-// NaN-propagating max (fmaxf would drop a NaN).
+// NaN-propagating max: PTX max with the .NaN modifier returns NaN when
+// either operand is NaN (fmaxf would drop it).  One instruction.
 __device__ __forceinline__ float nanmax(float a, float b) {
-    return (a > b || a != a) ? a : b;
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+// NaN-propagating max over the 32 lanes of a warp, returned to every lane:
+// one warp-wide reduction instruction (redux.sync on FP32, sm_100 family).
+__device__ __forceinline__ float warp_nanmax(float v) {
+    float r;
+    asm volatile("redux.sync.max.NaN.f32 %0, %1, %2;"
+                 : "=f"(r)
+                 : "f"(v), "r"(kFull));
+    return r;
 }
 
 // Error-free transformation of a + b (Knuth's two-sum): s + err == a + b
@@ -71,14 +84,18 @@ __device__ __forceinline__ void two_sum(float a, float b, float &s,
     err = __fadd_rn(__fsub_rn(a, ap), __fsub_rn(b, bp));
 }
 
-// e^d for d = x - max(row) <= 0, as 2^(d * log2(e)) with CUDA's exp2f.  The
-// difference d is formed first (exact when x is near the max), so the only
-// extra error is the rounding of the product: a relative error of at most
-// |d| * 2^-24 in the result.  A term's weight e^d makes its absolute error
-// at most max(e^d |d|) 2^-24 = 2^-24 / e, far below the FP32 tolerance of
-// every output that sums or normalises these terms.
+// e^d for d = x - max(row) <= 0, as 2^(d * log2(e)) with the PTX base-2
+// exponential instruction ex2.approx.ftz.f32 (one MUFU operation; results
+// below 2^-126 flush to zero, 2^-inf = 0, NaN stays NaN).  The difference d
+// is formed first (exact when x is near the max), so the product adds a
+// relative error of at most |d| * 2^-24, whose absolute effect on a term of
+// weight e^d is at most 2^-24 / e; the instruction itself is an
+// approximation within a few units in the last place.  Both are far below
+// the FP32 tolerance of every output that sums or normalises these terms.
 __device__ __forceinline__ float exp_shifted(float d) {
-    return exp2f(d * 1.4426950408889634f);
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(d * 1.4426950408889634f));
+    return r;
 }
 
 // Operators that add a residual to x before normalising.
@@ -245,12 +262,15 @@ __device__ __forceinline__ float param_at(const T *p, int col, float dflt) {
 
 // ---- cooperative reductions ---------------------------------------------
 struct SumOp {
+    static constexpr bool kWarpRedux = false;
     __device__ __forceinline__ float operator()(float a, float b) const {
         return a + b;
     }
     static __device__ __forceinline__ float ident() { return 0.f; }
 };
 struct MaxOp {
+    // A full warp reduces with one redux.sync instead of a butterfly.
+    static constexpr bool kWarpRedux = true;
     __device__ __forceinline__ float operator()(float a, float b) const {
         return nanmax(a, b);
     }
@@ -269,14 +289,19 @@ __device__ __forceinline__ float row_allreduce(float v, int W,
                                                RedScratch &red,
                                                int &parity) {
     Op op;
-    if (W <= 32) {
+    if (W < 32 || (W == 32 && !Op::kWarpRedux)) {
         for (int off = W >> 1; off > 0; off >>= 1)
             v = op(v, __shfl_xor_sync(kFull, v, off));
         return v;
     }
+    if constexpr (Op::kWarpRedux) {
+        v = warp_nanmax(v);
+    } else {
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-        v = op(v, __shfl_xor_sync(kFull, v, off));
+        for (int off = 16; off > 0; off >>= 1)
+            v = op(v, __shfl_xor_sync(kFull, v, off));
+    }
+    if (W == 32) return v;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int nw = W >> 5;
@@ -286,6 +311,7 @@ __device__ __forceinline__ float row_allreduce(float v, int W,
     __syncthreads();
     const int first = warp & ~(nw - 1);
     float t = lane < nw ? buf[first + lane] : Op::ident();
+    if constexpr (Op::kWarpRedux) return warp_nanmax(t);
     for (int off = nw >> 1; off > 0; off >>= 1)
         t = op(t, __shfl_xor_sync(kFull, t, off));
     return __shfl_sync(kFull, t, 0);
