@@ -14,10 +14,12 @@ __global__ void __launch_bounds__(1024)
     mean_kernel(const float *loss, float *mean, int64_t rows,
                 const int32_t *labels, int32_t ignore_index,
                 int32_t has_ignore) {
-    // Launched as a programmatic dependent of the loss kernel: wait until
-    // that grid has completed and its losses are visible.
-    grid_wait_prerequisites();
+    // Launched as a programmatic dependent of the loss kernel.  Let the next
+    // kernel on the stream launch now (it waits for this grid to complete
+    // before it touches memory), then wait until the loss grid has
+    // completed and its losses are visible.
     grid_launch_dependents();
+    grid_wait_prerequisites();
     __shared__ RedScratch red;
     int parity = 0;
     __shared__ long long ignored_part[32];
@@ -31,17 +33,21 @@ __global__ void __launch_bounds__(1024)
         if (has_ignore && labels[i] == ignore_index) ++ignored;
     }
     row_allreduce_compensated(s, c, (int)blockDim.x, red, parity);
-    // Exact count of ignored rows: warp sums, then warp 0 adds the warps'.
-    for (int off = 16; off > 0; off >>= 1)
-        ignored += __shfl_xor_sync(kFull, ignored, off);
-    if ((threadIdx.x & 31) == 0) ignored_part[threadIdx.x >> 5] = ignored;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        long long total = 0;
-        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) total += ignored_part[w];
-        const double n = (double)(rows - total);
-        *mean = (float)((double)(s + c) / n);
+    long long total = 0;
+    if (has_ignore) {
+        // Exact count of ignored rows: warp sums, then thread 0 adds the
+        // warps'.
+        for (int off = 16; off > 0; off >>= 1)
+            ignored += __shfl_xor_sync(kFull, ignored, off);
+        if ((threadIdx.x & 31) == 0) ignored_part[threadIdx.x >> 5] = ignored;
+        __syncthreads();
+        if (threadIdx.x == 0)
+            for (int w = 0; w < (int)(blockDim.x >> 5); ++w)
+                total += ignored_part[w];
     }
+    // One FP32 rounding of the compensated sum, one of the count (exact up
+    // to 2^24 rows) and one of the quotient.
+    if (threadIdx.x == 0) *mean = (s + c) / (float)(rows - total);
 }
 
 cudaError_t launch_mean(const float *loss, float *mean, int64_t rows,
