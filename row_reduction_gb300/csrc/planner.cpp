@@ -76,8 +76,10 @@ bool v_instantiated(int dtype, int64_t V) {
 //  * wider rows, many of them: the loop path with 256 threads per row and
 //    two rows per CTA, so several rows stream through each SM at once;
 //  * wider rows, fewer rows than SMs: a cluster of 8 CTAs per row.
-// All launches use the programmatic-dependent prologue, and persistent
-// CTAs prefetch their next row group.
+// All launches use the programmatic-dependent prologue.  Register-path CTAs
+// prefetch their next row group; loop-path CTAs do not (the measured loop
+// winners mostly do without it: their own second pass re-reads the row from
+// L2, and the prefetch competes with it).
 mt_plan_t heuristic_plan(int op, int dtype, int64_t rows, int64_t cols) {
     (void)op;
     mt_plan_t p;
@@ -137,11 +139,13 @@ mt_plan_t heuristic_plan(int op, int dtype, int64_t rows, int64_t cols) {
         }
         p.path = MT_PATH_LOOP;
         p.chunks = 0;
+        p.flags = MT_PLAN_PDL;
         p.threads_per_row = 512;
         return p;
     }
     p.path = MT_PATH_LOOP;
     p.chunks = 0;
+    p.flags = MT_PLAN_PDL;
     // Two rows per CTA once there are enough rows for two CTAs per SM.
     p.threads_per_row = rows >= 304 ? 256 : 512;
     p.rows_per_block = rows >= 304 ? 2 : 1;
