@@ -834,10 +834,13 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
 #pragma unroll
             for (int k = 0; k < K; ++k) {
                 const int off = (k * WT + worker) * V;
+                // Aligned rows hold whole packs, so one test per pack.
+                const bool pack_in = active && off < nb;
 #pragma unroll
                 for (int e = 0; e < V; ++e) {
                     const float d = v[k][e] - mean;
-                    if (active && off + e < nb) acc[e] = fmaf(d, d, acc[e]);
+                    if (AL ? pack_in : (active && off + e < nb))
+                        acc[e] = fmaf(d, d, acc[e]);
                 }
             }
             float q = 0.f;
