@@ -153,6 +153,38 @@ def test_rmsnorm_sweep_full_size(shape):
     assert torch.allclose(lhs, rhs, rtol=2e-5, atol=0)
 
 
+@pytest.mark.parametrize("op", ["rmsnorm", "row_sum", "softmax"])
+def test_more_than_2_31_elements(op):
+    """A matrix of 524291 x 4096 = 2^31 + 12288 elements (8.6 GB of FP32):
+    element offsets need 64 bits.  The rows repeat a 64-row block made by
+    the input generator, so the oracle's 64 rows give every expected row;
+    sampled rows, the last ones past element 2^31 included, are checked."""
+    rows, cols, blk = (1 << 19) + 3, 4096, 64
+    assert rows * cols > 2 ** 31
+    d = inputs.make(op, blk, cols, SEED + 31)
+    ref = oracle.run(op, d)
+    x = torch.from_numpy(d["x"]).cuda().repeat((rows + blk - 1) // blk, 1)
+    x = x[:rows]
+    if op == "rmsnorm":
+        out = mt.rmsnorm(x, torch.from_numpy(d["weight"]).cuda(), d["eps"])
+        want = ref["y"]
+    elif op == "row_sum":
+        out = mt.row_sum(x)
+        want = ref["out"]
+    else:
+        out = mt.softmax(x)
+        want = ref["y"]
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(11)
+    sample = np.unique(np.concatenate(
+        [[0, blk - 1, rows // 2, rows - 2, rows - 1],
+         rng.integers(0, rows, 24)]))
+    got = out[torch.from_numpy(sample).cuda()].cpu().numpy()
+    assert_close(got, want[sample % blk], f"{op} {rows}x{cols} sampled rows")
+    del x, out
+    torch.cuda.empty_cache()
+
+
 # ------------------------------------------------ lane-mapping matrix
 MAP_N = [1, 31, 33, 127, 128, 129, 257, 4103]
 
