@@ -295,11 +295,11 @@ def time_e2e(work, steps, warmup, depth=1):
     copies the result back to pinned host memory.  Returns (seconds,
     host-to-device bytes per step, device-to-host bytes per step).
 
-    depth = 1 runs the steps one after another on one stream.  depth = 2
-    alternates two device buffer sets, two pinned result buffers and two
-    streams, so one step's upload overlaps the previous step's kernel and
-    download (the two copy directions use separate copy engines); each step
-    still moves its own input and result inside the timed region."""
+    depth = 1 runs the steps one after another on one stream.  depth > 1
+    rotates that many device buffer sets, pinned result buffers and streams,
+    so one step's upload overlaps earlier steps' kernels and downloads (the
+    two copy directions use separate copy engines); each step still moves
+    its own input and result inside the timed region."""
     import torch
     depth = max(1, min(depth, len(work.sets)))
     x_host, out_key = _e2e_host_buffers(work)
