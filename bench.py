@@ -42,11 +42,12 @@ import numpy as np  # noqa: E402
 
 from row_reduction_gb300.timing import (  # noqa: E402
     Workload, algorithmic_bytes, time_e2e, time_graph_steps,
-    time_plain_steps)
+    time_plain_steps, time_rounds)
 
 METRIC = ("RMSNorm FP32 µs/op and HBM GB/s (% of GB300 peak), "
           "1×127 … 1024×4096")
 FALLBACK_HBM_GBS = 6800.0
+DATASHEET_HBM_GBS = 7900.0   # GB300 HBM3e nominal, for context only
 H_OUT_OPS = ("residual_layernorm", "residual_rmsnorm")
 _OUTL = "with 1% x100 outliers"
 INPUT_RECIPE = {
@@ -188,28 +189,94 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sms)}
 
 
-def cpu_baseline(op, d, rows, cols, budget_s=10.0, dtype="f32"):
-    """The CPU oracle as it stands, single-threaded, on the same inputs
-    (`d` in `dtype` storage, handed to the oracle as their exact FP32
-    values), repeated for about `budget_s` seconds."""
-    import oracle
-    from row_reduction_gb300 import inputs
-    oracle.build()
-    d = inputs.widen_all(d, dtype)
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                k = line.split(":")[0].strip().lower()
+                if k in ("model name", "cpu model", "hardware"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+def row_slices(d, bounds):
+    """The input dict restricted to rows [lo, hi) for each bound pair."""
+    return [{k: (v[lo:hi] if isinstance(v, np.ndarray) and
+                 k in ("x", "residual", "labels") else v)
+             for k, v in d.items()} for lo, hi in bounds]
+
+
+class OracleRunner:
+    """Runs the oracle over the rows of `d` on `threads` threads, each on a
+    contiguous block of rows.  The oracle's C code runs through ctypes,
+    which releases the interpreter lock, so the blocks run in parallel."""
+
+    def __init__(self, op, d, rows, threads):
+        import oracle
+        from concurrent.futures import ThreadPoolExecutor
+        oracle.build()
+        self.oracle, self.op = oracle, op
+        threads = max(1, min(threads, rows))
+        step = -(-rows // threads)
+        bounds = [(lo, min(rows, lo + step)) for lo in range(0, rows, step)]
+        self.parts = row_slices(d, bounds)
+        self.threads = len(self.parts)
+        self.pool = ThreadPoolExecutor(self.threads) if self.threads > 1 \
+            else None
+
+    def __call__(self):
+        if self.pool is None:
+            self.oracle.run(self.op, self.parts[0])
+        else:
+            list(self.pool.map(lambda p: self.oracle.run(self.op, p),
+                               self.parts))
+
+    def close(self):
+        if self.pool is not None:
+            self.pool.shutdown()
+
+
+def time_oracle(runner, budget_s):
     reps, t0 = 0, time.perf_counter()
     while True:
-        oracle.run(op, d)
+        runner()
         reps += 1
         el = time.perf_counter() - t0
-        if el >= budget_s or (reps >= 1 and el * (reps + 1) / reps > 3 * budget_s):
-            break
+        if el >= budget_s or el * (reps + 1) / reps > 3 * budget_s:
+            return reps, el
+
+
+def cpu_baseline(op, d, rows, cols, budget_s=10.0, dtype="f32"):
+    """The CPU oracle as it stands on the same inputs (`d` in `dtype`
+    storage, handed to the oracle as their exact FP32 values), on all host
+    cores (row blocks on parallel threads) and on one thread, each repeated
+    for about budget_s / 2 seconds."""
+    from row_reduction_gb300 import inputs
+    d = inputs.widen_all(d, dtype)
     b = algorithmic_bytes(op, rows, cols, op in H_OUT_OPS,
                           op == "cross_entropy", dtype)
-    return {"value": b * reps / el / 1e9, "unit": "GB/s", "cores": 1,
-            "kind": "oracle",
-            "sample": f"{op} {dtype} {rows}x{cols} (the full workload) x {reps} "
-                      f"repetitions, {el:.1f} s, one thread",
-            "us_per_op": el / reps * 1e6}
+    cores = os.cpu_count() or 1
+    out = {}
+    for name, threads in (("all", cores), ("one", 1)):
+        runner = OracleRunner(op, d, rows, threads)
+        reps, el = time_oracle(runner, budget_s / 2)
+        runner.close()
+        out[name] = (runner.threads, reps, el, b * reps / el / 1e9)
+    n, reps, el, gbs = out["all"]
+    n1, reps1, el1, gbs1 = out["one"]
+    return {"value": gbs, "unit": "GB/s", "cores": n, "kind": "oracle",
+            "sample": f"{op} {dtype} {rows}x{cols} (the full workload) x "
+                      f"{reps} repetitions in {el:.1f} s, rows split into "
+                      f"{n} blocks on {n} threads",
+            "us_per_op": el / reps * 1e6, "cpu": cpu_model(),
+            "cpu_count": cores,
+            "single_thread": {"value": gbs1, "unit": "GB/s", "cores": 1,
+                              "us_per_op": el1 / reps1 * 1e6,
+                              "sample": f"x {reps1} repetitions in "
+                                        f"{el1:.1f} s"}}
 
 
 # ---------------------------------------------------------------- arms
@@ -224,23 +291,24 @@ def run_reference(args, rank, world):
         inputs.as_storage(inputs.make(args.op, rows, cols, inputs.TUNE_SEED,
                                       outliers=True), args.dtype),
         args.dtype)
-    # Size the per-step row sample so the whole run stays near 60 s.
-    def rows_of(n):
-        return {k: (v[:n] if isinstance(v, np.ndarray) and
-                    k in ("x", "residual", "labels") else v)
-                for k, v in d.items()}
+    cores = os.cpu_count() or 1
+    # Size the per-step row sample so the whole run stays near 60 s with
+    # the rows split over every host core.
     t0 = time.perf_counter()
-    oracle.run(args.op, rows_of(8))
-    per_row = max((time.perf_counter() - t0) / 8, 1e-7)
+    oracle.run(args.op, row_slices(d, [(0, min(rows, 8))])[0])
+    per_row = max((time.perf_counter() - t0) / min(rows, 8), 1e-7)
     total_steps = args.steps + args.warmup
-    sample_rows = int(max(1, min(rows, 60.0 / total_steps / per_row)))
-    sub = rows_of(sample_rows)
+    sample_rows = int(max(1, min(rows, 60.0 * cores / total_steps /
+                                 per_row)))
+    runner = OracleRunner(args.op, row_slices(d, [(0, sample_rows)])[0],
+                          sample_rows, cores)
     for _ in range(args.warmup):
-        oracle.run(args.op, sub)
+        runner()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.run(args.op, sub)
+        runner()
     el = time.perf_counter() - t0
+    runner.close()
     b = algorithmic_bytes(args.op, sample_rows, cols, args.op in H_OUT_OPS,
                           args.op == "cross_entropy", args.dtype)
     value = b * args.steps / el / 1e9
@@ -254,10 +322,12 @@ def run_reference(args, rank, world):
                    "op": args.op, "storage": args.dtype,
                    "rows": rows, "cols": cols,
                    "sample_rows_per_step": sample_rows},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1,
-                         "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "GB/s",
+                         "cores": runner.threads, "kind": "oracle",
                          "sample": f"first {sample_rows} of {rows} rows "
-                                   f"per step, one thread"},
+                                   f"per step, split into {runner.threads} "
+                                   f"row blocks on as many threads",
+                         "cpu": cpu_model()},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -299,7 +369,9 @@ def run_ours(args, rank, world, local_rank):
                 "traffic": profiled_traffic(key, args.op, plan, args.dtype),
                 "peak_source": f"{peak_kind} HBM copy bandwidth "
                                "(MEASURED_PEAKS.json hbm_gbs)"
-                if peak_kind == "measured" else "fallback 6.8 TB/s"}
+                if peak_kind == "measured" else "fallback 6.8 TB/s",
+                "datasheet_frac": achieved / DATASHEET_HBM_GBS,
+                "datasheet_peak": DATASHEET_HBM_GBS}
 
     plain = time_plain_steps(work, min(args.steps, 20000),
                              min(args.warmup, 200))
@@ -315,6 +387,7 @@ def run_ours(args, rank, world, local_rank):
                      "and buffer sets take turns, so one step's upload "
                      "overlaps earlier steps' kernels and downloads",
            "serial_us_per_step": serial_el / e2e_steps * 1e6}
+    rounds = time_rounds(work, rounds=4, min_round_s=0.03)
 
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
@@ -343,7 +416,15 @@ def run_ours(args, rank, world, local_rank):
                          "us_per_op": plain / plain_steps * 1e6,
                          "steps": plain_steps,
                          "note": "one Python ctypes call per step"},
+        "rounds": {"us_per_op_median": statistics.median(rounds),
+                   "us_per_op_min": min(rounds), "us_per_op_max": max(rounds),
+                   "rounds": len(rounds),
+                   "note": "graph replays over the same pool, each round "
+                           ">= 30 ms"},
     }
+    if world == 1:
+        line["hot"] = hot_number(args, l2)
+        line["torch_context"] = torch_context(work)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.op, work.host, args.rows,
                                             args.cols, args.cpu_seconds,
@@ -352,6 +433,77 @@ def run_ours(args, rank, world, local_rank):
         line["sweep"] = run_sweep(l2, peak)
     print(json.dumps(line))
     return 0
+
+
+def hot_number(args, l2):
+    """The same step on one buffer set every time (inputs and outputs stay
+    in L2 when they fit): a labelled upper bound, not the headline."""
+    import torch
+    from row_reduction_gb300 import inputs
+    hot = Workload(args.op, args.rows, args.cols, inputs.TUNE_SEED,
+                   outliers=True, l2_bytes=l2, max_pool_bytes=0,
+                   dtype=args.dtype)
+    steps = 2000
+    el = time_graph_steps(hot, steps, 100)
+    out = {"us_per_op": el / steps * 1e6,
+           "value": hot.bytes * steps / el / 1e9, "unit": "GB/s",
+           "note": "same buffers every step (L2-resident when they fit)"}
+    del hot
+    torch.cuda.empty_cache()
+    return out
+
+
+def torch_context(work):
+    """PyTorch's own kernel for the operator on the same buffer pool, timed
+    the same way (CUDA graphs, events): context from another library, not
+    a target and not part of this library."""
+    import torch
+    import torch.nn.functional as F
+    op = work.op
+    if op == "cross_entropy":
+        long_labels = {id(s): s["labels"].long() for s in work.sets}
+    fns = {
+        "rmsnorm": lambda s: F.rms_norm(s["x"], (work.cols,), s["weight"],
+                                        work.eps),
+        "layernorm": lambda s: F.layer_norm(s["x"], (work.cols,), s["gamma"],
+                                            s["beta"], work.eps),
+        "softmax": lambda s: torch.softmax(s["x"], dim=1),
+        "log_softmax": lambda s: torch.log_softmax(s["x"], dim=1),
+        "row_sum": lambda s: s["x"].sum(dim=1),
+        "cross_entropy": lambda s: F.cross_entropy(s["x"],
+                                                   long_labels[id(s)]),
+    }
+    if op not in fns or not hasattr(F, "rms_norm"):
+        return None
+    f = fns[op]
+    n = len(work.sets)
+    stream = torch.cuda.Stream()
+    try:
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                f(work.sets[i % n])
+        stream.synchronize()
+        G = n * max(1, math.ceil(64 / n))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(G):
+                f(work.sets[i % n])
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            g.replay()
+            start.record(stream)
+            for _ in range(20):
+                g.replay()
+            end.record(stream)
+        end.synchronize()
+    except Exception as e:  # context only: report why it is missing
+        return {"unavailable": str(e)[:200]}
+    us = start.elapsed_time(end) * 1e3 / (20 * G)
+    del g
+    return {"system": f"torch {torch.__version__}", "us_per_op": us,
+            "value": work.bytes / us / 1e3, "unit": "GB/s",
+            "note": "PyTorch's own kernel on the same pool; context only"}
 
 
 def run_sweep(l2, peak):
