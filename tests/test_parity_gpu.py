@@ -525,6 +525,48 @@ def test_cross_entropy_mean_on_concurrent_streams():
         assert len(set(got.tolist())) == 1     # deterministic per stream
 
 
+def test_calls_from_several_host_threads():
+    """Eight host threads, each with its own stream, call every operator at
+    once; results match a single-threaded run of the same calls bit for
+    bit."""
+    import threading
+    shapes = [(37, 3000), (5, 70001), (300, 129)]
+    jobs = []
+    for op in OPS:
+        for rows, cols in shapes:
+            d = inputs.make(op, rows, cols, SEED + rows + cols)
+            jobs.append((op, {k: (torch.from_numpy(v).cuda()
+                                  if isinstance(v, np.ndarray) else v)
+                              for k, v in d.items()}))
+
+    def run_all(results, idx, stream):
+        with torch.cuda.stream(stream):
+            for j, (op, t) in enumerate(jobs):
+                if j % 8 == idx % 8:
+                    results[j] = mt.run(op, t, stream=stream)
+        stream.synchronize()
+
+    ref = {}
+    run_all(ref, 0, torch.cuda.current_stream())
+    for j in range(1, 8):
+        run_all(ref, j, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    got = {}
+    threads = [threading.Thread(target=run_all,
+                                args=(got, i, torch.cuda.Stream()))
+               for i in range(8)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    torch.cuda.synchronize()
+    assert set(got) == set(ref) == set(range(len(jobs)))
+    for j, (op, _) in enumerate(jobs):
+        for k, v in ref[j].items():
+            assert torch.equal(got[j][k].view(torch.int32),
+                               v.view(torch.int32)), (op, k)
+
+
 # ------------------------------------------------------ ignore index
 @pytest.mark.parametrize("ignore_index", [-100, 0, 7])
 def test_cross_entropy_ignore_index(ignore_index):
