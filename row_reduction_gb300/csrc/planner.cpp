@@ -66,6 +66,21 @@ bool v_instantiated(int dtype, int64_t V) {
     return V == 2 || V == 4 || V == 8;
 }
 
+// Values one CTA's registers hold with V-value packs: 256 threads x 16
+// chunks, the largest register-path team at the 256-thread limit.
+int64_t cta_register_values(int64_t V) { return 256 * 16 * V; }
+
+// Rows wider than one CTA's registers stay on the register path, on a
+// cluster of two CTAs, when there are enough rows to keep every SM busy
+// with such CTAs: measured on 4096 and 8192 rows of 32000 values.  With
+// fewer rows the loop path's wider teams keep more bytes in flight.
+int64_t wide_row_cluster(int64_t rows, int64_t cols, int64_t V) {
+    if (rows < 512) return 0;
+    for (int64_t C = 1; C <= 2; C *= 2)
+        if (C * cta_register_values(V) >= cols) return C;
+    return 0;
+}
+
 // Heuristic plan for shapes far from every measured one.  It follows what
 // the measured winners have in common:
 //  * 16-byte packs (V = 16 / element size) unless the row is tiny;
@@ -73,9 +88,12 @@ bool v_instantiated(int dtype, int64_t V) {
 //  * rows that fit in registers at about 16 values per thread (up to 64 KiB
 //    of FP32 data): one row per CTA of W = row/16 threads (at most 1024),
 //    two rows per CTA when that leaves fewer than 256 threads;
-//  * wider rows, many of them: the loop path with 256 threads per row and
-//    two rows per CTA, so several rows stream through each SM at once;
-//  * wider rows, fewer rows than SMs: a cluster of 8 CTAs per row.
+//  * wider rows, fewer rows than SMs: a cluster of 8 CTAs per row;
+//  * wider rows, at least 512 of them, that one or two CTAs of 256 threads
+//    x 16 chunks hold: the register path on that cluster -- one read of
+//    the row instead of the loop path's two (wide_row_cluster);
+//  * the other wide rows: the loop path with 256 threads per row and two
+//    rows per CTA, so several rows stream through each SM at once.
 // All launches use the programmatic-dependent prologue.  Register-path CTAs
 // prefetch their next row group; loop-path CTAs do not (the measured loop
 // winners mostly do without it: their own second pass re-reads the row from
@@ -143,6 +161,23 @@ mt_plan_t heuristic_plan(int op, int dtype, int64_t rows, int64_t cols) {
         p.threads_per_row = 512;
         return p;
     }
+    if (V * es == 16) {
+        const int64_t Cw = wide_row_cluster(rows, cols, V);
+        if (Cw > 0) {
+            int64_t K = 16;
+            for (int i = 0; i < kNumChunkSet; ++i)
+                if (Cw * 256 * V * kChunkSet[i] >= cols) {
+                    K = kChunkSet[i];
+                    break;
+                }
+            p.cluster = Cw > 1 ? (int)Cw : 0;
+            p.threads_per_row = 256;
+            p.chunks = (int)K;
+            p.rows_per_block = 1;
+            p.path = MT_PATH_REGISTERS;
+            return p;
+        }
+    }
     p.path = MT_PATH_LOOP;
     p.chunks = 0;
     p.flags = MT_PLAN_PDL;
@@ -164,8 +199,12 @@ mt_status plan_check_impl(int op, int dtype, int64_t cols, const mt_plan_t &p);
 // (rows_src * W * cluster) and how they were grouped (threads per CTA,
 // flags, V); the re-fit keeps those and recomputes the rest:
 //  * cluster: cluster_for(rows) for wide rows (>= 8192) of 16-byte packs;
+//    on the register path, rows wider than those CTAs' registers take
+//    wide_row_cluster's cluster, or the loop path when it has none;
 //  * W = the source's threads in flight / rows / cluster (a power of two),
-//    raised until the row fits in at most 8 chunks, capped at 1024;
+//    raised until the row fits in at most 8 chunks, capped at 1024, then
+//    lowered while that breaks the kernel's thread limit for the chunk
+//    count the row needs;
 //  * chunks: the smallest instantiated count that holds the row, the loop
 //    path when none does;
 //  * rows per CTA: what keeps the source's CTA size.
@@ -175,10 +214,19 @@ bool refit(int op, int dtype, int64_t rows_src, int64_t rows, int64_t cols,
     const int64_t V = p->values_per_thread;
     const int64_t cta = (int64_t)p->threads_per_row * p->rows_per_block;
     const int64_t c_src = p->cluster > 1 ? p->cluster : 1;
-    // Split rows when there are few of them and they are wide.
-    const int64_t C = (V * dtype_size(dtype) == 16 && cols >= 8192)
-                          ? cluster_for(rows)
-                          : 1;
+    // Split rows when there are few of them and they are wide, and on the
+    // register path whenever one CTA's registers cannot hold the row.
+    const bool packs16 = V * dtype_size(dtype) == 16;
+    const int64_t c_loop = (packs16 && cols >= 8192) ? cluster_for(rows) : 1;
+    int64_t C = c_loop;
+    if (packs16 && p->path == MT_PATH_REGISTERS &&
+        C * cta_register_values(V) < cols) {
+        const int64_t cw = wide_row_cluster(rows, cols, V);
+        if (cw == 0)
+            p->path = MT_PATH_LOOP;
+        else if (cw > C)
+            C = cw;
+    }
     p->cluster = C > 1 ? (int32_t)C : 0;
     p->grid = 0;
     const double inflight = (double)(rows_src < 1 ? 1 : rows_src) *
@@ -190,22 +238,31 @@ bool refit(int op, int dtype, int64_t rows_src, int64_t rows, int64_t cols,
     while (W < 1024 && C * W * V * 8 < cols) W *= 2;
     if (W > 1024) W = 1024;
     if (p->path == MT_PATH_REGISTERS) {
-        int64_t K = 0;
-        for (int i = 0; i < kNumChunkSet; ++i)
-            if (C * W * V * kChunkSet[i] >= cols) {
-                K = kChunkSet[i];
-                break;
+        // From W down: narrower teams hold more chunks each, and the
+        // kernel's thread limit falls as the chunks per thread rise.
+        for (int64_t w = W; w >= wmin; w /= 2) {
+            int64_t K = 0;
+            for (int i = 0; i < kNumChunkSet; ++i)
+                if (C * w * V * kChunkSet[i] >= cols) {
+                    K = kChunkSet[i];
+                    break;
+                }
+            if (K == 0) break;
+            int64_t B = C > 1 ? 1 : (cta / w < 1 ? 1 : cta / w);
+            while (B > 1 && w * B > reg_max_threads((int)(V * K))) B /= 2;
+            if ((w * B) % 32 == 0 && w * B <= reg_max_threads((int)(V * K))) {
+                p->threads_per_row = (int32_t)w;
+                p->chunks = (int32_t)K;
+                p->rows_per_block = (int32_t)B;
+                if (plan_check_impl(op, dtype, cols, *p) == MT_OK)
+                    return true;
             }
-        int64_t B = C > 1 ? 1 : (cta / W < 1 ? 1 : cta / W);
-        while (K > 0 && B > 1 && W * B > reg_max_threads((int)(V * K))) B /= 2;
-        if (K > 0 && (W * B) % 32 == 0 &&
-            W * B <= reg_max_threads((int)(V * K))) {
-            p->threads_per_row = (int32_t)W;
-            p->chunks = (int32_t)K;
-            p->rows_per_block = (int32_t)B;
-            if (plan_check_impl(op, dtype, cols, *p) == MT_OK) return true;
         }
         p->path = MT_PATH_LOOP;
+        // The loop path splits rows only when they are few.
+        C = c_loop;
+        p->cluster = C > 1 ? (int32_t)C : 0;
+        if (W < 32 && C > 1) W = 32;
     }
     p->chunks = 0;
     if (W > kLoopMaxThreads) W = kLoopMaxThreads;

@@ -71,10 +71,12 @@ def candidates(op, rows, cols, dtype="f32"):
                             out.append(B.make_plan(W, V, 0, Bk,
                                                    B.MT_PATH_LOOP, flags=fl))
             W *= 2
-    # Split rows (clusters of CTAs per row) when rows are too few to give
-    # every SM work: 16-byte packs, one row per CTA.
+    # Split rows (clusters of CTAs per row): when rows are too few to give
+    # every SM work, and when a row is wider than one CTA can hold in
+    # registers (16384 values), so that the cluster holds it instead of the
+    # loop path reading it twice.  16-byte packs, one row per CTA.
     vmax = VALUES[dtype][0]
-    if rows < 304 and cols >= 1024:
+    if (rows < 304 and cols >= 1024) or cols > 16384:
         for C in (2, 4, 8):
             for W in (128, 256, 512, 1024):
                 K = next((k for k in CHUNKS if C * W * vmax * k >= cols),
@@ -248,9 +250,13 @@ def evaluate(records, l2, rounds=7, log=print):
 
 
 # ------------------------------------------------------------ the table
+ROWS_REACH = 16   # a measured plan serves row counts within this factor
+
+
 def _rows_ranges(rows_list):
-    """Splits [1, inf) between the tuned row counts at geometric
-    midpoints."""
+    """Splits the row counts between the tuned ones at geometric midpoints,
+    each range at most a factor ROWS_REACH from its tuned row count (the
+    planner re-fits or falls back beyond that)."""
     rows_list = sorted(rows_list)
     out = []
     for i, r in enumerate(rows_list):
@@ -258,6 +264,8 @@ def _rows_ranges(rows_list):
             rows_list[i - 1] * r))) + 1
         hi = (2 ** 62 if i == len(rows_list) - 1 else
               int(math.floor(math.sqrt(r * rows_list[i + 1]))))
+        lo = max(lo, r // ROWS_REACH)
+        hi = min(hi, r * ROWS_REACH)
         out.append((r, lo, hi))
     return out
 
