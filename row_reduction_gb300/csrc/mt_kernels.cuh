@@ -1027,9 +1027,15 @@ __device__ __forceinline__ void stream_row(int worker, int W, int hd, int nb,
 template <int OP, typename T, int V, bool AL, bool CL>
 __global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
     kernel_prologue<OP, T, CL>(a);
-    // Packs in flight per thread: 4, or 2 for 8-value packs (keeps the
-    // residual LayerNorm variants within the register budget).
-    constexpr int U = V >= 8 ? 2 : 4;
+    // Packs in flight per thread.  RMSNorm, softmax and log-softmax (one
+    // input, light per-pack work, a second pass that re-reads the row): 8,
+    // or 4 for 8-value packs (128 bytes), measured faster on wide rows.  The
+    // others keep 4, or 2 for 8-value packs: the one-pass row sum and
+    // cross-entropy measured slower with 8, and LayerNorm and the residual
+    // operators would leave the register budget.
+    constexpr bool kDeep =
+        OP == OP_RMSNORM || OP == OP_SOFTMAX || OP == OP_LOG_SOFTMAX;
+    constexpr int U = kDeep ? (V >= 8 ? 4 : 8) : (V >= 8 ? 2 : 4);
     __shared__ RedScratch red;
     int parity = 0;
     const T *X = static_cast<const T *>(a.x);
