@@ -136,8 +136,11 @@ typedef struct mt_plan {
                                   resident on the device), the CTAs then loop
                                   over row groups (grid-stride) */
     int32_t flags;             /* MT_PLAN_* bits */
-    int32_t cluster;           /* CTAs sharing one row: 0 or 1 = none; 2, 4
-                                  or 8 = a thread-block cluster of that many
+    int32_t cluster;           /* CTAs sharing one row: 0 or 1 = none; 2, 4,
+                                  8 or 16 (16: beyond the portable cluster
+                                  size; the launch fails with MT_ERR_CUDA
+                                  where the device cannot place it) = a
+                                  thread-block cluster of that many
                                   CTAs splits every row (then
                                   rows_per_block = 1, W >= 32, 16-byte packs
                                   (V*element size = 16), the ownership map

@@ -1329,6 +1329,13 @@ __host__ cudaError_t launch_op(const mt_plan_t &p, const KArgs &a,
         attr[n].val.programmaticStreamSerializationAllowed = 1;
         ++n;
     }
+    if (a.csize > 8) {
+        // 16 CTAs per cluster is beyond the portable size of 8.
+        if (cudaError_t e = cudaFuncSetAttribute(
+                reinterpret_cast<const void *>(k),
+                cudaFuncAttributeNonPortableClusterSizeAllowed, 1))
+            return e;
+    }
     if (a.csize > 1) {
         attr[n].id = cudaLaunchAttributeClusterDimension;
         attr[n].val.clusterDim.x = (unsigned)a.csize;

@@ -47,10 +47,14 @@ int64_t pow2_ceil(int64_t v) {
 }
 
 // CTAs per row for a row count: rows are split across a cluster only while
-// there are too few rows to give each SM work (152 SMs: 8 CTAs per row up to
-// 19 rows, 4 up to 38, 2 up to 76).
+// there are too few rows to give each SM work (152 SMs: 16 CTAs per row up
+// to 9 rows, 8 up to 19, 4 up to 38, 2 up to 76).
 int64_t cluster_for(int64_t rows) {
-    return rows <= 19 ? 8 : rows <= 38 ? 4 : rows <= 76 ? 2 : 1;
+    return rows <= 9    ? 16
+           : rows <= 19 ? 8
+           : rows <= 38 ? 4
+           : rows <= 76 ? 2
+                        : 1;
 }
 
 bool chunk_instantiated(int k) {
@@ -295,7 +299,7 @@ mt_status plan_check_impl(int op, int dtype, int64_t cols, const mt_plan_t &p) {
     if (p.flags & ~(MT_PLAN_PDL | MT_PLAN_PREFETCH_NEXT))
         return MT_ERR_INVALID_ARGUMENT;
     const int64_t C = p.cluster <= 1 ? 1 : p.cluster;
-    if (p.cluster < 0 || (C != 1 && C != 2 && C != 4 && C != 8))
+    if (p.cluster < 0 || (C != 1 && C != 2 && C != 4 && C != 8 && C != 16))
         return MT_ERR_INVALID_ARGUMENT;
     // Split rows (clusters) are built for 16-byte packs only.
     if (C > 1 && (B != 1 || W < 32 || p.grid % C != 0 ||

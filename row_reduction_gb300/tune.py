@@ -77,7 +77,7 @@ def candidates(op, rows, cols, dtype="f32"):
     # loop path reading it twice.  16-byte packs, one row per CTA.
     vmax = VALUES[dtype][0]
     if (rows < 304 and cols >= 1024) or cols > 16384:
-        for C in (2, 4, 8):
+        for C in ((2, 4, 8, 16) if rows <= 19 else (2, 4, 8)):
             for W in (128, 256, 512, 1024):
                 K = next((k for k in CHUNKS if C * W * vmax * k >= cols),
                          None)

@@ -275,7 +275,8 @@ def test_cluster_plan_legality():
     assert chk(16384, cluster=4) == OK          # 4 * 256 * 4 * 4 = 16384
     assert chk(16384, cluster=2) == OOR         # half the row does not fit
     assert chk(16384, cluster=3) == INV
-    assert chk(16384, cluster=16) == INV
+    assert chk(16384, cluster=16) == OK         # 16 CTAs: non-portable size
+    assert chk(16384, cluster=32) == INV
     assert chk(16384, cluster=-1) == INV
     assert chk(16384, cluster=4, rows_per_block=2) == INV
     assert chk(4096, cluster=2, W=16, chunks=16, rows_per_block=2) == INV

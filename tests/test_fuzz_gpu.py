@@ -31,7 +31,7 @@ def random_plan(rng, op, dt, cols):
         V = int(rng.choice(VALUES[dt]))
         W = int(2 ** rng.integers(0, 11))
         path = int(rng.choice([mt.MT_PATH_REGISTERS, mt.MT_PATH_LOOP]))
-        cluster = int(rng.choice([0, 0, 0, 2, 4, 8]))
+        cluster = int(rng.choice([0, 0, 0, 2, 4, 8, 16]))
         B = int(2 ** rng.integers(0, 6))
         K = 0
         if path == mt.MT_PATH_REGISTERS:

@@ -623,7 +623,7 @@ def test_residual_rmsnorm_aliasing_and_zero_residual():
 # ------------------------------------------ split rows (thread-block clusters)
 def cluster_plans(cols, V=4):
     plans = []
-    for C in (2, 4, 8):
+    for C in (2, 4, 8, 16):
         for W in (32, 128, 512):
             for K in (1, 2, 4, 8, 16):
                 p = mt.make_plan(W, V, K, 1, cluster=C,

@@ -300,7 +300,9 @@ def test_cluster_split_rows_half(dt, op):
     rows, cols = 3, 50003
     st, wide = case(op, rows, cols, dt, SEED + 31)
     for p in (mt.make_plan(512, 8, 4, 1, cluster=4),
-              mt.make_plan(256, 8, 0, 1, mt.MT_PATH_LOOP, cluster=8)):
+              mt.make_plan(256, 8, 0, 1, mt.MT_PATH_LOOP, cluster=8),
+              mt.make_plan(128, 8, 4, 1, cluster=16),
+              mt.make_plan(512, 8, 0, 1, mt.MT_PATH_LOOP, cluster=16)):
         assert mt.mt_plan_check_dtype(op, dt, cols, p) == mt.MT_OK
         outs = run(op, st, dt, rows, cols, plan=p)
         check(op, dt, outs, st, wide, f"{op} {dt} {mt.mt_describe_plan(p)}")
