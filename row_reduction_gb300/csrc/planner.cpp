@@ -258,6 +258,18 @@ bool refit(int op, int dtype, int64_t rows_src, int64_t rows, int64_t cols,
                 p->threads_per_row = (int32_t)w;
                 p->chunks = (int32_t)K;
                 p->rows_per_block = (int32_t)B;
+                // ptxas holds the FP32 4-value, 2-chunk instance to 32
+                // registers (it spills); the same row in 2-value packs and
+                // 4 chunks does not.
+                if (dtype == DT_F32 && V == 4 && K == 2 && C == 1 &&
+                    w >= 2) {
+                    p->values_per_thread = 2;
+                    p->chunks = 4;
+                    if (plan_check_impl(op, dtype, cols, *p) == MT_OK)
+                        return true;
+                    p->values_per_thread = 4;
+                    p->chunks = 2;
+                }
                 if (plan_check_impl(op, dtype, cols, *p) == MT_OK)
                     return true;
             }
