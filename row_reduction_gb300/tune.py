@@ -1,9 +1,12 @@
 """Measured launch-plan search; writes the planner's table.
 
-For each (operator, rows, cols) the tuner enumerates the legal plans
-(V in {1, 2, 4}; W a power of two; the smallest register chunk count that
-holds the row; rows per CTA B so that a CTA has 32..1024 threads; the loop
-path for wide rows), and for each plan:
+For each (operator, storage type, rows, cols) the tuner enumerates the legal
+plans (V in {1, 2, 4} for FP32 and {2, 4, 8} for FP16/BF16; W a power of
+two; the smallest register chunk count that holds the row; rows per CTA B so
+that a CTA has 32..1024 threads; the loop path for wide rows; clusters of
+2, 4, 8 or 16 CTAs per row for few or very wide rows; the launch flags),
+then, in a second stage, the four fastest again on persistent grids of one
+to three CTAs per SM.  For each plan it:
 
 1. runs it once on the tuning-seed inputs and validates the complete output
    against the reference plan's output (|a-b| <= 1e-5*(1+|b|)); a plan that
