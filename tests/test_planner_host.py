@@ -1,0 +1,85 @@
+"""Host-side checks of the planner and the input generator's storage
+rounding (no GPU): every measured table entry is a legal plan, and the
+documented planning rules hold on the shapes they were measured on."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import row_reduction_gb300 as mt
+from row_reduction_gb300 import inputs
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+TABLE = os.path.join(ROOT, "row_reduction_gb300", "csrc", "plan_table.json")
+
+
+def plan(op, dt, rows, cols):
+    return mt.mt_plan_query_dtype(op, dt, rows, cols)
+
+
+def test_every_table_winner_is_legal_and_served():
+    recs = json.load(open(TABLE))["records"]
+    assert len(recs) >= 100
+    for r in recs:
+        dt = r.get("dtype", "f32")
+        w = mt.MtPlan(**r["winner"])
+        assert mt.mt_plan_check_dtype(mt.OP_IDS[r["op"]], dt, r["cols"],
+                                      w) == mt.MT_OK, r["winner_text"]
+        # the planner returns the measured winner on its own shape
+        got = plan(r["op"], dt, r["rows"], r["cols"]).as_dict()
+        assert got == w.as_dict(), (r["op"], dt, r["rows"], r["cols"])
+
+
+def test_few_wide_rows_split_across_clusters():
+    # up to 9 rows: 16 CTAs per row; up to 19: 8; up to 38: 4; up to 76: 2
+    for rows, C in ((1, 16), (9, 16), (10, 8), (19, 8), (20, 4), (38, 4),
+                    (39, 2), (76, 2)):
+        p = plan("layernorm", "f32", rows, 300000)
+        assert p.cluster == C, (rows, p.as_dict())
+
+
+def test_many_wide_rows_stay_in_registers_when_two_ctas_hold_them():
+    # 32000 FP32 values need two CTAs of 256 threads x 16 chunks; 32000
+    # BF16 values fit one
+    p = plan("layernorm", "f32", 8192, 32000)
+    assert (p.path, p.cluster) == (mt.MT_PATH_REGISTERS, 2)
+    p = plan("layernorm", "bf16", 8192, 32000)
+    assert p.path == mt.MT_PATH_REGISTERS and p.cluster <= 1
+    # wider than two CTAs, or too few rows: the loop path
+    assert plan("layernorm", "f32", 8192, 65536).path == mt.MT_PATH_LOOP
+    assert plan("softmax", "bf16", 128, 50257).path == mt.MT_PATH_LOOP
+
+
+def test_refit_avoids_the_spilling_fp32_instance():
+    for op in ("rmsnorm", "residual_layernorm"):
+        for rows, cols in ((512, 2048), (300, 3000)):
+            p = plan(op, "f32", rows, cols)
+            assert not (p.values_per_thread == 4 and p.chunks == 2 and
+                        p.path == mt.MT_PATH_REGISTERS), (op, rows, cols)
+
+
+def test_loop_heuristic_leaves_the_next_group_prefetch_off():
+    p = plan("row_sum", "f32", 2048, 131072)
+    assert p.path == mt.MT_PATH_LOOP
+    assert not p.flags & mt.MT_PLAN_PREFETCH_NEXT
+
+
+@pytest.mark.parametrize("seed", [1, 2, 3])
+def test_bf16_storage_rounding_matches_torch(seed):
+    """The generator's BF16 rounding (nearest even, on the bit pattern) is
+    torch's; FP16 is NumPy's IEEE conversion; widening is exact."""
+    rng = np.random.default_rng(seed)
+    x = (rng.standard_normal(4096) *
+         10.0 ** rng.integers(-20, 20, 4096)).astype(np.float32)
+    x[:4] = [0.0, -0.0, 1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8]  # ties
+    st = inputs.as_storage({"x": x}, "bf16")["x"]
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy()
+    assert np.array_equal(st.view(np.int16), ref)
+    wide = inputs.widen(st, "bf16")
+    assert np.array_equal(
+        wide, torch.from_numpy(x).to(torch.bfloat16).float().numpy())
+    h = inputs.as_storage({"x": np.clip(x, -6e4, 6e4)}, "f16")["x"]
+    assert h.dtype == np.float16
+    assert np.array_equal(inputs.widen(h, "f16"), h.astype(np.float32))
