@@ -198,6 +198,14 @@ def cpu_model():
                     return line.split(":", 1)[1].strip()
     except OSError:
         pass
+    try:   # Arm hosts: /proc/cpuinfo has no model name, lscpu does
+        out = subprocess.run(["lscpu"], capture_output=True, text=True,
+                             timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
     import platform
     return platform.machine()
 
