@@ -21,7 +21,10 @@ Definitions, per row of n = cols entries (see the header of ``oracle.c``):
   variants on the same rows, the plain compositions of those definitions.
 
 Pins: ``tests/test_oracle_pins.py`` checks every function against closed
-forms, invariants, exactly-rounded sums and torch float64 library routines.
+forms, invariants, exactly-rounded sums and torch float64 library routines;
+``tests/test_oracle_mutations.py`` plants slips in a copy of ``oracle.c`` and
+checks that the pins catch each one (it points ``ORACLE_LIB`` at the
+mutant's library; unset, the module builds and loads ``liboracle.so``).
 """
 from __future__ import annotations
 
@@ -56,8 +59,10 @@ def _load():
     global _lib
     with _lock:
         if _lib is None:
-            build()
-            lib = ctypes.CDLL(_LIB)
+            path = os.environ.get("ORACLE_LIB")
+            if not path:
+                path = build()
+            lib = ctypes.CDLL(path)
             P = ctypes.c_void_p
             I = ctypes.c_int64
             D = ctypes.c_double
