@@ -426,7 +426,7 @@ def run_ours(args, rank, world, local_rank):
                          "note": "one Python ctypes call per step"},
         "rounds": {"us_per_op_median": statistics.median(rounds),
                    "us_per_op_min": min(rounds), "us_per_op_max": max(rounds),
-                   "rounds": len(rounds),
+                   "rounds": len(rounds), "samples_us": rounds,
                    "note": "graph replays over the same pool, each round "
                            ">= 30 ms"},
     }
@@ -550,6 +550,43 @@ def run_sweep(l2, peak):
     return out
 
 
+def verify_line(line):
+    """Audits one JSON line of this benchmark: the reported figures
+    recomputed from the raw ones (steps, time, bytes, samples), and the
+    recorded plan against the planner's current choice.  Returns a list of
+    problems (empty when the line is consistent)."""
+    bad = []
+
+    def close(a, b, what, rel=1e-6):
+        if a is None or b is None or abs(a - b) > rel * max(abs(b), 1e-30):
+            bad.append(f"{what}: {a} vs {b}")
+
+    if line.get("impl") == "reference":
+        close(line["cpu_baseline"]["value"], line["value"], "cpu_baseline")
+        return bad
+    cfg = line["config"]
+    dtype = cfg.get("storage", "f32")
+    op, rows, cols = cfg["op"], cfg["rows"], cfg["cols"]
+    b = algorithmic_bytes(op, rows, cols, op in H_OUT_OPS,
+                          op == "cross_entropy", dtype)
+    per_step = line["ms_per_step"] / 1e3
+    close(line["value"], line["n_gpus"] * b / per_step / 1e9, "value")
+    close(line["us_per_op"], line["ms_per_step"] * 1e3, "us_per_op")
+    roof = line["roofline"]
+    close(roof["achieved"], b / per_step / 1e9, "roofline.achieved")
+    close(roof["frac"], roof["achieved"] / roof["peak"], "roofline.frac")
+    r = line.get("rounds")
+    if r and "samples_us" in r:
+        s = r["samples_us"]
+        close(r["us_per_op_median"], statistics.median(s), "rounds median")
+        close(r["us_per_op_min"], min(s), "rounds min")
+        close(r["us_per_op_max"], max(s), "rounds max")
+    if cfg["plan"] != plan_text(op, rows, cols, dtype):
+        bad.append(f"plan: recorded {cfg['plan']!r}, planner now "
+                   f"{plan_text(op, rows, cols, dtype)!r}")
+    return bad
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -565,7 +602,18 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--verify", metavar="FILE", default=None,
+                    help="audit the JSON line(s) in FILE instead of timing")
     args = ap.parse_args()
+    if args.verify:
+        problems = []
+        for ln in open(args.verify):
+            if ln.startswith("{"):
+                problems += verify_line(json.loads(ln))
+        for p in problems:
+            print(p)
+        print("consistent" if not problems else f"{len(problems)} problems")
+        return 1 if problems else 0
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
 

@@ -64,3 +64,35 @@ def test_algorithmic_bytes_match_the_documented_formulas():
     assert algorithmic_bytes("cross_entropy", R, C, mean=True) == 16785412
     assert algorithmic_bytes("rmsnorm", R, C, dtype="bf16") == \
         4 * R * C + 2 * C
+
+
+def _line(us=5.9, plan=None):
+    import bench
+    from row_reduction_gb300.timing import algorithmic_bytes
+    b = algorithmic_bytes("rmsnorm", 1024, 4096)
+    ach = b / (us * 1e-6) / 1e9
+    return {"metric": "m", "value": ach, "unit": "GB/s", "n_gpus": 1,
+            "steps": 100, "warmup": 10, "ms_per_step": us / 1e3,
+            "us_per_op": us,
+            "config": {"op": "rmsnorm", "storage": "f32", "rows": 1024,
+                       "cols": 4096,
+                       "plan": plan or bench.plan_text("rmsnorm", 1024,
+                                                       4096)},
+            "roofline": {"achieved": ach, "peak": 6783.1,
+                         "frac": ach / 6783.1},
+            "rounds": {"us_per_op_median": 5.95, "us_per_op_min": 5.9,
+                       "us_per_op_max": 6.0,
+                       "samples_us": [5.9, 5.95, 6.0]}}
+
+
+def test_verify_accepts_a_consistent_line_and_flags_the_rest():
+    import bench
+    assert bench.verify_line(_line()) == []
+    bad = _line()
+    bad["value"] *= 1.01
+    bad["rounds"]["us_per_op_median"] = 5.0
+    problems = bench.verify_line(bad)
+    assert any(p.startswith("value") for p in problems)
+    assert any(p.startswith("rounds median") for p in problems)
+    assert bench.verify_line(_line(plan="path=loop W=1"))[0].startswith(
+        "plan")
