@@ -185,6 +185,25 @@ def test_more_than_2_31_elements(op):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16,
+                                   torch.float16])
+def test_signed_zeros_keep_their_sign(dtype):
+    """RMSNorm scales x by a positive factor (weights > 0), so -0.0 and
+    +0.0 come out with their own sign; bit-checked."""
+    rows, cols = 33, 4096
+    g = torch.Generator().manual_seed(5)
+    x = torch.randn(rows, cols, generator=g)
+    x[:, ::7] = 0.0
+    x[:, 3::7] = -0.0
+    w = 1.0 + 0.1 * torch.rand(cols, generator=g)
+    xd, wd = x.to(dtype).cuda(), w.to(dtype).cuda()
+    y = mt.rmsnorm(xd, wd, 1e-6).cpu()
+    neg = torch.signbit(x.to(dtype)) & (x == 0)
+    pos = ~torch.signbit(x.to(dtype)) & (x == 0)
+    assert bool((y[neg] == 0).all()) and bool(torch.signbit(y[neg]).all())
+    assert bool((y[pos] == 0).all()) and not bool(torch.signbit(y[pos]).any())
+
+
 # ------------------------------------------------ lane-mapping matrix
 MAP_N = [1, 31, 33, 127, 128, 129, 257, 4103]
 
