@@ -178,7 +178,8 @@ MT_API mt_status mt_rmsnorm_f32_with_plan(const float *x, const float *weight,
 
 /* LayerNorm per row: mu = mean(x), var = mean((x-mu)^2) (biased),
  * y = (x - mu) / sqrt(var + eps) * gamma + beta.  gamma may be NULL (ones),
- * beta may be NULL (zeros). */
+ * beta may be NULL (zeros).  ("Consecutive-worker reduction layout checkpoint", §Evidence and
+ * what remains, names the operator; the textbook definition is used.) */
 MT_API mt_status mt_layernorm_f32(const float *x, const float *gamma,
                            const float *beta, float *y, int64_t rows,
                            int64_t cols, float eps, mt_stream_t stream);
@@ -189,7 +190,9 @@ MT_API mt_status mt_layernorm_f32_with_plan(const float *x, const float *gamma,
                                      const mt_plan_t *plan);
 
 /* Residual LayerNorm per row: h = x + residual (FP32 add);
- * y = LayerNorm(h) as above; if h_out != NULL it receives h. */
+ * y = LayerNorm(h) as above; if h_out != NULL it receives h.
+ * ("Consecutive-worker reduction layout checkpoint", §Evidence and
+ * what remains, names the operator; the textbook definition is used.) */
 MT_API mt_status mt_residual_layernorm_f32(const float *x, const float *residual,
                                     const float *gamma, const float *beta,
                                     float *y, float *h_out, int64_t rows,
@@ -201,7 +204,8 @@ MT_API mt_status mt_residual_layernorm_f32_with_plan(
     float eps, mt_stream_t stream, const mt_plan_t *plan);
 
 /* Softmax per row: y = exp(x - max(x)) / sum(exp(x - max(x))).  A row that
- * holds a NaN gives an all-NaN output row. */
+ * holds a NaN gives an all-NaN output row.  ("Consecutive-worker reduction layout checkpoint", §Evidence and
+ * what remains, names the operator; the textbook definition is used.) */
 MT_API mt_status mt_softmax_f32(const float *x, float *y, int64_t rows,
                          int64_t cols, mt_stream_t stream);
 MT_API mt_status mt_softmax_f32_with_plan(const float *x, float *y, int64_t rows,
@@ -210,7 +214,9 @@ MT_API mt_status mt_softmax_f32_with_plan(const float *x, float *y, int64_t rows
 
 /* Row sum: out[r] = sum of row r (rows outputs).  Accumulated with
  * compensated (two-sum) FP32 arithmetic, so sums of small integers are
- * exact and near-zero sums keep their relative accuracy. */
+ * exact and near-zero sums keep their relative accuracy.
+ * ("Consecutive-worker reduction layout checkpoint", §Evidence and
+ * what remains, names the operator; the textbook definition is used.) */
 MT_API mt_status mt_row_sum_f32(const float *x, float *out, int64_t rows,
                          int64_t cols, mt_stream_t stream);
 MT_API mt_status mt_row_sum_f32_with_plan(const float *x, float *out, int64_t rows,
@@ -221,7 +227,9 @@ MT_API mt_status mt_row_sum_f32_with_plan(const float *x, float *out, int64_t ro
  * (computed with the row max subtracted).  labels holds rows int32 class
  * indices; a label outside [0, cols) gives loss NaN for that row.  If
  * mean_loss != NULL it receives sum(loss) / rows, summed in a fixed order by
- * a second one-CTA kernel on the same stream (deterministic). */
+ * a second one-CTA kernel on the same stream (deterministic).
+ * ("Consecutive-worker reduction layout checkpoint", §Evidence and
+ * what remains, names the operator; the textbook definition is used.) */
 MT_API mt_status mt_cross_entropy_f32(const float *logits, const int32_t *labels,
                                float *loss, float *mean_loss, int64_t rows,
                                int64_t cols, mt_stream_t stream);
@@ -231,7 +239,9 @@ MT_API mt_status mt_cross_entropy_f32_with_plan(const float *logits,
                                          int64_t cols, mt_stream_t stream,
                                          const mt_plan_t *plan);
 
-/* ---- fused variants (same engine, same conventions) --------------------- */
+/* ---- fused variants (same engine, same conventions) ---------------------
+ * The pages do not name these; each is the plain composition of the
+ * definitions above. */
 
 /* Residual RMSNorm (pre-norm add-and-norm) per row: h = x + residual (FP32
  * add); y = h / sqrt(mean(h^2) + eps) * weight; if h_out != NULL it
