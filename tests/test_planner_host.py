@@ -83,3 +83,31 @@ def test_bf16_storage_rounding_matches_torch(seed):
     h = inputs.as_storage({"x": np.clip(x, -6e4, 6e4)}, "f16")["x"]
     assert h.dtype == np.float16
     assert np.array_equal(inputs.widen(h, "f16"), h.astype(np.float32))
+
+
+def test_tuner_candidates_are_legal_and_cover_the_plan_space():
+    from row_reduction_gb300 import tune
+    for op, rows, cols, dt in (("rmsnorm", 1, 1048576, "f32"),
+                               ("softmax", 4096, 32000, "bf16"),
+                               ("layernorm", 1024, 4096, "f32"),
+                               ("cross_entropy", 17, 257, "f16")):
+        cands = tune.candidates(op, rows, cols, dt)
+        assert cands
+        for p in cands:
+            assert mt.mt_plan_check_dtype(mt.OP_IDS[op], dt, cols,
+                                          p) == mt.MT_OK
+        clusters = {p.cluster for p in cands}
+        if cols > 16384 or (rows < 304 and cols >= 1024):
+            assert clusters & {2, 4, 8}
+        if rows <= 19 and cols >= 1024:
+            assert 16 in clusters
+        paths = {p.path for p in cands}
+        assert mt.MT_PATH_REGISTERS in paths or cols > 16384
+        if cols >= 8192:
+            assert mt.MT_PATH_LOOP in paths
+        # second stage: persistent grids below the row-group count
+        extra = tune.grid_variants(rows, cands[:4], 152)
+        for p in extra:
+            C = max(1, p.cluster)
+            assert p.grid % C == 0
+            assert p.grid // C < -(-rows // p.rows_per_block)
