@@ -5,20 +5,23 @@ One step = one call of the headline operator (RMSNorm, FP32) over one
 rows x cols matrix, through the C ABI.  Default workload: RMSNorm 1024x4096,
 x ~ N(0,1) with 1% outliers x100, weight ~ 1 + 0.1 N(0,1), eps = 1e-6.
 
-Device timing: the K timed steps run back to back on one stream, replayed
-from CUDA graphs of captured library calls (so host launch cost is not in the
-number), bracketed by CUDA events with a synchronize (and, for N > 1, a
-barrier) on both sides.  Consecutive steps cycle through a pool of input /
-output buffers at least 4x the L2 size, so no step finds its input in L2.
-`value` = algorithmic bytes moved per step x steps / time, in GB/s (the
-HBM-bandwidth form of the metric; `us_per_op` gives the time form).
+Device timing: exactly K timed steps run back to back on one stream,
+replayed from CUDA graphs of captured library calls (so host launch cost is
+not in the number), bracketed by CUDA events with a synchronize (and, for
+N > 1, a barrier) on both sides.  One untimed replay is enqueued ahead of the
+start event, so the host's graph-launch latency is not in the timed region
+either.  Consecutive steps cycle through a pool of input / output buffers at
+least 4x the L2 size, so no step finds its input in L2.  `value` =
+algorithmic bytes moved per step x steps / time, in GB/s (the HBM-bandwidth
+form of the metric; `us_per_op` gives the time form).
 
-Also reported: `e2e` (same metric, each step copying x from pinned host
-memory and y back, around the library call), `roofline` (vs the measured HBM
-copy bandwidth), `cpu_baseline` (the CPU oracle on the host cores),
-`clocks` (nvidia-smi samples during the timed region), `plain_launch` (the
-same steps launched one by one from Python instead of replayed from graphs)
-and `sweep` (every published shape and operator, same method).
+Output.  The LAST line on stdout is one compact JSON object, the headline
+(at most HEADLINE_MAX_BYTES bytes), carrying the keys a reader needs:
+value, roofline, e2e (with its host-link ceiling), clocks, the per-round
+median, the copy/empty-kernel floor and the CPU baseline.  Everything else
+(the sweep over every published shape and operator, the same-buffer "hot"
+number, plain launches, PyTorch's own kernels as context) goes to stderr as
+a table, and to --details FILE as JSON.
 
 `--impl reference` times the CPU oracle instead, on a bounded row sample of
 the same workload per step.
@@ -33,6 +36,7 @@ import os
 import statistics
 import subprocess
 import sys
+import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -41,14 +45,18 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 
 from row_reduction_gb300.timing import (  # noqa: E402
-    Workload, algorithmic_bytes, time_e2e, time_graph_steps,
-    time_plain_steps, time_rounds)
+    CopyProbe, EmptyProbe, Workload, algorithmic_bytes, time_e2e,
+    time_graph_steps, time_link, time_plain_steps, time_rounds)
 
 METRIC = ("RMSNorm FP32 µs/op and HBM GB/s (% of GB300 peak), "
           "1×127 … 1024×4096")
 FALLBACK_HBM_GBS = 6800.0
 DATASHEET_HBM_GBS = 7900.0   # GB300 HBM3e nominal, for context only
+HEADLINE_MAX_BYTES = 1536
 H_OUT_OPS = ("residual_layernorm", "residual_rmsnorm")
+# Operators with one input matrix x and one output matrix y of its shape:
+# the copy floor moves exactly their matrix bytes.
+COPY_FLOOR_OPS = ("rmsnorm", "layernorm", "softmax", "log_softmax")
 _OUTL = "with 1% x100 outliers"
 INPUT_RECIPE = {
     "rmsnorm": f"x~N(0,1) {_OUTL}, weight~1+0.1N(0,1), eps=1e-6",
@@ -81,6 +89,13 @@ def job_value(bytes_per_step, steps, elapsed, world):
     """Whole-job GB/s: every rank moves bytes_per_step per step (replicas,
     weak scaling); time is the slowest rank's."""
     return world * bytes_per_step * steps / elapsed / 1e9
+
+
+def sig(x, digits=6):
+    """x rounded to `digits` significant digits (None stays None)."""
+    if x is None or x == 0 or not math.isfinite(x):
+        return x
+    return float(f"{x:.{digits}g}")
 
 
 def plan_text(op, rows, cols, dtype="f32"):
@@ -132,19 +147,24 @@ def profiled_traffic(workload_key, op, plan, dtype="f32"):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason samples while running."""
+    """nvidia-smi clock / throttle-reason samples, read by a background
+    thread while the GPU runs (start() ... stop())."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,"
              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
              "clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,"
              "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+             "sw_power_cap")
 
     def __init__(self, index):
         self.index = index
         self.proc = None
+        self.lines = []
+        self.reader = None
 
-    def __enter__(self):
+    def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}",
@@ -153,40 +173,56 @@ class ClockSampler:
                 stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
-        return self
+            return
+        self.reader = threading.Thread(target=self._read, daemon=True)
+        self.reader.start()
 
-    def __exit__(self, *exc):
-        self.lines = []
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                out, _ = self.proc.communicate(timeout=5)
-            except Exception:
-                self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [l for l in out.splitlines() if l.strip()]
+    def _read(self):
+        for line in self.proc.stdout:
+            if line.strip():
+                self.lines.append(line)
+
+    def samples(self):
+        return [p for p in (self._parse(l) for l in list(self.lines)) if p]
+
+    def has_samples(self, n):
+        """At least n samples so far (True at once if nvidia-smi could not
+        be started: there is nothing to wait for)."""
+        return self.proc is None or len(self.samples()) >= n
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+            self.proc.wait()
+        if self.reader is not None:
+            self.reader.join(timeout=5)
+
+    def _parse(self, line):
+        f = [x.strip() for x in line.split(",")]
+        if len(f) < 9:
+            return None
+        try:
+            sm, mx = float(f[1]), float(f[2])
+        except ValueError:
+            return None
+        active = [n for n, v in zip(self.NAMES, f[5:9])
+                  if v.lower() == "active"]
+        return sm, mx, active
 
     def summary(self):
-        sms, maxs, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
-                 "sw_power_cap"]
-        for line in getattr(self, "lines", []):
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sms.append(float(f[1]))
-                maxs.append(float(f[2]))
-            except ValueError:
-                continue
-            for name, val in zip(names, f[5:9]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        if not sms:
+        s = self.samples()
+        if not s:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
                     "samples": 0}
-        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxs),
-                "reasons": sorted(reasons), "samples": len(sms)}
+        return {"sm_mhz": statistics.median(x[0] for x in s),
+                "sm_max_mhz": max(x[1] for x in s),
+                "reasons": sorted({r for x in s for r in x[2]}),
+                "samples": len(s)}
 
 
 def cpu_model():
@@ -276,15 +312,28 @@ def cpu_baseline(op, d, rows, cols, budget_s=10.0, dtype="f32"):
     n, reps, el, gbs = out["all"]
     n1, reps1, el1, gbs1 = out["one"]
     return {"value": gbs, "unit": "GB/s", "cores": n, "kind": "oracle",
-            "sample": f"{op} {dtype} {rows}x{cols} (the full workload) x "
-                      f"{reps} repetitions in {el:.1f} s, rows split into "
-                      f"{n} blocks on {n} threads",
-            "us_per_op": el / reps * 1e6, "cpu": cpu_model(),
-            "cpu_count": cores,
+            "sample": f"full {rows}x{cols} x{reps} in {el:.1f} s, "
+                      f"{n} row blocks on {n} threads",
+            "cpu": cpu_model(), "us_per_op": el / reps * 1e6,
             "single_thread": {"value": gbs1, "unit": "GB/s", "cores": 1,
-                              "us_per_op": el1 / reps1 * 1e6,
-                              "sample": f"x {reps1} repetitions in "
-                                        f"{el1:.1f} s"}}
+                              "us_per_op": el1 / reps1 * 1e6}}
+
+
+def headline_json(line):
+    """The headline as one compact JSON line; raises if it would exceed
+    HEADLINE_MAX_BYTES (a reader that keeps only the tail of stdout must
+    still see all of it)."""
+    text = json.dumps(line, separators=(",", ":"))
+    n = len(text.encode())
+    if n > HEADLINE_MAX_BYTES:
+        raise ValueError(f"headline is {n} bytes, over {HEADLINE_MAX_BYTES}")
+    return text
+
+
+def emit_headline(line):
+    sys.stdout.flush()
+    sys.stderr.flush()
+    print(headline_json(line), flush=True)
 
 
 # ---------------------------------------------------------------- arms
@@ -339,8 +388,96 @@ def run_reference(args, rank, world):
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
-    print(json.dumps(line))
+    emit_headline(line)
     return 0
+
+
+def quick_us(work, rounds=3, min_round_s=0.01):
+    """Median µs per step over a few short graph-replay rounds."""
+    return statistics.median(time_rounds(work, rounds=rounds,
+                                         min_round_s=min_round_s))
+
+
+def measure_floor(work):
+    """The floor of one step, timed like the steps themselves (graph
+    replays of dependent launches over the same rotating pool): the
+    library's plain copy kernel moving the step's matrix bytes (best of a
+    few launch shapes), and its empty kernel, alone and on a full wave."""
+    out = {}
+    if work.op in COPY_FLOOR_OPS:
+        best = None
+        for threads in (256, 512, 1024):
+            for unroll in (2, 4, 8):
+                us = quick_us(CopyProbe(work, threads, unroll))
+                if best is None or us < best[0]:
+                    best = (us, threads, unroll)
+        us, threads, unroll = best
+        out["copy_us"] = quick_us(CopyProbe(work, threads, unroll), rounds=5,
+                                  min_round_s=0.03)
+        out["copy_bytes"] = CopyProbe(work).bytes
+        out["copy_shape"] = f"{threads} threads, {unroll} in flight, one wave"
+    out["empty_us"] = quick_us(EmptyProbe(32, 1), rounds=5, min_round_s=0.03)
+    out["empty_wave_us"] = quick_us(EmptyProbe(512, 0), rounds=5,
+                                    min_round_s=0.03)
+    return out
+
+
+def build_headline(f):
+    """The headline line from the raw figures of a run (a dict: shape and
+    steps, bytes per step, elapsed seconds, peak, plan, traffic, per-round
+    µs, floor, e2e and link seconds, clock summary, pool, CPU baseline)."""
+    per_step = f["elapsed"] / f["steps"]
+    achieved = f["bytes"] / per_step / 1e9
+    peak = f["peak"]
+    moved = f["h2d"] + f["d2h"]
+    e2e_us = f["e2e_el"] / f["e2e_steps"] * 1e6
+    link_gbs = moved * f["e2e_steps"] / f["link_el"] / 1e9
+    rounds = f["rounds"]
+    line = {
+        "metric": METRIC,
+        "value": sig(f["world"] * achieved), "unit": "GB/s",
+        "n_gpus": f["world"], "steps": f["steps"], "warmup": f["warmup"],
+        "ms_per_step": sig(per_step * 1e3), "us_per_op": sig(per_step * 1e6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "storage": f["dtype"], "data": "synthetic",
+        "config": {
+            "workload": f"{f['op']} {f['dtype']} {f['rows']}x{f['cols']}, "
+                        f"{INPUT_RECIPE[f['op']]}",
+            "op": f["op"], "storage": f["dtype"], "rows": f["rows"],
+            "cols": f["cols"], "plan": f["plan"],
+            "l2": f"inputs larger than L2: {f['pool_sets']}-set rotating "
+                  f"pool, {f['pool_bytes'] / 2**20:.0f} MiB >= 4x L2",
+            "parallelism": "replicas" if f["world"] > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": sig(achieved),
+                     "peak": peak, "unit": "GB/s",
+                     "frac": sig(sig(achieved) / peak),
+                     "traffic": f["traffic"], "peak_source": f["peak_kind"]},
+        "rounds_us": {"median": sig(statistics.median(rounds), 4),
+                      "min": sig(min(rounds), 4), "max": sig(max(rounds), 4),
+                      "n": len(rounds)},
+        "e2e": {"value": sig(f["bytes"] / (e2e_us * 1e3)), "unit": "GB/s",
+                "h2d_bytes_per_step": f["h2d"],
+                "d2h_bytes_per_step": f["d2h"],
+                "us_per_step": sig(e2e_us), "link_gbs": sig(link_gbs),
+                "frac": sig(moved / (sig(e2e_us) * 1e3) / sig(link_gbs))},
+        "gpu_launches": f["steps"] * f["launches_per_step"],
+        "clocks": f["clocks"],
+    }
+    fl = f["floor"]
+    line["floor"] = {"empty_us": sig(fl["empty_us"], 4)}
+    if "copy_us" in fl:
+        line["floor"] = {
+            "copy_us": sig(fl["copy_us"], 4),
+            "copy_frac": sig(fl["copy_bytes"] / fl["copy_us"] / 1e3 / peak,
+                             4),
+            "frac_of_copy": sig(fl["copy_us"] / (per_step * 1e6), 4),
+            "empty_us": sig(fl["empty_us"], 4)}
+    cb = f.get("cpu")
+    if cb:
+        line["cpu_baseline"] = {k: (sig(cb[k], 4) if k == "value" else cb[k])
+                                for k in ("value", "unit", "cores", "kind",
+                                          "sample", "cpu")}
+    return line
 
 
 def run_ours(args, rank, world, local_rank):
@@ -363,84 +500,82 @@ def run_ours(args, rank, world, local_rank):
                                barrier=barrier, sampler=sampler)
     if world > 1:
         elapsed = max_over_ranks(elapsed, "cuda")
-    per_step = elapsed / args.steps
-    value = job_value(work.bytes, args.steps, elapsed, world)
     if rank != 0:
         return 0
 
     peak, peak_kind = measured_peak()
     key = f"{args.op}_{args.dtype}_{args.rows}x{args.cols}"
     plan = plan_text(args.op, args.rows, args.cols, args.dtype)
-    achieved = work.bytes / per_step / 1e9
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak,
-                "unit": "GB/s", "frac": achieved / peak,
-                "traffic": profiled_traffic(key, args.op, plan, args.dtype),
-                "peak_source": f"{peak_kind} HBM copy bandwidth "
-                               "(MEASURED_PEAKS.json hbm_gbs)"
-                if peak_kind == "measured" else "fallback 6.8 TB/s",
-                "datasheet_frac": achieved / DATASHEET_HBM_GBS,
-                "datasheet_peak": DATASHEET_HBM_GBS}
-
-    plain = time_plain_steps(work, min(args.steps, 20000),
-                             min(args.warmup, 200))
-    plain_steps = min(args.steps, 20000)
+    rounds = time_rounds(work, rounds=5, min_round_s=0.03)
+    floor = measure_floor(work)
     e2e_steps = max(3, min(args.steps, 200))
     e2e_el, bi, bo = time_e2e(work, e2e_steps, 3, depth=3)
+    link_el = time_link(bi, bo, e2e_steps, 3, depth=3)
+    fig = {"op": args.op, "dtype": args.dtype, "rows": args.rows,
+           "cols": args.cols, "steps": args.steps, "warmup": args.warmup,
+           "world": world, "bytes": work.bytes, "elapsed": elapsed,
+           "peak": peak, "peak_kind": peak_kind, "plan": plan,
+           "traffic": profiled_traffic(key, args.op, plan, args.dtype),
+           "rounds": rounds, "floor": floor, "e2e_el": e2e_el,
+           "e2e_steps": e2e_steps, "h2d": bi, "d2h": bo, "link_el": link_el,
+           "clocks": sampler.summary(), "pool_sets": len(work.sets),
+           "pool_bytes": work.pool_bytes,
+           "launches_per_step": work.launches_per_step, "cpu": None}
+    line = build_headline(fig)
+    details = {"headline": line, "floor": floor,
+               "rounds_us": rounds, "e2e_serial_us_per_step": None}
     serial_el, _, _ = time_e2e(work, e2e_steps, 3, depth=1)
-    e2e = {"value": work.bytes * e2e_steps / e2e_el / 1e9, "unit": "GB/s",
-           "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-           "us_per_step": e2e_el / e2e_steps * 1e6,
-           "method": "each step uploads x from pinned host memory, calls "
-                     "the library and downloads its result; three streams "
-                     "and buffer sets take turns, so one step's upload "
-                     "overlaps earlier steps' kernels and downloads",
-           "serial_us_per_step": serial_el / e2e_steps * 1e6}
-    rounds = time_rounds(work, rounds=4, min_round_s=0.03)
-
-    line = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": per_step * 1e3, "us_per_op": per_step * 1e6,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic",
-        "config": {
-            "workload": f"{args.op}_{args.dtype} rows={args.rows} "
-                        f"cols={args.cols}, {INPUT_RECIPE[args.op]}",
-            "op": args.op, "storage": args.dtype, "rows": args.rows,
-            "cols": args.cols, "plan": plan,
-            "l2": f"inputs larger than L2: rotating pool of "
-                  f"{len(work.sets)} buffer sets, "
-                  f"{work.pool_bytes / 2**20:.0f} MiB >= 4x L2 "
-                  f"({l2 / 2**20:.0f} MiB)",
-            "timing": "CUDA graphs of captured library calls, back to back "
-                      "on one stream, CUDA events",
-            "parallelism": "replicas" if world > 1 else "single GPU"},
-        "roofline": roofline,
-        "e2e": e2e,
-        "gpu_launches": args.steps * work.launches_per_step,
-        "clocks": sampler.summary(),
-        "plain_launch": {"value": work.bytes * plain_steps / plain / 1e9,
-                         "unit": "GB/s",
-                         "us_per_op": plain / plain_steps * 1e6,
-                         "steps": plain_steps,
-                         "note": "one Python ctypes call per step"},
-        "rounds": {"us_per_op_median": statistics.median(rounds),
-                   "us_per_op_min": min(rounds), "us_per_op_max": max(rounds),
-                   "rounds": len(rounds), "samples_us": rounds,
-                   "note": "graph replays over the same pool, each round "
-                           ">= 30 ms"},
-    }
+    details["e2e_serial_us_per_step"] = serial_el / e2e_steps * 1e6
+    plain_steps = min(args.steps, 20000)
+    plain = time_plain_steps(work, plain_steps, min(args.warmup, 200))
+    details["plain_launch"] = {"us_per_op": plain / plain_steps * 1e6,
+                               "note": "one Python ctypes call per step"}
     if world == 1:
-        line["hot"] = hot_number(args, l2)
-        line["torch_context"] = torch_context(work)
+        details["hot"] = hot_number(args, l2)
+        details["torch_context"] = torch_context(work)
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.op, work.host, args.rows,
-                                            args.cols, args.cpu_seconds,
-                                            args.dtype)
+        cb = cpu_baseline(args.op, work.host, args.rows, args.cols,
+                          args.cpu_seconds, args.dtype)
+        details["cpu_baseline"] = cb
+        fig["cpu"] = cb
+        line = build_headline(fig)
+        details["headline"] = line
     if world == 1 and not args.no_sweep:
-        line["sweep"] = run_sweep(l2, peak)
-    print(json.dumps(line))
+        details["sweep"] = run_sweep(l2, peak)
+    print_details(details, peak)
+    if args.details:
+        with open(args.details, "w") as f:
+            json.dump(details, f, indent=1)
+    emit_headline(line)
     return 0
+
+
+def print_details(d, peak):
+    """A human-readable summary of the details on stderr."""
+    err = sys.stderr
+    fl = d["floor"]
+    print("== floor (same pool, graph replays of dependent launches)",
+          file=err)
+    for k, v in fl.items():
+        print(f"   {k}: {v}", file=err)
+    print(f"== e2e serial (one stream): "
+          f"{d['e2e_serial_us_per_step']:.2f} us/step", file=err)
+    print(f"== plain Python launches: {d['plain_launch']['us_per_op']:.3f} "
+          "us/op", file=err)
+    for k in ("hot", "torch_context"):
+        if d.get(k):
+            print(f"== {k}: {json.dumps(d[k])}", file=err)
+    if d.get("cpu_baseline"):
+        print(f"== cpu_baseline: {json.dumps(d['cpu_baseline'])}", file=err)
+    if d.get("sweep"):
+        print("== sweep: op dtype rows x cols | us/op | GB/s | % of "
+              f"{peak:.0f} | plan", file=err)
+        for r in d["sweep"]:
+            tag = "" if r.get("mean", True) else " (loss only)"
+            print(f"   {r['op']}{tag} {r['dtype']} {r['rows']}x{r['cols']}"
+                  f" | {r['us_per_op']:.3f} | {r['gbs']:.0f} | "
+                  f"{100 * r['frac_of_peak']:.1f} | {r['plan']}", file=err)
+    err.flush()
 
 
 def hot_number(args, l2):
@@ -514,25 +649,37 @@ def torch_context(work):
             "note": "PyTorch's own kernel on the same pool; context only"}
 
 
-def run_sweep(l2, peak):
+def sweep_cases():
     """Every published shape: RMSNorm shapes and bandwidth sweep, then the
-    operator family, each timed like the headline; then the same RMSNorm
-    sweep and the family at 1024x4096 with BF16 and FP16 storage."""
+    operator family (cross-entropy with its mean and with the per-row losses
+    alone); then the same RMSNorm sweep and the family at 1024x4096 with
+    BF16 and FP16 storage.  Entries: (op, rows, cols, outliers, dtype,
+    with the CE mean)."""
     from row_reduction_gb300 import inputs
-    cases = [("rmsnorm", r, c, False, "f32") for r, c in inputs.RMSNORM_SHAPES]
-    cases += [("rmsnorm", r, c, True, "f32") for r, c in inputs.RMSNORM_SWEEP]
-    cases += [(op, r, c, False, "f32") for op in inputs.ALL_OPS
+    cases = [("rmsnorm", r, c, False, "f32", True)
+             for r, c in inputs.RMSNORM_SHAPES]
+    cases += [("rmsnorm", r, c, True, "f32", True)
+              for r, c in inputs.RMSNORM_SWEEP]
+    cases += [(op, r, c, False, "f32", True) for op in inputs.ALL_OPS
               if op != "rmsnorm" for r, c in inputs.FAMILY_SHAPES]
+    cases.append(("cross_entropy", 1024, 4096, False, "f32", False))
     for dt in ("bf16", "f16"):
-        cases += [("rmsnorm", r, c, True, dt)
+        cases += [("rmsnorm", r, c, True, dt, True)
                   for r, c in inputs.RMSNORM_SWEEP]
-        cases += [(op, 1024, 4096, False, dt) for op in inputs.ALL_OPS
+        cases += [(op, 1024, 4096, False, dt, True) for op in inputs.ALL_OPS
                   if op != "rmsnorm"]
-    out = []
+        cases.append(("cross_entropy", 1024, 4096, False, dt, False))
+    return cases
+
+
+def run_sweep(l2, peak):
     import torch
-    for op, r, c, outl, dt in cases:
+    from row_reduction_gb300 import inputs
+    out = []
+    for op, r, c, outl, dt, mean in sweep_cases():
         work = Workload(op, r, c, inputs.TUNE_SEED, outliers=outl,
-                        l2_bytes=l2, max_pool_bytes=8 << 30, dtype=dt)
+                        l2_bytes=l2, max_pool_bytes=8 << 30, dtype=dt,
+                        ce_mean=mean)
         # about 0.25 s of timed work, at least 64 steps
         probe = time_graph_steps(work, 64, 16)
         steps = int(max(64, min(200000, 0.25 / max(probe / 64, 1e-7))))
@@ -540,8 +687,8 @@ def run_sweep(l2, peak):
         us = el / steps * 1e6
         gbs = work.bytes / (el / steps) / 1e9
         out.append({"op": op, "dtype": dt, "rows": r, "cols": c,
-                    "outliers": outl, "us_per_op": us, "gbs": gbs,
-                    "frac_of_peak": gbs / peak,
+                    "outliers": outl, "mean": mean, "us_per_op": us,
+                    "gbs": gbs, "frac_of_peak": gbs / peak,
                     "plan": plan_text(op, r, c, dt),
                     "pool_sets": len(work.sets),
                     "l2_resident": work.l2_resident, "steps": steps})
@@ -551,13 +698,14 @@ def run_sweep(l2, peak):
 
 
 def verify_line(line):
-    """Audits one JSON line of this benchmark: the reported figures
-    recomputed from the raw ones (steps, time, bytes, samples), and the
-    recorded plan against the planner's current choice.  Returns a list of
-    problems (empty when the line is consistent)."""
+    """Audits one headline JSON line of this benchmark: the reported figures
+    recomputed from the raw ones (steps, time, bytes), and the recorded plan
+    against the planner's current choice.  Returns a list of problems
+    (empty when the line is consistent).  Figures in the line carry six
+    significant digits, so they are compared to within 1e-5."""
     bad = []
 
-    def close(a, b, what, rel=1e-6):
+    def close(a, b, what, rel=1e-5):
         if a is None or b is None or abs(a - b) > rel * max(abs(b), 1e-30):
             bad.append(f"{what}: {a} vs {b}")
 
@@ -575,12 +723,17 @@ def verify_line(line):
     roof = line["roofline"]
     close(roof["achieved"], b / per_step / 1e9, "roofline.achieved")
     close(roof["frac"], roof["achieved"] / roof["peak"], "roofline.frac")
-    r = line.get("rounds")
-    if r and "samples_us" in r:
-        s = r["samples_us"]
-        close(r["us_per_op_median"], statistics.median(s), "rounds median")
-        close(r["us_per_op_min"], min(s), "rounds min")
-        close(r["us_per_op_max"], max(s), "rounds max")
+    r = line.get("rounds_us")
+    if r and not r["min"] <= r["median"] <= r["max"]:
+        bad.append(f"rounds_us: median {r['median']} outside "
+                   f"[{r['min']}, {r['max']}]")
+    e = line.get("e2e")
+    if e and "link_gbs" in e:
+        moved = e["h2d_bytes_per_step"] + e["d2h_bytes_per_step"]
+        close(e["frac"], moved / (e["us_per_step"] * 1e3) / e["link_gbs"],
+              "e2e.frac", rel=1e-4)
+        close(e["value"], b / (e["us_per_step"] * 1e3), "e2e.value",
+              rel=1e-4)
     if cfg["plan"] != plan_text(op, rows, cols, dtype):
         bad.append(f"plan: recorded {cfg['plan']!r}, planner now "
                    f"{plan_text(op, rows, cols, dtype)!r}")
@@ -602,6 +755,9 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--details", metavar="FILE", default=None,
+                    help="also write every figure (sweep, floor, hot, "
+                         "context) to FILE as JSON")
     ap.add_argument("--verify", metavar="FILE", default=None,
                     help="audit the JSON line(s) in FILE instead of timing")
     args = ap.parse_args()

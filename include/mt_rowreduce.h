@@ -398,6 +398,28 @@ MT_API int64_t mt_private_slot_bound(int64_t n, int32_t W, int32_t V);
  * excluding the NUL (snprintf convention). */
 MT_API size_t mt_describe_plan(const mt_plan_t *plan, char *buf, size_t n);
 
+/* ---- measurement aids ----------------------------------------------------
+ * Not operators, and the pages have no counterpart: they give the floor a
+ * row-reduction launch is measured against.  Both launch like the
+ * operators, as programmatic dependents of the previous kernel on the stream
+ * (MT_PLAN_PDL), so a chain of them is timed the way a chain of operator
+ * calls is.  threads: CTA size, a multiple of 32 in [32, 1024]; grid: CTAs
+ * to launch, 0 = one wave (SMs x CTAs resident per SM).  They allocate
+ * nothing and never synchronise. */
+
+/* Copies `bytes` bytes from src to dst (device pointers, both 16-byte
+ * aligned, bytes a multiple of 16, the two ranges disjoint) with 16-byte
+ * loads and stores: the grid's threads stride over the 16-byte words and
+ * each keeps `unroll` (1, 2, 4 or 8) loads in flight.  bytes == 0 is a
+ * no-op.  Bad arguments give MT_ERR_INVALID_ARGUMENT and enqueue nothing. */
+MT_API mt_status mt_probe_copy(const void *src, void *dst, int64_t bytes,
+                               int32_t threads, int32_t unroll, int32_t grid,
+                               mt_stream_t stream);
+
+/* A kernel that does no work: the fixed cost of one dependent launch. */
+MT_API mt_status mt_probe_empty(int32_t threads, int32_t grid,
+                                mt_stream_t stream);
+
 /* Static string naming a status. */
 MT_API const char *mt_status_string(mt_status status);
 

@@ -70,6 +70,7 @@ EXPORTS = (
     "mt_log_softmax_f16", "mt_log_softmax_bf16",
     "mt_cross_entropy_ignore_f32", "mt_cross_entropy_ignore_f16",
     "mt_cross_entropy_ignore_bf16",
+    "mt_probe_copy", "mt_probe_empty",
 )
 
 
@@ -157,6 +158,8 @@ def lib() -> ctypes.CDLL:
                 "mt_plan_query_dtype": [ctypes.c_int, ctypes.c_int, I64, I64,
                                         PP],
                 "mt_plan_check_dtype": [ctypes.c_int, ctypes.c_int, I64, PP],
+                "mt_probe_copy": [P, P, I64, I32, I32, I32, P],
+                "mt_probe_empty": [I32, I32, P],
             }
             for dt in ("f16", "bf16"):
                 sig.update({
@@ -460,3 +463,28 @@ mt_status_string = status_string
 
 def mt_last_cuda_error() -> int:
     return lib().mt_last_cuda_error()
+
+
+def mt_probe_copy(src, dst, nbytes, threads=512, unroll=4, grid=0,
+                  stream=None):
+    """Measurement aid: a plain 16-byte-vector copy of `nbytes` bytes."""
+    _check(lib().mt_probe_copy(_ptr(src, "src", _any_dtype(src)),
+                               _ptr(dst, "dst", _any_dtype(dst)), nbytes,
+                               threads, unroll, grid, _stream(stream)),
+           "mt_probe_copy")
+
+
+def mt_probe_empty(threads=32, grid=1, stream=None):
+    """Measurement aid: a dependent launch that does no work."""
+    _check(lib().mt_probe_empty(threads, grid, _stream(stream)),
+           "mt_probe_empty")
+
+
+def _any_dtype(t):
+    """The storage name of a tensor argument (any of the library's types),
+    so _ptr's checks apply without constraining the type."""
+    if t is None or isinstance(t, int):
+        return "float32"
+    import torch
+    return {torch.float32: "f32", torch.float16: "f16",
+            torch.bfloat16: "bf16", torch.int32: "int32"}[t.dtype]

@@ -24,7 +24,7 @@ HEADER = os.path.join(ROOT, "include", "mt_rowreduce.h")
 OPS = ("rmsnorm", "layernorm", "residual_layernorm", "softmax", "row_sum",
        "cross_entropy", "residual_rmsnorm", "log_softmax")
 DTYPES = ("f32", "f16", "bf16")
-SOURCES = (["api.cpp", "planner.cpp", "mean.cu"] +
+SOURCES = (["api.cpp", "planner.cpp", "mean.cu", "probe.cu"] +
            [f"ops_{op}_{dt}.cu" for op in OPS for dt in DTYPES])
 DEPENDS = ["mt_internal.h", "mt_kernels.cuh", "plan_table.inc"]
 

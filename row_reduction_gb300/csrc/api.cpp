@@ -6,21 +6,47 @@
 #include <atomic>
 #include <mutex>
 #include <unordered_map>
+#include <unordered_set>
 
 #include "mt_internal.h"
 
 namespace mt {
 namespace {
-
 thread_local int g_last_cuda_error = 0;
+}  // namespace
 
-mt_status cuda_status(cudaError_t e) {
+mt_status status_from_cuda(cudaError_t e) {
     if (e == cudaSuccess) return MT_OK;
     (void)cudaGetLastError();  // do not leave the error for the caller
     g_last_cuda_error = (int)e;
     return e == cudaErrorLaunchOutOfResources ? MT_ERR_OUT_OF_RESOURCES
                                               : MT_ERR_CUDA;
 }
+
+// Kernels that have been allowed clusters beyond the portable size, per
+// device: the attribute is set once per (device, kernel), not per launch.
+namespace {
+std::mutex g_nonportable_mu;
+std::unordered_set<uint64_t> g_nonportable;
+}  // namespace
+
+cudaError_t allow_nonportable_cluster(const void *kernel) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t key = (reinterpret_cast<uintptr_t>(kernel) << 8) ^
+                         (uint64_t)(dev & 0xff);
+    std::lock_guard<std::mutex> lk(g_nonportable_mu);
+    if (g_nonportable.count(key)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel,
+                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e == cudaSuccess) g_nonportable.insert(key);
+    return e;
+}
+
+namespace {
+
+mt_status cuda_status(cudaError_t e) { return status_from_cuda(e); }
 
 bool misaligned(const void *p, int bytes) {
     return (reinterpret_cast<uintptr_t>(p) & (uintptr_t)(bytes - 1)) != 0;

@@ -105,6 +105,16 @@ cudaError_t launch_mean(const float *loss, float *mean, int64_t rows,
                         const int32_t *labels, int32_t ignore_index,
                         int32_t has_ignore, cudaStream_t stream);
 
+// MT_OK for cudaSuccess; otherwise records e as the calling thread's last
+// CUDA error (mt_last_cuda_error), clears it and returns MT_ERR_CUDA (or
+// MT_ERR_OUT_OF_RESOURCES for a launch out of resources).
+mt_status status_from_cuda(cudaError_t e);
+
+// Lets `kernel` launch with clusters beyond the portable size (16 CTAs) on
+// the current device.  The attribute is set on the first call for each
+// (device, kernel) and remembered, so later launches make no driver call.
+cudaError_t allow_nonportable_cluster(const void *kernel);
+
 // Planner (planner.cpp).
 mt_status plan_lookup(int op, int dtype, int64_t rows, int64_t cols,
                       mt_plan_t *out);

@@ -1331,9 +1331,8 @@ __host__ cudaError_t launch_op(const mt_plan_t &p, const KArgs &a,
     }
     if (a.csize > 8) {
         // 16 CTAs per cluster is beyond the portable size of 8.
-        if (cudaError_t e = cudaFuncSetAttribute(
-                reinterpret_cast<const void *>(k),
-                cudaFuncAttributeNonPortableClusterSizeAllowed, 1))
+        if (cudaError_t e =
+                allow_nonportable_cluster(reinterpret_cast<const void *>(k)))
             return e;
     }
     if (a.csize > 1) {

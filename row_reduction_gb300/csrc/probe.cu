@@ -1,0 +1,130 @@
+// probe.cu -- measurement aids: a plain vectorised device-to-device copy and
+// an empty kernel.  Both launch the way the row-reduction kernels do (as
+// programmatic dependents of the previous kernel on the stream, one wave of
+// resident CTAs), so a benchmark can put a row-reduction launch beside the
+// floor of a launch that moves the same bytes with no arithmetic, or no
+// bytes at all, timed by the same method on the same buffers.
+#include "mt_kernels.cuh"
+
+namespace mt {
+
+// Copies n 16-byte words from src to dst.  The grid's T threads stride over
+// the words; each thread keeps U loads in flight before it stores them.
+template <int U>
+__global__ void __launch_bounds__(1024)
+    probe_copy_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst,
+                      int64_t n) {
+    grid_launch_dependents();
+    grid_wait_prerequisites();
+    const int64_t T = (int64_t)gridDim.x * blockDim.x;
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; i + (int64_t)(U - 1) * T < n; i += (int64_t)U * T) {
+        uint4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) v[u] = src[i + u * T];
+#pragma unroll
+        for (int u = 0; u < U; ++u) dst[i + u * T] = v[u];
+    }
+    for (; i < n; i += T) dst[i] = src[i];
+}
+
+// Does nothing but take part in the dependent-launch chain.
+__global__ void __launch_bounds__(1024) probe_empty_kernel() {
+    grid_launch_dependents();
+    grid_wait_prerequisites();
+}
+
+namespace {
+
+typedef void (*CopyFn)(const uint4 *, uint4 *, int64_t);
+
+CopyFn copy_kernel_for(int unroll) {
+    switch (unroll) {
+        case 1: return probe_copy_kernel<1>;
+        case 2: return probe_copy_kernel<2>;
+        case 4: return probe_copy_kernel<4>;
+        case 8: return probe_copy_kernel<8>;
+    }
+    return nullptr;
+}
+
+cudaError_t launch_pdl(const void *fn, int grid, int threads, void **args,
+                       cudaStream_t stream) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+// grid == 0: every CTA the device holds at once (SMs x resident CTAs).
+cudaError_t resolve_grid(const void *fn, int threads, int *grid) {
+    if (*grid > 0) return cudaSuccess;
+    int dev = 0, sms = 0, bps = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, fn, threads,
+                                                          0);
+    if (e != cudaSuccess) return e;
+    *grid = sms * (bps > 0 ? bps : 1);
+    return cudaSuccess;
+}
+
+bool bad_block(int threads) {
+    return threads < 32 || threads > 1024 || threads % 32 != 0;
+}
+
+}  // namespace
+}  // namespace mt
+
+using namespace mt;
+
+extern "C" {
+
+mt_status mt_probe_copy(const void *src, void *dst, int64_t bytes,
+                        int32_t threads, int32_t unroll, int32_t grid,
+                        mt_stream_t stream) {
+    if (bytes < 0 || bytes % 16 != 0 || bad_block(threads) || grid < 0)
+        return MT_ERR_INVALID_ARGUMENT;
+    CopyFn fn = copy_kernel_for(unroll);
+    if (fn == nullptr) return MT_ERR_INVALID_ARGUMENT;
+    if (bytes == 0) return MT_OK;
+    if (src == nullptr || dst == nullptr ||
+        (reinterpret_cast<uintptr_t>(src) & 15) != 0 ||
+        (reinterpret_cast<uintptr_t>(dst) & 15) != 0)
+        return MT_ERR_INVALID_ARGUMENT;
+    const char *s = static_cast<const char *>(src);
+    char *d = static_cast<char *>(dst);
+    if (s < d + bytes && d < s + bytes) return MT_ERR_INVALID_ARGUMENT;
+    int g = grid;
+    cudaError_t e =
+        resolve_grid(reinterpret_cast<const void *>(fn), threads, &g);
+    if (e == cudaSuccess) {
+        const uint4 *sp = static_cast<const uint4 *>(src);
+        uint4 *dp = static_cast<uint4 *>(dst);
+        int64_t n = bytes / 16;
+        void *args[] = {&sp, &dp, &n};
+        e = launch_pdl(reinterpret_cast<const void *>(fn), g, threads, args,
+                       (cudaStream_t)stream);
+    }
+    return status_from_cuda(e);
+}
+
+mt_status mt_probe_empty(int32_t threads, int32_t grid, mt_stream_t stream) {
+    if (bad_block(threads) || grid < 0) return MT_ERR_INVALID_ARGUMENT;
+    const void *fn = reinterpret_cast<const void *>(probe_empty_kernel);
+    int g = grid;
+    cudaError_t e = resolve_grid(fn, threads, &g);
+    if (e == cudaSuccess)
+        e = launch_pdl(fn, g, threads, nullptr, (cudaStream_t)stream);
+    return status_from_cuda(e);
+}
+
+}  // extern "C"

@@ -63,7 +63,7 @@ class Workload:
 
     def __init__(self, op, rows, cols, seed, outliers=False,
                  l2_bytes=126 << 20, max_pool_bytes=16 << 30, data=None,
-                 dtype="f32"):
+                 dtype="f32", ce_mean=True):
         import torch
         self.op, self.rows, self.cols, self.dtype = op, rows, cols, dtype
         d = data if data is not None else inputs.make(op, rows, cols, seed,
@@ -71,7 +71,9 @@ class Workload:
         d = inputs.as_storage(d, dtype)
         self.host = d
         self.eps = float(d.get("eps", 0.0))
-        self.mean = op == "cross_entropy"
+        # Cross-entropy: with the batch mean (a second, one-CTA kernel) or
+        # the per-row losses alone (mean_loss = NULL).
+        self.mean = op == "cross_entropy" and ce_mean
         self.h_out = op in ("residual_layernorm", "residual_rmsnorm")
         self.bytes = algorithmic_bytes(op, rows, cols, self.h_out, self.mean,
                                        dtype)
@@ -98,7 +100,8 @@ class Workload:
                 s["out"] = torch.empty(rows, device="cuda")
             if op == "cross_entropy":
                 s["loss"] = torch.empty(rows, device="cuda")
-                s["mean_loss"] = torch.empty(1, device="cuda")
+                if self.mean:
+                    s["mean_loss"] = torch.empty(1, device="cuda")
             self.sets.append(s)
         del x0
         self.pool_bytes = n * set_bytes
@@ -176,11 +179,37 @@ def graph_size(work, per_graph=64):
     return n * max(1, math.ceil(per_graph / n))
 
 
+def _replay_for(graph, stream, seconds, until=None, max_seconds=5.0):
+    """Replays `graph` on `stream` for about `seconds` (and, when `until` is
+    given, until it returns True or `max_seconds` have passed)."""
+    import time
+    import torch
+    t0 = time.perf_counter()
+    while True:
+        with torch.cuda.stream(stream):
+            graph.replay()
+        stream.synchronize()
+        el = time.perf_counter() - t0
+        if el >= max_seconds:
+            return
+        if el >= seconds and (until is None or until()):
+            return
+
+
 def time_graph_steps(work, steps, warmup, plan=None, per_graph=64,
-                     barrier=None, sampler=None):
-    """Device seconds for exactly `steps` steps (after `warmup` steps),
-    replayed from CUDA graphs.  `sampler` (a context manager) runs around
-    the timed region; `barrier` is called before and after it."""
+                     barrier=None, sampler=None, load_s=0.3):
+    """Device seconds for exactly `steps` steps (after at least `warmup`
+    steps), replayed from CUDA graphs.
+
+    The timed region is bracketed by a synchronize (and `barrier`, when
+    given) on both sides.  After the first synchronize one untimed replay is
+    enqueued ahead of the start event, so the GPU is busy while the host
+    enqueues the timed replays: the start event then marks the first timed
+    step, not the host's graph-launch latency.  With `sampler` (an object
+    with start(), stop() and has_samples(n)), the GPU also runs the same steps
+    for `load_s` seconds before and after the timed region (before: until
+    the sampler holds at least two samples), so clock samples are taken
+    under the timed load."""
     import torch
     stream = torch.cuda.Stream()
     h = stream.cuda_stream
@@ -196,24 +225,30 @@ def time_graph_steps(work, steps, warmup, plan=None, per_graph=64,
         for _ in range(max(1, math.ceil(warmup / G))):
             full.replay()
     stream.synchronize()
+    if sampler is not None:
+        sampler.start()
+        _replay_for(full, stream, load_s,
+                    until=lambda: sampler.has_samples(2))
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     if barrier:
         barrier()
-    ctx = sampler if sampler is not None else _Null()
-    with ctx:
-        with torch.cuda.stream(stream):
-            start.record(stream)
-            for _ in range(steps // G):
-                full.replay()
-            if tail is not None:
-                tail.replay()
-            end.record(stream)
-        end.synchronize()
+    with torch.cuda.stream(stream):
+        full.replay()                   # untimed spacer
+        start.record(stream)
+        for _ in range(steps // G):
+            full.replay()
+        if tail is not None:
+            tail.replay()
+        end.record(stream)
+    end.synchronize()
     torch.cuda.synchronize()
     if barrier:
         barrier()
+    if sampler is not None:
+        _replay_for(full, stream, load_s)
+        sampler.stop()
     return start.elapsed_time(end) / 1e3
 
 
@@ -252,12 +287,50 @@ def time_rounds(work, plan=None, rounds=5, min_round_s=0.01, per_graph=64):
     return out
 
 
-class _Null:
-    def __enter__(self):
-        return self
+class CopyProbe:
+    """The library's plain copy kernel (mt_probe_copy) over a workload's own
+    buffer pool: step i copies set i's x to its y, the same bytes in and out
+    as one RMSNorm or softmax step (without the parameter vector).  Timed
+    like a workload, it is the floor of a launch that moves those bytes."""
 
-    def __exit__(self, *a):
-        return False
+    def __init__(self, work, threads=512, unroll=4, grid=0):
+        self.work, self.sets = work, work.sets
+        self.threads, self.unroll, self.grid = threads, unroll, grid
+        x0 = work.sets[0]["x"]
+        self.nbytes = x0.numel() * x0.element_size()
+        self.bytes = 2 * self.nbytes
+
+    def call_fn(self, i, stream_handle, plan=None):
+        L = B.lib()
+        s = self.sets[i % len(self.sets)]
+        args = (s["x"].data_ptr(), s["y"].data_ptr(), self.nbytes,
+                self.threads, self.unroll, self.grid, stream_handle)
+
+        def go():
+            rc = L.mt_probe_copy(*args)
+            if rc != 0:
+                raise B.MTError(rc, "mt_probe_copy")
+        return go
+
+
+class EmptyProbe:
+    """The library's empty kernel (mt_probe_empty): a chain of dependent
+    launches that move nothing, the fixed cost of one step."""
+
+    def __init__(self, threads=32, grid=1):
+        self.sets = [None]
+        self.threads, self.grid = threads, grid
+        self.bytes = 0
+
+    def call_fn(self, i, stream_handle, plan=None):
+        L = B.lib()
+        args = (self.threads, self.grid, stream_handle)
+
+        def go():
+            rc = L.mt_probe_empty(*args)
+            if rc != 0:
+                raise B.MTError(rc, "mt_probe_empty")
+        return go
 
 
 def time_plain_steps(work, steps, warmup):
@@ -336,3 +409,47 @@ def time_e2e(work, steps, warmup, depth=1):
     return (start.elapsed_time(end) / 1e3,
             x_host.numel() * x_host.element_size(),
             outs[0].numel() * outs[0].element_size())
+
+
+def time_link(h2d_bytes, d2h_bytes, steps, warmup, depth=3):
+    """The host link alone: each step copies `h2d_bytes` from pinned host
+    memory to the device and `d2h_bytes` from the device to pinned host
+    memory, with the same rotation over `depth` streams and buffers as
+    :func:`time_e2e` (so the two directions overlap on their copy engines).
+    Returns seconds for `steps` steps: the ceiling an end-to-end step that
+    moves those bytes can reach."""
+    import torch
+    depth = max(1, depth)
+    n_in, n_out = max(1, h2d_bytes), max(1, d2h_bytes)
+    h_in = torch.empty(n_in, dtype=torch.uint8, pin_memory=True)
+    h_out = [torch.empty(n_out, dtype=torch.uint8, pin_memory=True)
+             for _ in range(depth)]
+    d_in = [torch.empty(n_in, dtype=torch.uint8, device="cuda")
+            for _ in range(depth)]
+    d_out = [torch.empty(n_out, dtype=torch.uint8, device="cuda")
+             for _ in range(depth)]
+    streams = [torch.cuda.Stream() for _ in range(depth)]
+
+    def step(k):
+        b = k % depth
+        with torch.cuda.stream(streams[b]):
+            d_in[b].copy_(h_in, non_blocking=True)
+            h_out[b].copy_(d_out[b], non_blocking=True)
+
+    for k in range(max(warmup, depth)):
+        step(k)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    done = [torch.cuda.Event() for _ in range(depth)]
+    start.record(streams[0])
+    for st in streams[1:]:
+        st.wait_event(start)
+    for k in range(steps):
+        step(k)
+    for b in range(1, depth):
+        done[b].record(streams[b])
+        streams[0].wait_event(done[b])
+    end.record(streams[0])
+    end.synchronize()
+    return start.elapsed_time(end) / 1e3

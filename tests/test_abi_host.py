@@ -33,7 +33,7 @@ def header_symbols():
 
 def test_library_exports_every_declared_symbol():
     declared = header_symbols()
-    assert len(declared) == 44
+    assert len(declared) == 46
     L = mt.lib()
     for name in declared:
         assert hasattr(L, name), name
@@ -212,6 +212,23 @@ def test_invalid_arguments_are_rejected_before_launch():
     assert L.mt_row_sum_f32(A, None, 4, 4, None) == INV
     assert L.mt_cross_entropy_f32(A, None, A, None, 4, 4, None) == INV
     assert L.mt_cross_entropy_f32(A, A, A, A + 2, 4, 4, None) == INV
+
+
+def test_probe_arguments_are_rejected_before_launch():
+    """The measurement aids check their arguments before any CUDA call."""
+    L = mt.lib()
+    assert L.mt_probe_copy(A, A + 4096, 4095, 512, 4, 0, None) == INV
+    assert L.mt_probe_copy(A, A + 4096, -16, 512, 4, 0, None) == INV
+    assert L.mt_probe_copy(A, A + 4096, 4096, 500, 4, 0, None) == INV
+    assert L.mt_probe_copy(A, A + 4096, 4096, 2048, 4, 0, None) == INV
+    assert L.mt_probe_copy(A, A + 4096, 4096, 512, 3, 0, None) == INV
+    assert L.mt_probe_copy(A, A + 4096, 4096, 512, 4, -1, None) == INV
+    assert L.mt_probe_copy(A + 4, A + 4096, 4096, 512, 4, 0, None) == INV
+    assert L.mt_probe_copy(None, A, 4096, 512, 4, 0, None) == INV
+    assert L.mt_probe_copy(A, A + 2048, 4096, 512, 4, 0, None) == INV
+    assert L.mt_probe_copy(A, A + 4096, 0, 512, 4, 0, None) == OK
+    assert L.mt_probe_empty(16, 1, None) == INV
+    assert L.mt_probe_empty(32, -1, None) == INV
 
 
 def test_zero_rows_is_a_no_op():

@@ -66,33 +66,111 @@ def test_algorithmic_bytes_match_the_documented_formulas():
         4 * R * C + 2 * C
 
 
-def _line(us=5.9, plan=None):
+def _figures(us=5.9, plan=None, cpu=True):
+    """Raw figures of a run, as run_ours collects them, with long text
+    fields so the size cap is tested near its worst case."""
     import bench
     from row_reduction_gb300.timing import algorithmic_bytes
-    b = algorithmic_bytes("rmsnorm", 1024, 4096)
-    ach = b / (us * 1e-6) / 1e9
-    return {"metric": "m", "value": ach, "unit": "GB/s", "n_gpus": 1,
-            "steps": 100, "warmup": 10, "ms_per_step": us / 1e3,
-            "us_per_op": us,
-            "config": {"op": "rmsnorm", "storage": "f32", "rows": 1024,
-                       "cols": 4096,
-                       "plan": plan or bench.plan_text("rmsnorm", 1024,
-                                                       4096)},
-            "roofline": {"achieved": ach, "peak": 6783.1,
-                         "frac": ach / 6783.1},
-            "rounds": {"us_per_op_median": 5.95, "us_per_op_min": 5.9,
-                       "us_per_op_max": 6.0,
-                       "samples_us": [5.9, 5.95, 6.0]}}
+    steps = 20
+    f = {"op": "rmsnorm", "dtype": "f32", "rows": 1024, "cols": 4096,
+         "steps": steps, "warmup": 5, "world": 1,
+         "bytes": algorithmic_bytes("rmsnorm", 1024, 4096),
+         "elapsed": us * 1e-6 * steps, "peak": 6783.1,
+         "peak_kind": "measured",
+         "plan": plan or bench.plan_text("rmsnorm", 1024, 4096),
+         "traffic": 32590080, "rounds": [5.91, 5.93, 5.95, 5.97, 6.02],
+         "floor": {"copy_us": 5.71, "copy_bytes": 2 * 4 * 1024 * 4096,
+                   "empty_us": 1.31, "empty_wave_us": 1.52},
+         "e2e_el": 108e-6 * 200, "e2e_steps": 200,
+         "h2d": 16777216, "d2h": 16777216, "link_el": 101e-6 * 200,
+         "clocks": {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0,
+                    "reasons": ["sw_power_cap"], "samples": 12},
+         "pool_sets": 17, "pool_bytes": 17 * 33570816,
+         "launches_per_step": 1, "cpu": None}
+    if cpu:
+        f["cpu"] = {"value": 41.234567, "unit": "GB/s", "cores": 16,
+                    "kind": "oracle",
+                    "sample": "full 1024x4096 x123 in 5.0 s, 16 row blocks "
+                              "on 16 threads",
+                    "cpu": "Neoverse-V2 (a long model name, for the size)",
+                    "us_per_op": 812.3,
+                    "single_thread": {"value": 4.5, "unit": "GB/s"}}
+    return f
+
+
+HEADLINE_KEYS = ("metric", "value", "unit", "n_gpus", "steps", "warmup",
+                 "ms_per_step", "us_per_op", "higher_is_better", "scaling",
+                 "vs_baseline", "dtype", "data", "config", "roofline",
+                 "cpu_baseline", "e2e", "gpu_launches", "clocks",
+                 "rounds_us", "floor")
+
+
+def test_headline_fits_the_cap_and_carries_every_key():
+    import bench
+    line = bench.build_headline(_figures())
+    text = bench.headline_json(line)
+    assert len(text.encode()) <= bench.HEADLINE_MAX_BYTES
+    back = json.loads(text)
+    for key in HEADLINE_KEYS:
+        assert key in back, key
+    assert back["config"]["workload"].startswith("rmsnorm f32 1024x4096")
+    for key in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
+        assert key in back["roofline"], key
+    for key in ("value", "unit", "cores", "kind", "sample", "cpu"):
+        assert key in back["cpu_baseline"], key
+    for key in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step",
+                "us_per_step", "link_gbs", "frac"):
+        assert key in back["e2e"], key
+    for key in ("sm_mhz", "sm_max_mhz", "reasons"):
+        assert key in back["clocks"], key
+    assert back["value"] == pytest.approx(33570816 / 5.9e-6 / 1e9,
+                                          rel=1e-5)
+    assert back["roofline"]["frac"] == pytest.approx(
+        back["roofline"]["achieved"] / 6783.1, rel=1e-5)
+    assert back["floor"]["frac_of_copy"] == pytest.approx(5.71 / 5.9,
+                                                          rel=1e-3)
+    assert back["e2e"]["frac"] == pytest.approx(101 / 108, rel=1e-4)
+    assert back["gpu_launches"] == 20
+
+
+def test_headline_over_the_cap_is_refused():
+    import bench
+    line = bench.build_headline(_figures())
+    line["sweep"] = [{"op": "rmsnorm", "us": 1.0}] * 100
+    with pytest.raises(ValueError):
+        bench.headline_json(line)
+
+
+def test_headline_is_the_last_stdout_line(capsys):
+    import bench
+    print('{"op": "rmsnorm", "a sweep row": 1}')
+    print("a table row", file=sys.stderr)
+    bench.emit_headline(bench.build_headline(_figures(cpu=False)))
+    out = capsys.readouterr().out.splitlines()
+    last = json.loads(out[-1])
+    assert last["metric"] == bench.METRIC and "cpu_baseline" not in last
 
 
 def test_verify_accepts_a_consistent_line_and_flags_the_rest():
     import bench
-    assert bench.verify_line(_line()) == []
-    bad = _line()
+    assert bench.verify_line(bench.build_headline(_figures())) == []
+    bad = bench.build_headline(_figures())
     bad["value"] *= 1.01
-    bad["rounds"]["us_per_op_median"] = 5.0
+    bad["rounds_us"]["median"] = 9.0
+    bad["e2e"]["frac"] *= 1.1
     problems = bench.verify_line(bad)
     assert any(p.startswith("value") for p in problems)
-    assert any(p.startswith("rounds median") for p in problems)
-    assert bench.verify_line(_line(plan="path=loop W=1"))[0].startswith(
-        "plan")
+    assert any(p.startswith("rounds_us") for p in problems)
+    assert any(p.startswith("e2e.frac") for p in problems)
+    assert bench.verify_line(bench.build_headline(
+        _figures(plan="path=loop W=1")))[0].startswith("plan")
+
+
+def test_sweep_covers_every_operator_and_the_loss_only_call():
+    import bench
+    from row_reduction_gb300 import inputs
+    cases = bench.sweep_cases()
+    for dt in ("f32", "bf16", "f16"):
+        ops = {c[0] for c in cases if c[4] == dt}
+        assert ops == set(inputs.ALL_OPS), dt
+        assert ("cross_entropy", 1024, 4096, False, dt, False) in cases
