@@ -406,16 +406,24 @@ def measure_floor(work):
     out = {}
     if work.op in COPY_FLOOR_OPS:
         best = None
-        for threads in (256, 512, 1024):
-            for unroll in (2, 4, 8):
-                us = quick_us(CopyProbe(work, threads, unroll))
-                if best is None or us < best[0]:
-                    best = (us, threads, unroll)
-        us, threads, unroll = best
-        out["copy_us"] = quick_us(CopyProbe(work, threads, unroll), rounds=5,
+        # one wave of resident CTAs, or one CTA per row (as the operators'
+        # one-row-per-CTA plans), with and without the L2 prefetch
+        for grid in (0, work.rows):
+            for threads in (128, 256, 512, 1024):
+                for unroll in (2, 4, 8):
+                    for flags in (0, 1):
+                        p = CopyProbe(work, threads, unroll, grid, flags)
+                        us = quick_us(p)
+                        if best is None or us < best[0]:
+                            best = (us, threads, unroll, grid, flags)
+        us, threads, unroll, grid, flags = best
+        out["copy_us"] = quick_us(CopyProbe(work, threads, unroll, grid,
+                                            flags), rounds=5,
                                   min_round_s=0.03)
         out["copy_bytes"] = CopyProbe(work).bytes
-        out["copy_shape"] = f"{threads} threads, {unroll} in flight, one wave"
+        out["copy_shape"] = (f"{threads} threads, {unroll} in flight, "
+                             f"grid {grid or 'one wave'}, "
+                             f"{'L2 prefetch' if flags else 'no prefetch'}")
     out["empty_us"] = quick_us(EmptyProbe(32, 1), rounds=5, min_round_s=0.03)
     out["empty_wave_us"] = quick_us(EmptyProbe(512, 0), rounds=5,
                                     min_round_s=0.03)

@@ -409,12 +409,16 @@ MT_API size_t mt_describe_plan(const mt_plan_t *plan, char *buf, size_t n);
 
 /* Copies `bytes` bytes from src to dst (device pointers, both 16-byte
  * aligned, bytes a multiple of 16, the two ranges disjoint) with 16-byte
- * loads and stores: the grid's threads stride over the 16-byte words and
- * each keeps `unroll` (1, 2, 4 or 8) loads in flight.  bytes == 0 is a
- * no-op.  Bad arguments give MT_ERR_INVALID_ARGUMENT and enqueue nothing. */
+ * loads and stores.  Each CTA copies one contiguous slice of the buffer (as
+ * an operator's CTA owns its rows); its threads stride over the slice, each
+ * keeping `unroll` (1, 2, 4 or 8) loads in flight.  flags: 0, or
+ * MT_PLAN_PDL to have each CTA prefetch its slice into L2 before it waits
+ * for the previous kernel, as the operators do under that flag.
+ * bytes == 0 is a no-op.  Bad arguments give MT_ERR_INVALID_ARGUMENT and
+ * enqueue nothing. */
 MT_API mt_status mt_probe_copy(const void *src, void *dst, int64_t bytes,
                                int32_t threads, int32_t unroll, int32_t grid,
-                               mt_stream_t stream);
+                               int32_t flags, mt_stream_t stream);
 
 /* A kernel that does no work: the fixed cost of one dependent launch. */
 MT_API mt_status mt_probe_empty(int32_t threads, int32_t grid,

@@ -158,7 +158,7 @@ def lib() -> ctypes.CDLL:
                 "mt_plan_query_dtype": [ctypes.c_int, ctypes.c_int, I64, I64,
                                         PP],
                 "mt_plan_check_dtype": [ctypes.c_int, ctypes.c_int, I64, PP],
-                "mt_probe_copy": [P, P, I64, I32, I32, I32, P],
+                "mt_probe_copy": [P, P, I64, I32, I32, I32, I32, P],
                 "mt_probe_empty": [I32, I32, P],
             }
             for dt in ("f16", "bf16"):
@@ -466,11 +466,12 @@ def mt_last_cuda_error() -> int:
 
 
 def mt_probe_copy(src, dst, nbytes, threads=512, unroll=4, grid=0,
-                  stream=None):
+                  flags=0, stream=None):
     """Measurement aid: a plain 16-byte-vector copy of `nbytes` bytes."""
     _check(lib().mt_probe_copy(_ptr(src, "src", _any_dtype(src)),
                                _ptr(dst, "dst", _any_dtype(dst)), nbytes,
-                               threads, unroll, grid, _stream(stream)),
+                               threads, unroll, grid, flags,
+                               _stream(stream)),
            "mt_probe_copy")
 
 

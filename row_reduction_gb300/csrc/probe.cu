@@ -8,24 +8,33 @@
 
 namespace mt {
 
-// Copies n 16-byte words from src to dst.  The grid's T threads stride over
-// the words; each thread keeps U loads in flight before it stores them.
+// Copies n 16-byte words from src to dst.  CTA b copies the contiguous
+// slice [b*per, min(n, (b+1)*per)) of per = ceil(n / grid) words, the way a
+// row-reduction CTA owns its rows; its threads stride over the slice with U
+// predicated loads in flight before the U stores.  With `prefetch`, thread 0
+// first asks L2 for the CTA's slice, before the wait on the previous grid,
+// as the operators' MT_PLAN_PDL launches do.
 template <int U>
 __global__ void __launch_bounds__(1024)
     probe_copy_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst,
-                      int64_t n) {
+                      int64_t n, int prefetch) {
+    const int64_t per = (n + gridDim.x - 1) / gridDim.x;
+    const int64_t lo = (int64_t)blockIdx.x * per;
+    const int64_t hi = lo + per < n ? lo + per : n;
+    if (prefetch && threadIdx.x == 0 && lo < hi)
+        prefetch_l2(src + lo, (hi - lo) * 16);
     grid_launch_dependents();
     grid_wait_prerequisites();
-    const int64_t T = (int64_t)gridDim.x * blockDim.x;
-    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    for (; i + (int64_t)(U - 1) * T < n; i += (int64_t)U * T) {
+    const int64_t T = blockDim.x;
+    for (int64_t i = lo + threadIdx.x; i < hi; i += (int64_t)U * T) {
         uint4 v[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) v[u] = src[i + u * T];
+        for (int u = 0; u < U; ++u)
+            if (i + u * T < hi) v[u] = src[i + u * T];
 #pragma unroll
-        for (int u = 0; u < U; ++u) dst[i + u * T] = v[u];
+        for (int u = 0; u < U; ++u)
+            if (i + u * T < hi) dst[i + u * T] = v[u];
     }
-    for (; i < n; i += T) dst[i] = src[i];
 }
 
 // Does nothing but take part in the dependent-launch chain.
@@ -36,7 +45,7 @@ __global__ void __launch_bounds__(1024) probe_empty_kernel() {
 
 namespace {
 
-typedef void (*CopyFn)(const uint4 *, uint4 *, int64_t);
+typedef void (*CopyFn)(const uint4 *, uint4 *, int64_t, int);
 
 CopyFn copy_kernel_for(int unroll) {
     switch (unroll) {
@@ -90,8 +99,9 @@ extern "C" {
 
 mt_status mt_probe_copy(const void *src, void *dst, int64_t bytes,
                         int32_t threads, int32_t unroll, int32_t grid,
-                        mt_stream_t stream) {
-    if (bytes < 0 || bytes % 16 != 0 || bad_block(threads) || grid < 0)
+                        int32_t flags, mt_stream_t stream) {
+    if (bytes < 0 || bytes % 16 != 0 || bad_block(threads) || grid < 0 ||
+        (flags & ~MT_PLAN_PDL) != 0)
         return MT_ERR_INVALID_ARGUMENT;
     CopyFn fn = copy_kernel_for(unroll);
     if (fn == nullptr) return MT_ERR_INVALID_ARGUMENT;
@@ -110,7 +120,8 @@ mt_status mt_probe_copy(const void *src, void *dst, int64_t bytes,
         const uint4 *sp = static_cast<const uint4 *>(src);
         uint4 *dp = static_cast<uint4 *>(dst);
         int64_t n = bytes / 16;
-        void *args[] = {&sp, &dp, &n};
+        int prefetch = (flags & MT_PLAN_PDL) != 0;
+        void *args[] = {&sp, &dp, &n, &prefetch};
         e = launch_pdl(reinterpret_cast<const void *>(fn), g, threads, args,
                        (cudaStream_t)stream);
     }

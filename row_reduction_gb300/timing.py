@@ -205,7 +205,9 @@ def time_graph_steps(work, steps, warmup, plan=None, per_graph=64,
     given) on both sides.  After the first synchronize one untimed replay is
     enqueued ahead of the start event, so the GPU is busy while the host
     enqueues the timed replays: the start event then marks the first timed
-    step, not the host's graph-launch latency.  With `sampler` (an object
+    step, not the host's graph-launch latency.  The spacer is a graph of
+    its own, so the timed graph is not a relaunch of the one still
+    running.  With `sampler` (an object
     with start(), stop() and has_samples(n)), the GPU also runs the same steps
     for `load_s` seconds before and after the timed region (before: until
     the sampler holds at least two samples), so clock samples are taken
@@ -221,13 +223,15 @@ def time_graph_steps(work, steps, warmup, plan=None, per_graph=64,
     full = _graph_of(work, G, stream, plan)
     rem = steps % G
     tail = _graph_of(work, rem, stream, plan) if rem else None
+    spacer = _graph_of(work, graph_size(work, per_graph), stream, plan)
     with torch.cuda.stream(stream):
         for _ in range(max(1, math.ceil(warmup / G))):
             full.replay()
+        spacer.replay()
     stream.synchronize()
     if sampler is not None:
         sampler.start()
-        _replay_for(full, stream, load_s,
+        _replay_for(spacer, stream, load_s,
                     until=lambda: sampler.has_samples(2))
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
@@ -235,7 +239,7 @@ def time_graph_steps(work, steps, warmup, plan=None, per_graph=64,
     if barrier:
         barrier()
     with torch.cuda.stream(stream):
-        full.replay()                   # untimed spacer
+        spacer.replay()                 # untimed
         start.record(stream)
         for _ in range(steps // G):
             full.replay()
@@ -247,7 +251,7 @@ def time_graph_steps(work, steps, warmup, plan=None, per_graph=64,
     if barrier:
         barrier()
     if sampler is not None:
-        _replay_for(full, stream, load_s)
+        _replay_for(spacer, stream, load_s)
         sampler.stop()
     return start.elapsed_time(end) / 1e3
 
@@ -293,9 +297,10 @@ class CopyProbe:
     as one RMSNorm or softmax step (without the parameter vector).  Timed
     like a workload, it is the floor of a launch that moves those bytes."""
 
-    def __init__(self, work, threads=512, unroll=4, grid=0):
+    def __init__(self, work, threads=512, unroll=4, grid=0, flags=0):
         self.work, self.sets = work, work.sets
         self.threads, self.unroll, self.grid = threads, unroll, grid
+        self.flags = flags
         x0 = work.sets[0]["x"]
         self.nbytes = x0.numel() * x0.element_size()
         self.bytes = 2 * self.nbytes
@@ -304,7 +309,8 @@ class CopyProbe:
         L = B.lib()
         s = self.sets[i % len(self.sets)]
         args = (s["x"].data_ptr(), s["y"].data_ptr(), self.nbytes,
-                self.threads, self.unroll, self.grid, stream_handle)
+                self.threads, self.unroll, self.grid, self.flags,
+                stream_handle)
 
         def go():
             rc = L.mt_probe_copy(*args)

@@ -217,16 +217,17 @@ def test_invalid_arguments_are_rejected_before_launch():
 def test_probe_arguments_are_rejected_before_launch():
     """The measurement aids check their arguments before any CUDA call."""
     L = mt.lib()
-    assert L.mt_probe_copy(A, A + 4096, 4095, 512, 4, 0, None) == INV
-    assert L.mt_probe_copy(A, A + 4096, -16, 512, 4, 0, None) == INV
-    assert L.mt_probe_copy(A, A + 4096, 4096, 500, 4, 0, None) == INV
-    assert L.mt_probe_copy(A, A + 4096, 4096, 2048, 4, 0, None) == INV
-    assert L.mt_probe_copy(A, A + 4096, 4096, 512, 3, 0, None) == INV
-    assert L.mt_probe_copy(A, A + 4096, 4096, 512, 4, -1, None) == INV
-    assert L.mt_probe_copy(A + 4, A + 4096, 4096, 512, 4, 0, None) == INV
-    assert L.mt_probe_copy(None, A, 4096, 512, 4, 0, None) == INV
-    assert L.mt_probe_copy(A, A + 2048, 4096, 512, 4, 0, None) == INV
-    assert L.mt_probe_copy(A, A + 4096, 0, 512, 4, 0, None) == OK
+    assert L.mt_probe_copy(A, A + 4096, 4095, 512, 4, 0, 0, None) == INV
+    assert L.mt_probe_copy(A, A + 4096, -16, 512, 4, 0, 0, None) == INV
+    assert L.mt_probe_copy(A, A + 4096, 4096, 500, 4, 0, 0, None) == INV
+    assert L.mt_probe_copy(A, A + 4096, 4096, 2048, 4, 0, 0, None) == INV
+    assert L.mt_probe_copy(A, A + 4096, 4096, 512, 3, 0, 0, None) == INV
+    assert L.mt_probe_copy(A, A + 4096, 4096, 512, 4, -1, 0, None) == INV
+    assert L.mt_probe_copy(A, A + 4096, 4096, 512, 4, 0, 2, None) == INV
+    assert L.mt_probe_copy(A + 4, A + 4096, 4096, 512, 4, 0, 0, None) == INV
+    assert L.mt_probe_copy(None, A, 4096, 512, 4, 0, 0, None) == INV
+    assert L.mt_probe_copy(A, A + 2048, 4096, 512, 4, 0, 0, None) == INV
+    assert L.mt_probe_copy(A, A + 4096, 0, 512, 4, 0, 0, None) == OK
     assert L.mt_probe_empty(16, 1, None) == INV
     assert L.mt_probe_empty(32, -1, None) == INV
 

@@ -25,10 +25,10 @@ def built():
 
 
 @pytest.mark.parametrize("nbytes", [16, 4096, 16 * 1000 + 16, 33554432])
-@pytest.mark.parametrize("threads,unroll,grid", [(512, 4, 0), (256, 8, 0),
-                                                 (1024, 2, 0), (32, 1, 1),
-                                                 (128, 8, 3)])
-def test_probe_copy_is_an_exact_copy(nbytes, threads, unroll, grid):
+@pytest.mark.parametrize("threads,unroll,grid,flags", [
+    (512, 4, 0, 0), (256, 8, 0, 1), (1024, 2, 0, 0), (32, 1, 1, 1),
+    (128, 8, 3, 0), (128, 4, 1024, 1), (64, 2, 5000, 1)])
+def test_probe_copy_is_an_exact_copy(nbytes, threads, unroll, grid, flags):
     n = nbytes // 4
     rng = np.random.default_rng(nbytes + threads)
     src_host = rng.integers(-2**31, 2**31 - 1, n, dtype=np.int64).astype(
@@ -37,7 +37,8 @@ def test_probe_copy_is_an_exact_copy(nbytes, threads, unroll, grid):
     dst = Guarded(n, 0, Guarded.SENTINEL)
     assert src.ptr % 16 == 0 and dst.ptr % 16 == 0
     rc = mt.lib().mt_probe_copy(src.ptr, dst.ptr, nbytes, threads, unroll,
-                                grid, torch.cuda.current_stream().cuda_stream)
+                                grid, flags,
+                                torch.cuda.current_stream().cuda_stream)
     assert rc == mt.MT_OK
     torch.cuda.synchronize()
     dst.check()

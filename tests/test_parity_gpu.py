@@ -18,7 +18,8 @@ import torch
 import oracle
 import row_reduction_gb300 as mt
 from row_reduction_gb300 import inputs
-from gpu_util import Guarded, assert_close, to_dev
+from gpu_util import (Guarded, assert_close, check_softmax_rows,
+                      compare_row_blocks, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -109,6 +110,9 @@ def compare(op, got, ref, what):
                                   r.view(np.uint32)), f"{what}: h_out bits"
         else:
             assert_close(got[k], r, f"{what} {k}")
+            if op in ("softmax", "log_softmax"):
+                check_softmax_rows(got[k], r, f"{what} {k}",
+                                   log=op == "log_softmax")
 
 
 # --------------------------------------------------- published shapes
@@ -130,20 +134,18 @@ def test_rmsnorm_published_small_shapes(shape):
 
 @pytest.mark.parametrize("shape", inputs.RMSNORM_SWEEP)
 def test_rmsnorm_sweep_full_size(shape):
-    """Full-size sweep shapes (1% outliers) with the default plan: sampled
-    rows against the oracle, and on every row the unit-weight invariant
+    """Full-size sweep shapes (1% outliers) with the default plan: every
+    element against the oracle, and on every row the unit-weight invariant
     mean((y/w)^2) = ms/(ms+eps) recomputed in float64."""
     rows, cols = shape
     d = inputs.make("rmsnorm", rows, cols, SEED + 2, outliers=True)
     t = to_dev(d)
     y = mt.rmsnorm(t["x"], t["weight"], d["eps"])
     torch.cuda.synchronize()
-    rng = np.random.default_rng(7)
-    sample = np.unique(np.concatenate(
-        [[0, rows - 1], rng.integers(0, rows, 30)]))
-    ref = oracle.rmsnorm(d["x"][sample], d["weight"], d["eps"])
-    assert_close(y[torch.from_numpy(sample).cuda()].cpu().numpy(), ref,
-                 f"rmsnorm {shape} sampled rows")
+    compare_row_blocks(
+        y.cpu().numpy(),
+        lambda lo, hi: oracle.rmsnorm(d["x"][lo:hi], d["weight"], d["eps"]),
+        assert_close, f"rmsnorm {shape}")
     xd = t["x"].double()
     ms = (xd * xd).mean(dim=1)
     eps = float(np.float32(d["eps"]))
@@ -358,6 +360,7 @@ def test_softmax_special_rows():
     ref = oracle.softmax(x)
     got = mt.softmax(torch.from_numpy(x).cuda()).cpu().numpy()
     assert_close(got, ref, "softmax special rows")
+    check_softmax_rows(got, ref, "softmax special rows")
 
 
 def test_cross_entropy_labels_and_mean():
