@@ -45,7 +45,7 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 
 from row_reduction_gb300.timing import (  # noqa: E402
-    CopyProbe, EmptyProbe, Workload, algorithmic_bytes, time_e2e,
+    CopyProbe, EmptyProbe, ReadProbe, Workload, algorithmic_bytes, time_e2e,
     time_graph_steps, time_link, time_plain_steps, time_rounds)
 
 METRIC = ("RMSNorm FP32 µs/op and HBM GB/s (% of GB300 peak), "
@@ -55,8 +55,10 @@ DATASHEET_HBM_GBS = 7900.0   # GB300 HBM3e nominal, for context only
 HEADLINE_MAX_BYTES = 1536
 H_OUT_OPS = ("residual_layernorm", "residual_rmsnorm")
 # Operators with one input matrix x and one output matrix y of its shape:
-# the copy floor moves exactly their matrix bytes.
+# the copy floor moves exactly their matrix bytes.  Operators that read x
+# and write one value per row: the read floor.
 COPY_FLOOR_OPS = ("rmsnorm", "layernorm", "softmax", "log_softmax")
+READ_FLOOR_OPS = ("row_sum", "cross_entropy")
 _OUTL = "with 1% x100 outliers"
 INPUT_RECIPE = {
     "rmsnorm": f"x~N(0,1) {_OUTL}, weight~1+0.1N(0,1), eps=1e-6",
@@ -398,32 +400,40 @@ def quick_us(work, rounds=3, min_round_s=0.01):
                                          min_round_s=min_round_s))
 
 
+def best_probe(cls, work):
+    """The fastest launch shape of a probe kernel on the workload's pool:
+    one wave of resident CTAs or one CTA per row (as the operators'
+    one-row-per-CTA plans), with and without the L2 prefetch; then that
+    shape re-timed with longer rounds.  Returns (µs, shape text)."""
+    best = None
+    for grid in (0, work.rows):
+        for threads in (128, 256, 512, 1024):
+            for unroll in (2, 4, 8):
+                for flags in (0, 1):
+                    us = quick_us(cls(work, threads, unroll, grid, flags))
+                    if best is None or us < best[0]:
+                        best = (us, threads, unroll, grid, flags)
+    us, threads, unroll, grid, flags = best
+    us = quick_us(cls(work, threads, unroll, grid, flags), rounds=5,
+                  min_round_s=0.03)
+    return us, (f"{threads} threads, {unroll} in flight, "
+                f"grid {grid or 'one wave'}, "
+                f"{'L2 prefetch' if flags else 'no prefetch'}")
+
+
 def measure_floor(work):
     """The floor of one step, timed like the steps themselves (graph
     replays of dependent launches over the same rotating pool): the
-    library's plain copy kernel moving the step's matrix bytes (best of a
-    few launch shapes), and its empty kernel, alone and on a full wave."""
+    library's plain copy kernel moving the step's matrix bytes in and out,
+    or its read kernel reading them (best of a few launch shapes each), and
+    its empty kernel, alone and on a full wave."""
     out = {}
     if work.op in COPY_FLOOR_OPS:
-        best = None
-        # one wave of resident CTAs, or one CTA per row (as the operators'
-        # one-row-per-CTA plans), with and without the L2 prefetch
-        for grid in (0, work.rows):
-            for threads in (128, 256, 512, 1024):
-                for unroll in (2, 4, 8):
-                    for flags in (0, 1):
-                        p = CopyProbe(work, threads, unroll, grid, flags)
-                        us = quick_us(p)
-                        if best is None or us < best[0]:
-                            best = (us, threads, unroll, grid, flags)
-        us, threads, unroll, grid, flags = best
-        out["copy_us"] = quick_us(CopyProbe(work, threads, unroll, grid,
-                                            flags), rounds=5,
-                                  min_round_s=0.03)
+        out["copy_us"], out["copy_shape"] = best_probe(CopyProbe, work)
         out["copy_bytes"] = CopyProbe(work).bytes
-        out["copy_shape"] = (f"{threads} threads, {unroll} in flight, "
-                             f"grid {grid or 'one wave'}, "
-                             f"{'L2 prefetch' if flags else 'no prefetch'}")
+    if work.op in READ_FLOOR_OPS:
+        out["read_us"], out["read_shape"] = best_probe(ReadProbe, work)
+        out["read_bytes"] = ReadProbe(work).bytes
     out["empty_us"] = quick_us(EmptyProbe(32, 1), rounds=5, min_round_s=0.03)
     out["empty_wave_us"] = quick_us(EmptyProbe(512, 0), rounds=5,
                                     min_round_s=0.03)
@@ -472,20 +482,46 @@ def build_headline(f):
         "clocks": f["clocks"],
     }
     fl = f["floor"]
-    line["floor"] = {"empty_us": sig(fl["empty_us"], 4)}
-    if "copy_us" in fl:
-        line["floor"] = {
-            "copy_us": sig(fl["copy_us"], 4),
-            "copy_frac": sig(fl["copy_bytes"] / fl["copy_us"] / 1e3 / peak,
-                             4),
-            "frac_of_copy": sig(fl["copy_us"] / (per_step * 1e6), 4),
-            "empty_us": sig(fl["empty_us"], 4)}
+    line["floor"] = {}
+    for kind in ("copy", "read"):
+        if f"{kind}_us" in fl:
+            us = fl[f"{kind}_us"]
+            line["floor"].update({
+                f"{kind}_us": sig(us, 4),
+                f"{kind}_frac": sig(fl[f"{kind}_bytes"] / us / 1e3 / peak, 4),
+                f"frac_of_{kind}": sig(us / (per_step * 1e6), 4)})
+    line["floor"]["empty_us"] = sig(fl["empty_us"], 4)
     cb = f.get("cpu")
     if cb:
         line["cpu_baseline"] = {k: (sig(cb[k], 4) if k == "value" else cb[k])
                                 for k in ("value", "unit", "cores", "kind",
                                           "sample", "cpu")}
     return line
+
+
+def run_profile(args):
+    """--profile: only the timed steps of the workload (or of a probe's
+    chain on the workload's pool), for a profiler to capture; prints one
+    short line, not the headline."""
+    import torch
+    import row_reduction_gb300 as mt
+    from row_reduction_gb300 import build as mt_build, inputs
+    mt_build.build()
+    mt.lib()
+    props = torch.cuda.get_device_properties(0)
+    l2 = int(getattr(props, "L2_cache_size", 126 << 20)) or (126 << 20)
+    work = Workload(args.op, args.rows, args.cols, inputs.TUNE_SEED,
+                    outliers=True, l2_bytes=l2, dtype=args.dtype,
+                    ce_mean=not args.loss_only)
+    if args.probe == "copy":
+        work = CopyProbe(work, 512, 8, 0, 1)
+    elif args.probe == "read":
+        work = ReadProbe(work, 512, 8, 0, 1)
+    el = time_graph_steps(work, args.steps, args.warmup)
+    print(f"profile run: {args.op} {args.dtype} {args.rows}x{args.cols}"
+          f"{' ' + args.probe + ' probe' if args.probe else ''}: "
+          f"{el / args.steps * 1e6:.3f} us per step over {args.steps} steps")
+    return 0
 
 
 def run_ours(args, rank, world, local_rank):
@@ -763,6 +799,15 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--profile", action="store_true",
+                    help="only run the timed steps (for a profiler); print "
+                         "one short line instead of the headline")
+    ap.add_argument("--probe", choices=["copy", "read"], default=None,
+                    help="with --profile: run the library's copy or read "
+                         "probe over the workload's buffers instead")
+    ap.add_argument("--loss-only", action="store_true",
+                    help="cross-entropy without the batch mean "
+                         "(mean_loss = NULL); with --profile")
     ap.add_argument("--details", metavar="FILE", default=None,
                     help="also write every figure (sweep, floor, hot, "
                          "context) to FILE as JSON")
@@ -786,6 +831,8 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.profile:
+        return run_profile(args)
     if world > 1:
         import torch
         import torch.distributed as dist

@@ -420,6 +420,17 @@ MT_API mt_status mt_probe_copy(const void *src, void *dst, int64_t bytes,
                                int32_t threads, int32_t unroll, int32_t grid,
                                int32_t flags, mt_stream_t stream);
 
+/* Reads `bytes` bytes at src (16-byte aligned, bytes a multiple of 16)
+ * with the CTA slices, threads and loads in flight of mt_probe_copy, and
+ * writes one 32-bit word per CTA to dst[cta]: the XOR of the words of its
+ * slice.  dst holds dst_words words; the grid (given, or one wave when
+ * grid == 0) must not exceed it.  The floor of an operator that reads a
+ * matrix and writes one value per row.  flags as for mt_probe_copy. */
+MT_API mt_status mt_probe_read(const void *src, int64_t bytes, uint32_t *dst,
+                               int64_t dst_words, int32_t threads,
+                               int32_t unroll, int32_t grid, int32_t flags,
+                               mt_stream_t stream);
+
 /* A kernel that does no work: the fixed cost of one dependent launch. */
 MT_API mt_status mt_probe_empty(int32_t threads, int32_t grid,
                                 mt_stream_t stream);

@@ -70,7 +70,7 @@ EXPORTS = (
     "mt_log_softmax_f16", "mt_log_softmax_bf16",
     "mt_cross_entropy_ignore_f32", "mt_cross_entropy_ignore_f16",
     "mt_cross_entropy_ignore_bf16",
-    "mt_probe_copy", "mt_probe_empty",
+    "mt_probe_copy", "mt_probe_read", "mt_probe_empty",
 )
 
 
@@ -159,6 +159,7 @@ def lib() -> ctypes.CDLL:
                                         PP],
                 "mt_plan_check_dtype": [ctypes.c_int, ctypes.c_int, I64, PP],
                 "mt_probe_copy": [P, P, I64, I32, I32, I32, I32, P],
+                "mt_probe_read": [P, I64, P, I64, I32, I32, I32, I32, P],
                 "mt_probe_empty": [I32, I32, P],
             }
             for dt in ("f16", "bf16"):

@@ -7,10 +7,13 @@ namespace mt {
 // mean = (sum of loss[0..rows)) / n, n = rows, or with an ignore index the
 // number of rows whose label is not it (ignored rows hold loss 0; no such
 // row gives 0/0 = NaN).  One CTA; each thread sums a strided subset in index
-// order with compensated arithmetic, then the block combines the partials in
-// a fixed shuffle/shared-memory order, so the result does not depend on
-// timing (no atomics).
-__global__ void __launch_bounds__(1024)
+// order with compensated arithmetic (kMeanInFlight loads in flight per
+// thread), then the block combines the partials in a fixed shuffle/shared-
+// memory order, so the result does not depend on timing (no atomics).
+constexpr int kMeanThreads = 256;
+constexpr int kMeanInFlight = 4;   // loads in flight per thread
+
+__global__ void __launch_bounds__(kMeanThreads)
     mean_kernel(const float *loss, float *mean, int64_t rows,
                 const int32_t *labels, int32_t ignore_index,
                 int32_t has_ignore) {
@@ -25,12 +28,22 @@ __global__ void __launch_bounds__(1024)
     __shared__ long long ignored_part[32];
     float s = 0.f, c = 0.f;
     long long ignored = 0;
-    for (int64_t i = threadIdx.x; i < rows; i += blockDim.x) {
-        float t, err;
-        two_sum(s, loss[i], t, err);
-        s = t;
-        c += err;
-        if (has_ignore && labels[i] == ignore_index) ++ignored;
+    const int64_t T = blockDim.x;
+    for (int64_t i0 = threadIdx.x; i0 < rows; i0 += kMeanInFlight * T) {
+        float t[kMeanInFlight];
+#pragma unroll
+        for (int u = 0; u < kMeanInFlight; ++u)
+            t[u] = i0 + u * T < rows ? loss[i0 + u * T] : 0.f;
+#pragma unroll
+        for (int u = 0; u < kMeanInFlight; ++u) {
+            float sum, err;
+            two_sum(s, t[u], sum, err);
+            s = sum;
+            c += err;
+            if (has_ignore && i0 + u * T < rows &&
+                labels[i0 + u * T] == ignore_index)
+                ++ignored;
+        }
     }
     row_allreduce_compensated(s, c, (int)blockDim.x, red, parity);
     long long total = 0;
@@ -60,7 +73,7 @@ cudaError_t launch_mean(const float *loss, float *mean, int64_t rows,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1);
-    cfg.blockDim = dim3(1024);
+    cfg.blockDim = dim3(kMeanThreads);
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;

@@ -319,6 +319,39 @@ class CopyProbe:
         return go
 
 
+class ReadProbe:
+    """The library's read kernel (mt_probe_read) over a workload's own
+    buffer pool: step i reads set i's x, the same bytes in as one row-sum
+    or cross-entropy step, and writes one word per CTA.  The floor of a
+    launch that reads those bytes."""
+
+    def __init__(self, work, threads=512, unroll=4, grid=0, flags=0):
+        import torch
+        self.work, self.sets = work, work.sets
+        self.threads, self.unroll, self.grid = threads, unroll, grid
+        self.flags = flags
+        x0 = work.sets[0]["x"]
+        self.nbytes = x0.numel() * x0.element_size()
+        self.bytes = self.nbytes
+        self.words = max(grid, 152 * 64, 1)
+        self.out = [torch.empty(self.words, dtype=torch.int32, device="cuda")
+                    for _ in range(len(work.sets))]
+
+    def call_fn(self, i, stream_handle, plan=None):
+        L = B.lib()
+        s = self.sets[i % len(self.sets)]
+        args = (s["x"].data_ptr(), self.nbytes,
+                self.out[i % len(self.sets)].data_ptr(), self.words,
+                self.threads, self.unroll, self.grid, self.flags,
+                stream_handle)
+
+        def go():
+            rc = L.mt_probe_read(*args)
+            if rc != 0:
+                raise B.MTError(rc, "mt_probe_read")
+        return go
+
+
 class EmptyProbe:
     """The library's empty kernel (mt_probe_empty): a chain of dependent
     launches that move nothing, the fixed cost of one step."""

@@ -324,6 +324,41 @@ def published_shapes(ops):
     return shapes
 
 
+# Held-out shapes for the planner's regret: every operator and storage type,
+# row lengths outside the measured table (so the planner re-fits or falls
+# back), from short rows to rows wider than one CTA's registers.  They are
+# tuned to find each shape's own optimum, never written into the table.
+HELDOUT_CASES = (
+    "rmsnorm:f32:512x2048", "rmsnorm:f32:2048x5120", "rmsnorm:f32:300x3000",
+    "rmsnorm:f32:1x30000", "rmsnorm:f32:32x32768", "rmsnorm:f32:4096x12288",
+    "rmsnorm:bf16:3000x768", "rmsnorm:f16:777x5000",
+    "layernorm:f32:2048x1024", "layernorm:f32:100x8192",
+    "layernorm:bf16:4096x2560", "layernorm:f16:512x768",
+    "residual_layernorm:f32:1500x2048", "residual_layernorm:bf16:8192x1024",
+    "residual_layernorm:f16:64x12288",
+    "softmax:f32:4096x1000", "softmax:bf16:4096x1000",
+    "softmax:bf16:128x50257", "softmax:f16:2000x2000",
+    "log_softmax:f32:333x7777", "log_softmax:bf16:1024x32768",
+    "log_softmax:f16:64x100000",
+    "row_sum:f32:5000x1000", "row_sum:f32:16x50000",
+    "row_sum:bf16:2048x4000", "row_sum:f16:700x300",
+    "cross_entropy:f32:4096x1000", "cross_entropy:f32:2048x50257",
+    "cross_entropy:bf16:4096x1000", "cross_entropy:bf16:128x50257",
+    "cross_entropy:f16:1000x151936",
+    "residual_rmsnorm:f32:2048x3072", "residual_rmsnorm:bf16:4096x5120",
+    "residual_rmsnorm:f16:100x6000",
+)
+
+
+def parse_case(text):
+    """'op:dtype:RxC' -> (dtype, op, rows, cols)."""
+    op, dt, shape = text.split(":")
+    if op not in B.OP_IDS or dt not in B.DTYPE_IDS:
+        raise ValueError(f"bad case {text!r}")
+    r, c = shape.split("x")
+    return dt, op, int(r), int(c)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description="measured plan search")
     ap.add_argument("--ops", default=",".join(inputs.ALL_OPS))
@@ -337,6 +372,11 @@ def main(argv=None):
     ap.add_argument("--evaluate", default=None,
                     help="tuning records (JSON) to measure the planner's "
                          "regret on, instead of tuning")
+    ap.add_argument("--cases", default=None,
+                    help="explicit (operator, storage type, shape) cases "
+                         "instead of --ops/--dtypes/--shapes, e.g. "
+                         "rmsnorm:f32:512x2048,softmax:bf16:128x50257, "
+                         "or 'heldout' for HELDOUT_CASES")
     args = ap.parse_args(argv)
     import torch
     from . import build
@@ -356,6 +396,12 @@ def main(argv=None):
     else:
         shapes = [(op, int(s.split("x")[0]), int(s.split("x")[1]))
                   for op in ops for s in args.shapes.split(",")]
+    work = [(dt, op, r, c) for dt in args.dtypes.split(",") if dt
+            for op, r, c in shapes]
+    if args.cases:
+        cases = (HELDOUT_CASES if args.cases == "heldout"
+                 else args.cases.split(","))
+        work = [parse_case(c) for c in cases if c]
     props = torch.cuda.get_device_properties(0)
     l2 = int(getattr(props, "L2_cache_size", 126 << 20)) or (126 << 20)
     records = []
@@ -364,13 +410,12 @@ def main(argv=None):
     done = {(r["op"], r.get("dtype", "f32"), r["rows"], r["cols"])
             for r in records}
     t0 = time.time()
-    for dt in [d for d in args.dtypes.split(",") if d]:
-        for op, rows, cols in shapes:
-            if (op, dt, rows, cols) in done:
-                continue
-            records.append(tune_shape(op, rows, cols, l2, args.rounds,
-                                      log=lambda s: print(s, flush=True),
-                                      dtype=dt))
+    for dt, op, rows, cols in work:
+        if (op, dt, rows, cols) in done:
+            continue
+        records.append(tune_shape(op, rows, cols, l2, args.rounds,
+                                  log=lambda s: print(s, flush=True),
+                                  dtype=dt))
         with open(args.json, "w") as f:
             json.dump({"device": torch.cuda.get_device_name(0),
                        "records": records}, f, indent=1)

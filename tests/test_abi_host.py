@@ -33,7 +33,7 @@ def header_symbols():
 
 def test_library_exports_every_declared_symbol():
     declared = header_symbols()
-    assert len(declared) == 46
+    assert len(declared) == 47
     L = mt.lib()
     for name in declared:
         assert hasattr(L, name), name
@@ -228,6 +228,15 @@ def test_probe_arguments_are_rejected_before_launch():
     assert L.mt_probe_copy(None, A, 4096, 512, 4, 0, 0, None) == INV
     assert L.mt_probe_copy(A, A + 2048, 4096, 512, 4, 0, 0, None) == INV
     assert L.mt_probe_copy(A, A + 4096, 0, 512, 4, 0, 0, None) == OK
+    assert L.mt_probe_read(A, 4095, A + 8192, 64, 512, 4, 0, 0, None) == INV
+    assert L.mt_probe_read(A, 4096, A + 8192, 64, 512, 3, 0, 0, None) == INV
+    assert L.mt_probe_read(A, 4096, A + 8192, 64, 512, 4, 65, 0, None) == INV
+    assert L.mt_probe_read(A, 4096, A + 8194, 64, 512, 4, 8, 0, None) == INV
+    assert L.mt_probe_read(A + 8, 4096, A + 8192, 64, 512, 4, 8, 0,
+                           None) == INV
+    assert L.mt_probe_read(A, 4096, None, 64, 512, 4, 8, 0, None) == INV
+    assert L.mt_probe_read(A, 4096, A + 8192, 64, 512, 4, 8, 2, None) == INV
+    assert L.mt_probe_read(A, 0, A + 8192, 64, 512, 4, 8, 0, None) == OK
     assert L.mt_probe_empty(16, 1, None) == INV
     assert L.mt_probe_empty(32, -1, None) == INV
 

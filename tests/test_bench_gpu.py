@@ -46,6 +46,39 @@ def test_probe_copy_is_an_exact_copy(nbytes, threads, unroll, grid, flags):
     assert np.array_equal(got, src_host)
 
 
+@pytest.mark.parametrize("nbytes", [16, 16 * 1000 + 16, 33554432])
+@pytest.mark.parametrize("threads,unroll,grid,flags", [
+    (512, 4, 0, 0), (256, 8, 0, 1), (32, 1, 1, 0), (128, 4, 1024, 1),
+    (64, 2, 5000, 1)])
+def test_probe_read_writes_each_slices_xor(nbytes, threads, unroll, grid,
+                                           flags):
+    n = nbytes // 4
+    rng = np.random.default_rng(nbytes + threads + 1)
+    src_host = rng.integers(0, 2**32, n, dtype=np.uint64).astype(np.uint32)
+    src = Guarded(n, 0, -7, torch.int32, src_host.view(np.int32))
+    words = 152 * 64
+    dst = Guarded(words, 0, -7, torch.int32, np.zeros(words, np.int32))
+    rc = mt.lib().mt_probe_read(src.ptr, nbytes, dst.ptr, words, threads,
+                                unroll, grid, flags,
+                                torch.cuda.current_stream().cuda_stream)
+    assert rc == mt.MT_OK
+    torch.cuda.synchronize()
+    dst.check()
+    got = dst.view.cpu().numpy().view(np.uint32)
+    # XOR is associative: the CTAs' words together give the whole buffer's
+    assert np.bitwise_xor.reduce(got) == np.bitwise_xor.reduce(src_host)
+    if grid > 0:
+        # CTA b read the 16-byte words [b*per, (b+1)*per); the rest of dst
+        # is untouched
+        nw = nbytes // 16
+        per = -(-nw // grid)
+        for b in range(grid):
+            lo, hi = b * per * 4, min(nw, (b + 1) * per) * 4
+            want = np.bitwise_xor.reduce(src_host[lo:hi]) if lo < hi else 0
+            assert got[b] == want, b
+        assert not got[grid:].any()
+
+
 def test_probe_empty_chain_runs():
     s = torch.cuda.current_stream().cuda_stream
     for threads, grid in ((32, 1), (512, 0), (1024, 300)):

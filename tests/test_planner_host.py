@@ -111,3 +111,35 @@ def test_tuner_candidates_are_legal_and_cover_the_plan_space():
             C = max(1, p.cluster)
             assert p.grid % C == 0
             assert p.grid // C < -(-rows // p.rows_per_block)
+
+
+def _table_entries():
+    import re
+    path = os.path.join(os.path.dirname(os.path.dirname(
+        os.path.abspath(__file__))), "row_reduction_gb300", "csrc",
+        "plan_table.inc")
+    out = []
+    for line in open(path):
+        m = re.match(r"\s*\{(\d+), (\d+), (\d+), (\d+), (\d+), (\d+),",
+                     line)
+        if m:
+            out.append(tuple(int(v) for v in m.groups()))
+    return out
+
+
+def test_heldout_cases_cover_every_operator_and_type_outside_the_table():
+    """The regret set spans all operators and storage types, and no case is
+    served by a table entry (so it measures the re-fit and heuristic)."""
+    from row_reduction_gb300 import tune, inputs
+    import row_reduction_gb300 as mt
+    cases = [tune.parse_case(c) for c in tune.HELDOUT_CASES]
+    assert len(cases) >= 30
+    assert {c[1] for c in cases} == set(inputs.ALL_OPS)
+    assert {c[0] for c in cases} == {"f32", "f16", "bf16"}
+    table = _table_entries()
+    assert table
+    for dt, op, rows, cols in cases:
+        for e_op, e_dt, c0, c1, r0, r1 in table:
+            hit = (e_op == mt.OP_IDS[op] and e_dt == mt.DTYPE_IDS[dt] and
+                   c0 <= cols <= c1 and r0 <= rows <= r1)
+            assert not hit, (op, dt, rows, cols)
