@@ -1183,6 +1183,11 @@ __global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
                 });
         } else if constexpr (OP == OP_SOFTMAX || OP == OP_CROSS_ENTROPY ||
                              OP == OP_LOG_SOFTMAX) {
+            // Running (max, sum of exp(x - max)) of the thread's values:
+            // the sum is rescaled only when a pack raises the max (or turns
+            // it NaN), so a pack costs one exponential per value; while
+            // every value so far is -inf there is nothing to add (and
+            // exp(-inf - -inf) would be NaN).
             float m = -INFINITY, s = 0.f;
             stream_row<V, AL, U>(worker, WT, hd, nb, active, load_x,
                                  [&](const float *t, int nv, int) {
@@ -1190,11 +1195,19 @@ __global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
 #pragma unroll
                                      for (int e = 0; e < V; ++e)
                                          if (e < nv) pm = nanmax(pm, t[e]);
-                                     float ps = 0.f;
+                                     const float mm = nanmax(m, pm);
+                                     if (mm != m) {
+                                         s *= exp_shifted(m - mm);
+                                         m = mm;
+                                     }
+                                     if (m != -INFINITY) {
+                                         float ps = 0.f;
 #pragma unroll
-                                     for (int e = 0; e < V; ++e)
-                                         if (e < nv) ps += exp_shifted(t[e] - pm);
-                                     lse_merge(m, s, pm, ps);
+                                         for (int e = 0; e < V; ++e)
+                                             if (e < nv)
+                                                 ps += exp_shifted(t[e] - m);
+                                         s += ps;
+                                     }
                                  });
             team_allreduce_lse(m, s, W, csize, red, parity, cpar);
             if constexpr (OP == OP_SOFTMAX) {

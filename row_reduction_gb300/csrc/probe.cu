@@ -1,7 +1,8 @@
 // probe.cu -- measurement aids: a plain vectorised device-to-device copy, a
-// read of the same shape, and an empty kernel.  Both launch the way the row-reduction kernels do (as
-// programmatic dependents of the previous kernel on the stream, one wave of
-// resident CTAs), so a benchmark can put a row-reduction launch beside the
+// read of the same shape, and an empty kernel.  All three launch the way the
+// row-reduction kernels do (as programmatic dependents of the previous
+// kernel on the stream, one wave of resident CTAs), so a benchmark can put a
+// row-reduction launch beside the
 // floor of a launch that moves the same bytes with no arithmetic (in and
 // out, or in only), or no bytes at all, timed by the same method on the
 // same buffers.

@@ -2,7 +2,8 @@
 element-wise tolerance check against the oracle.
 
 Tolerance: an FP32 output element passes when |gpu - ref| <= 1e-5*(1+|ref|),
-ref being the oracle's double value; NaN must match NaN.
+ref being the oracle's double value; NaN must match NaN and an infinity the
+same infinity.
 """
 import os
 from concurrent.futures import ThreadPoolExecutor
@@ -19,16 +20,23 @@ def assert_close(got, ref, what=""):
     ref = np.asarray(ref, dtype=np.float64)
     assert got.shape == ref.shape, (what, got.shape, ref.shape)
     both_nan = np.isnan(got) & np.isnan(ref)
-    err = np.abs(got - ref)
-    tol = RTOL * (1.0 + np.abs(ref))
-    bad = ~((err <= tol) | both_nan)
+    with np.errstate(invalid="ignore"):
+        err = np.abs(got - ref)
+    with np.errstate(over="ignore"):
+        tol = RTOL * (1.0 + np.abs(ref))
+    # equal values pass, equal infinities included (log-softmax of -inf);
+    # an infinite reference admits nothing else (its tolerance would be
+    # infinite)
+    bad = ~(((err <= tol) & np.isfinite(ref)) | both_nan | (got == ref))
     if bad.any():
         idx = np.argwhere(bad)
         i = tuple(idx[0])
+        with np.errstate(invalid="ignore", divide="ignore"):
+            ratio = np.where(bad & np.isfinite(err / tol), err / tol, 0)
         raise AssertionError(
             f"{what}: {bad.sum()} of {bad.size} elements outside "
             f"1e-5*(1+|ref|); first at {i}: gpu={got[i]!r} ref={ref[i]!r}; "
-            f"max err/tol={np.nanmax(np.where(bad, err / tol, 0)):.3g}")
+            f"max finite err/tol={np.max(ratio):.3g}")
 
 
 class Guarded:

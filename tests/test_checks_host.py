@@ -73,3 +73,13 @@ def test_row_blocks_cover_every_row_and_report_the_block():
     with pytest.raises(AssertionError, match="rows 6..7"):
         compare_row_blocks(bad, lambda lo, hi: ref[lo:hi], assert_close,
                            "planted", block=3)
+
+
+def test_element_check_handles_infinities():
+    assert_close(np.array([-np.inf, np.inf, 1.0]),
+                 np.array([-np.inf, np.inf, 1.0]), "equal infinities")
+    for got in ([np.inf], [5.0], [np.nan]):
+        with pytest.raises(AssertionError):
+            assert_close(np.array(got), np.array([-np.inf]), "planted")
+    with pytest.raises(AssertionError):
+        assert_close(np.array([-np.inf]), np.array([3.0]), "planted")

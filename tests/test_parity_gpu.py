@@ -681,3 +681,50 @@ def test_cluster_split_rows(op, shape):
         p = mt.make_plan(128, 4, 0, 1, mt.MT_PATH_LOOP, grid=4, cluster=2)
         got = run_guarded(op, d, rows, cols, plan=p, offsets=offs)
         compare(op, got, ref, f"{op} {shape} persistent clusters")
+
+
+# ------------------------------------------------- masked (-inf) runs
+def masked_logits(rows, cols, seed):
+    """Softmax inputs N(0, 2^2) with runs of -inf covering whole packs and
+    more: a row's head, its tail, alternate 16-value blocks, all but one
+    value, pack-straddling runs, and one row without any."""
+    d = inputs.make("cross_entropy", rows, cols, seed)
+    x = d["x"]
+    x[0, :min(cols - 1, 64)] = -np.inf
+    x[1 % rows, max(1, cols - 100):] = -np.inf
+    for lo in range(0, cols - 16, 32):
+        x[2 % rows, lo:lo + 16] = -np.inf
+    x[3 % rows, 1:] = -np.inf
+    x[4 % rows, 3:cols - 5] = -np.inf
+    d["labels"] = np.array([int(np.flatnonzero(np.isfinite(r))[k % 7 %
+                            max(1, np.isfinite(r).sum())])
+                            for k, r in enumerate(x)], dtype=np.int32)
+    return d
+
+
+@pytest.mark.parametrize("op", ["softmax", "log_softmax", "cross_entropy"])
+@pytest.mark.parametrize("cols", [257, 4103, 20000])
+def test_masked_runs_of_minus_infinity(op, cols):
+    """-inf entries contribute exp(-inf) = 0: rows whose packs are wholly
+    -inf stay finite on the register, loop and cluster paths (only an
+    all -inf row is NaN, in the oracle as on the GPU)."""
+    rows = 6
+    d = masked_logits(rows, cols, SEED + cols)
+    dd = {"x": d["x"]} if op != "cross_entropy" else \
+        {"x": d["x"], "labels": d["labels"]}
+    ref = oracle.run(op, dd)
+    plans = [None] + [p for p in candidate_plans(min(cols, 4103))
+                      if cols <= 4103 or p.path == mt.MT_PATH_LOOP][::3]
+    if cols >= 4103:
+        plans += cluster_plans(cols)
+    for p in plans:
+        if p is not None and mt.mt_plan_check(mt.OP_IDS[op], cols, p) != 0:
+            continue
+        got = run_guarded(op, dd, rows, cols, plan=p)
+        what = f"{op} masked {rows}x{cols} " + (
+            "default" if p is None else mt.mt_describe_plan(p))
+        for k, r in ref.items():
+            # finite everywhere (log-softmax: wherever x is finite)
+            fin = np.isfinite(dd["x"]) if op == "log_softmax" else True
+            assert np.isfinite(r[fin]).all(), (what, k)
+        compare(op, got, ref, what)

@@ -39,9 +39,13 @@ def assert_close_storage(got, ref, dt, what):
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     assert got.shape == ref.shape
-    tol = 0.5 * ulp(np.abs(ref) * (1 + 2.0 ** -6), dt) + 1e-5 * (1 + np.abs(ref))
+    with np.errstate(invalid="ignore", over="ignore"):
+        tol = (0.5 * ulp(np.abs(ref) * (1 + 2.0 ** -6), dt) +
+               1e-5 * (1 + np.abs(ref)))
+        err = np.abs(got - ref)
     both_nan = np.isnan(got) & np.isnan(ref)
-    bad = ~((np.abs(got - ref) <= tol) | both_nan)
+    # an infinite reference admits only the same infinity
+    bad = ~(((err <= tol) & np.isfinite(ref)) | both_nan | (got == ref))
     if bad.any():
         i = tuple(np.argwhere(bad)[0])
         raise AssertionError(f"{what}: {bad.sum()} of {bad.size} outside; "
