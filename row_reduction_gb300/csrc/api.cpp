@@ -74,9 +74,9 @@ cudaError_t sm_count(int dev, int *out) {
     return cudaSuccess;
 }
 
-typedef cudaError_t (*LaunchFn)(const mt_plan_t &, const KArgs &, bool,
+typedef cudaError_t (*LaunchFn)(const mt_plan_t &, const KArgs &, int,
                                 cudaStream_t);
-typedef cudaError_t (*OccFn)(const mt_plan_t &, bool, int *);
+typedef cudaError_t (*OccFn)(const mt_plan_t &, int, int *);
 
 #define MT_ROW(op)                                                           \
     {launch_##op##_f32, launch_##op##_f16, launch_##op##_bf16}
@@ -101,12 +101,12 @@ std::mutex g_occ_mu;
 std::unordered_map<uint64_t, int> g_occ;
 
 cudaError_t blocks_per_sm(int dev, int op, int dtype, const mt_plan_t &p,
-                          bool aligned, int *out) {
+                          int mode, int *out) {
     const uint64_t key =
         ((uint64_t)(dev & 0xff) << 56) | ((uint64_t)op << 50) |
         ((uint64_t)dtype << 46) | ((uint64_t)p.path << 44) |
         ((uint64_t)p.values_per_thread << 40) |
-        ((uint64_t)(p.chunks & 0xff) << 32) | ((uint64_t)aligned << 31) |
+        ((uint64_t)(p.chunks & 0xff) << 32) | ((uint64_t)mode << 30) |
         (uint64_t)(p.threads_per_row * p.rows_per_block);
     {
         std::lock_guard<std::mutex> lk(g_occ_mu);
@@ -117,7 +117,7 @@ cudaError_t blocks_per_sm(int dev, int op, int dtype, const mt_plan_t &p,
         }
     }
     int n = 0;
-    cudaError_t e = kOcc[op][dtype](p, aligned, &n);
+    cudaError_t e = kOcc[op][dtype](p, mode, &n);
     if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lk(g_occ_mu);
     g_occ[key] = n;
@@ -243,6 +243,19 @@ mt_status run(const Call &c, const mt_plan_t *forced, cudaStream_t stream) {
     a.y_vec = phase(c.y);
     a.h_vec = phase(c.h);
     a.r_vec = phase(c.res);
+    // Whole tiles: every pack of every row exists and every parameter
+    // vector the operator reads is present, so the kernel needs no guard.
+    const bool params =
+        (c.op == OP_RMSNORM || c.op == OP_RESIDUAL_RMSNORM)
+            ? c.w != nullptr
+            : (c.op == OP_LAYERNORM || c.op == OP_RESIDUAL_LAYERNORM)
+                  ? (c.w != nullptr && c.b != nullptr)
+                  : true;
+    const bool full = aligned && params && p.path == MT_PATH_REGISTERS &&
+                      p.cluster <= 1 &&
+                      (int64_t)p.threads_per_row * V * p.chunks == c.cols &&
+                      c.rows % p.rows_per_block == 0;
+    const int mode = full ? KM_FULL : (aligned ? KM_ALIGNED : KM_UNALIGNED);
     a.W = p.threads_per_row;
     int l = 0;
     while ((1 << l) < a.W) ++l;
@@ -263,7 +276,7 @@ mt_status run(const Call &c, const mt_plan_t *forced, cudaStream_t stream) {
         int sms = 0, bps = 0;
         e = sm_count(dev, &sms);
         if (e != cudaSuccess) return cuda_status(e);
-        e = blocks_per_sm(dev, c.op, c.dtype, p, aligned, &bps);
+        e = blocks_per_sm(dev, c.op, c.dtype, p, mode, &bps);
         if (e != cudaSuccess) return cuda_status(e);
         if (bps < 1) return MT_ERR_OUT_OF_RESOURCES;
         grid = (int64_t)sms * bps / C;
@@ -274,7 +287,7 @@ mt_status run(const Call &c, const mt_plan_t *forced, cudaStream_t stream) {
     p.grid = (int32_t)(grid * C);
 
     if (mt_status st =
-            cuda_status(kLaunch[c.op][c.dtype](p, a, aligned, stream)))
+            cuda_status(kLaunch[c.op][c.dtype](p, a, mode, stream)))
         return st;
     if (c.op == OP_CROSS_ENTROPY && c.mean != nullptr)
         return cuda_status(launch_mean(c.out, c.mean, c.rows, c.labels,

@@ -74,15 +74,32 @@ constexpr int kNumChunkSet = 5;
 constexpr int reg_max_threads(int vk) {
     return vk <= 16 ? 1024 : (vk <= 32 ? 512 : 256);
 }
+// Whole-tile kernels issue every load unguarded, so the compiler hoists
+// more of them at once than in the guarded kernels.  For 32 values in
+// packs of 16 bytes a cap of kFullCapRegs registers lets seven 128-thread
+// CTAs share an SM (one wave for 1024 rows of one CTA each); it applies to
+// the operators that fit it without spilling (not the two-parameter
+// LayerNorms, nor residual RMSNorm).
+constexpr int kFullCapRegs = 72;
+constexpr bool reg_full_capped(int op, int vk, int pack_bytes) {
+    return vk == 32 && pack_bytes == 16 && op != MT_OP_LAYERNORM &&
+           op != MT_OP_RESIDUAL_LAYERNORM && op != MT_OP_RESIDUAL_RMSNORM;
+}
 constexpr int kLoopMaxThreads = 512;
 
-// Launchers, one translation unit per (operator, storage type).  `aligned`
-// selects the kernels whose every access of the row body is a V-wide vector
-// access without a head; `plan.grid` is already resolved (> 0).
+// Kernel variants of one plan.  KM_ALIGNED: every access of the row body is
+// a V-wide vector access without a head.  KM_FULL (register path, no
+// cluster): aligned, and every pack of every row exists (cols = W*V*K,
+// rows a multiple of B, every parameter vector present), so the kernel
+// carries no bounds guard at all.
+enum KMode : int { KM_UNALIGNED = 0, KM_ALIGNED = 1, KM_FULL = 2 };
+
+// Launchers, one translation unit per (operator, storage type).  `mode`
+// is a KMode; `plan.grid` is already resolved (> 0).
 #define MT_DECLARE_LAUNCHER(name)                                            \
-    cudaError_t name(const mt_plan_t &plan, const KArgs &a, bool aligned,    \
+    cudaError_t name(const mt_plan_t &plan, const KArgs &a, int mode,        \
                      cudaStream_t stream);                                   \
-    cudaError_t name##_occupancy(const mt_plan_t &plan, bool aligned,        \
+    cudaError_t name##_occupancy(const mt_plan_t &plan, int mode,            \
                                  int *blocks_per_sm);
 #define MT_DECLARE_OP(op)                                                    \
     MT_DECLARE_LAUNCHER(launch_##op##_f32)                                   \

@@ -632,11 +632,13 @@ struct RowGeom {
 // start + head): a vector access for a complete pack when `vec`, otherwise
 // guarded scalars; missing values read as `fill`.  In aligned kernels
 // (AL) cols % V == 0, so a pack is either complete or wholly past the end.
-template <typename T, int V, bool AL>
+template <typename T, int V, bool AL, bool FU = false>
 __device__ __forceinline__ void load_pack(const T *p, int off, int nb,
                                           bool active, bool vec, float fill,
                                           float *d) {
-    if constexpr (AL) {
+    if constexpr (FU) {
+        ld_vec<T, V>(p + off, d);
+    } else if constexpr (AL) {
         if (active && off < nb) {
             ld_vec<T, V>(p + off, d);
         } else {
@@ -657,10 +659,14 @@ __device__ __forceinline__ void load_pack(const T *p, int off, int nb,
     }
 }
 
-template <typename T, int V, bool AL>
+template <typename T, int V, bool AL, bool FU = false>
 __device__ __forceinline__ void store_pack(T *p, int off, int nb,
                                            bool active, bool vec,
                                            const float *d) {
+    if constexpr (FU) {
+        st_vec<T, V>(p + off, d);
+        return;
+    }
     if (!active) return;
     if constexpr (AL) {
         if (off < nb) st_vec<T, V>(p + off, d);
@@ -679,12 +685,15 @@ __device__ __forceinline__ void store_pack(T *p, int off, int nb,
 }
 
 // Parameter pack for the register path: aligned kernels read complete
-// vectors (or nothing past the end), the others guard each element.
-template <typename T, int V, bool AL>
+// vectors (or nothing past the end), the others guard each element; whole-
+// tile kernels (FU) read every pack of a vector that is known to exist.
+template <typename T, int V, bool AL, bool FU = false>
 __device__ __forceinline__ void param_row_pack(const T *p, int col,
                                                int off, int nb, bool active,
                                                float dflt, float *d) {
-    if constexpr (AL) {
+    if constexpr (FU) {
+        ld_vec<T, V, true>(p + col, d);
+    } else if constexpr (AL) {
         if (p != nullptr && active && off < nb) {
             ld_vec<T, V, true>(p + col, d);
         } else {
@@ -700,9 +709,10 @@ __device__ __forceinline__ void param_row_pack(const T *p, int col,
 // =========================================================================
 // Register path
 // =========================================================================
-template <int OP, typename T, int V, int K, bool AL, bool CL>
-__global__ void __launch_bounds__(reg_max_threads(V * K))
-    reg_kernel(const KArgs a) {
+template <int OP, typename T, int V, int K, bool AL, bool CL, bool FU>
+__device__ __forceinline__ void reg_body(const KArgs &a) {
+    static_assert(!FU || (AL && !CL), "whole-tile kernels are aligned, "
+                                      "one CTA per row group");
     kernel_prologue<OP, T, CL>(a);
     __shared__ RedScratch red;
     int parity = 0;
@@ -733,7 +743,7 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
     for (int64_t g = g0; g < ngroups; g += gstride) {
         prefetch_next_group<OP, T>(a, g, ngroups, gstride, rank);
         const int64_t row = g * a.B + slot;
-        const bool active = row < a.rows;
+        const bool active = FU || row < a.rows;
         const RowGeom<T, V, AL> geo(X, active ? row : 0, cols);
         const T *xb = X + geo.base + geo.hd;  // body start
         const int nb = geo.nb;
@@ -744,7 +754,7 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
         float hv = fill;
 #pragma unroll
         for (int k = 0; k < K; ++k)
-            load_pack<T, V, AL>(xb, (k * WT + worker) * V, nb, active, true,
+            load_pack<T, V, AL, FU>(xb, (k * WT + worker) * V, nb, active, true,
                                 fill, v[k]);
         if (head) hv = to_f(X[geo.base + worker]);
 
@@ -755,7 +765,7 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
 #pragma unroll
             for (int k = 0; k < K; ++k) {
                 float t[V];
-                load_pack<T, V, AL>(rb, (k * WT + worker) * V, nb, active,
+                load_pack<T, V, AL, FU>(rb, (k * WT + worker) * V, nb, active,
                                     rvec, 0.f, t);
 #pragma unroll
                 for (int e = 0; e < V; ++e) v[k][e] = __fadd_rn(v[k][e], t[e]);
@@ -767,7 +777,7 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
                 const bool hvec = AL || a.h_vec;
 #pragma unroll
                 for (int k = 0; k < K; ++k)
-                    store_pack<T, V, AL>(hb, (k * WT + worker) * V, nb, active,
+                    store_pack<T, V, AL, FU>(hb, (k * WT + worker) * V, nb, active,
                                          hvec, v[k]);
                 if (head) H[geo.base + worker] = from_f<T>(hv);
             }
@@ -806,11 +816,11 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
             for (int k = 0; k < K; ++k) {
                 const int off = (k * WT + worker) * V;
                 float wv[V], o[V];
-                param_row_pack<T, V, AL>(Wt, geo.hd + off, off, nb, active,
+                param_row_pack<T, V, AL, FU>(Wt, geo.hd + off, off, nb, active,
                                          1.f, wv);
 #pragma unroll
                 for (int e = 0; e < V; ++e) o[e] = v[k][e] * r * wv[e];
-                store_pack<T, V, AL>(yb, off, nb, active, yvec, o);
+                store_pack<T, V, AL, FU>(yb, off, nb, active, yvec, o);
             }
             if (head)
                 Y[geo.base + worker] =
@@ -839,7 +849,7 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
 #pragma unroll
                 for (int e = 0; e < V; ++e) {
                     const float d = v[k][e] - mean;
-                    if (AL ? pack_in : (active && off + e < nb))
+                    if (FU || (AL ? pack_in : (active && off + e < nb)))
                         acc[e] = fmaf(d, d, acc[e]);
                 }
             }
@@ -857,14 +867,14 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
             for (int k = 0; k < K; ++k) {
                 const int off = (k * WT + worker) * V;
                 float gv[V], bv[V], o[V];
-                param_row_pack<T, V, AL>(Wt, geo.hd + off, off, nb, active,
+                param_row_pack<T, V, AL, FU>(Wt, geo.hd + off, off, nb, active,
                                          1.f, gv);
-                param_row_pack<T, V, AL>(Bt, geo.hd + off, off, nb, active,
+                param_row_pack<T, V, AL, FU>(Bt, geo.hd + off, off, nb, active,
                                          0.f, bv);
 #pragma unroll
                 for (int e = 0; e < V; ++e)
                     o[e] = fmaf((v[k][e] - mean) * rstd, gv[e], bv[e]);
-                store_pack<T, V, AL>(yb, off, nb, active, yvec, o);
+                store_pack<T, V, AL, FU>(yb, off, nb, active, yvec, o);
             }
             if (head)
                 Y[geo.base + worker] = from_f<T>(
@@ -907,21 +917,30 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
                 float o[V];
 #pragma unroll
                 for (int e = 0; e < V; ++e) o[e] = v[k][e] * inv;
-                store_pack<T, V, AL>(yb, (k * WT + worker) * V, nb, active,
+                store_pack<T, V, AL, FU>(yb, (k * WT + worker) * V, nb, active,
                                      yvec, o);
             }
             if (head) Y[geo.base + worker] = from_f<T>(hv * inv);
         } else if constexpr (OP == OP_ROW_SUM) {
-            float s = hv, c = 0.f;
+            // Pairwise tree of error-free additions over the thread's V*K
+            // values (independent at every level, so every load is in
+            // flight before the first addition); the rounding errors of
+            // the tree are summed separately and carried as the
+            // compensation term.
+            float c = 0.f;
 #pragma unroll
-            for (int k = 0; k < K; ++k)
+            for (int step = 1; step < K * V; step <<= 1)
 #pragma unroll
-                for (int e = 0; e < V; ++e) {
+                for (int i = 0; i + step < K * V; i += 2 * step) {
                     float t, err;
-                    two_sum(s, v[k][e], t, err);
-                    s = t;
+                    two_sum(v[i / V][i % V], v[(i + step) / V][(i + step) % V],
+                            t, err);
+                    v[i / V][i % V] = t;
                     c += err;
                 }
+            float s, err;
+            two_sum(v[0][0], hv, s, err);
+            c += err;
             team_allreduce_compensated(s, c, W, csize, red, parity, cpar);
             if (active && worker == 0) a.out[row] = s + c;
         } else if constexpr (OP == OP_CROSS_ENTROPY) {
@@ -979,7 +998,7 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
                 float o[V];
 #pragma unroll
                 for (int e = 0; e < V; ++e) o[e] = (v[k][e] - m) - ls;
-                store_pack<T, V, AL>(yb, (k * WT + worker) * V, nb, active,
+                store_pack<T, V, AL, FU>(yb, (k * WT + worker) * V, nb, active,
                                      yvec, o);
             }
             if (head) Y[geo.base + worker] = from_f<T>((hv - m) - ls);
@@ -987,6 +1006,30 @@ __global__ void __launch_bounds__(reg_max_threads(V * K))
     }
     // Peers may still read this CTA's cluster slots.
     if (csize > 1) cluster_sync();
+}
+
+template <int OP, typename T, int V, int K, bool AL, bool CL>
+__global__ void __launch_bounds__(reg_max_threads(V * K))
+    reg_kernel(const KArgs a) {
+    reg_body<OP, T, V, K, AL, CL, false>(a);
+}
+
+// Whole tiles (every pack of every row exists, every parameter vector is
+// present): the same row program with no bounds guard.
+template <int OP, typename T, int V, int K>
+__global__ void __launch_bounds__(reg_max_threads(V * K))
+    reg_full_kernel(const KArgs a) {
+    reg_body<OP, T, V, K, true, false, true>(a);
+}
+
+// The same with a register cap (where reg_full_capped applies; the cap
+// also admits the largest CTA the thread bound allows).
+template <int OP, typename T, int V, int K>
+__global__ void __maxnreg__(kFullCapRegs)
+    reg_full_capped_kernel(const KArgs a) {
+    static_assert(kFullCapRegs * 512 <= 65536,
+                  "the cap must admit the largest CTA (512 threads)");
+    reg_body<OP, T, V, K, true, false, true>(a);
 }
 
 // =========================================================================
@@ -1275,56 +1318,81 @@ __global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
 // =========================================================================
 using KernelFn = void (*)(KArgs);
 
-template <int OP, typename T, int V, bool AL, bool CL>
+template <int OP, typename T, int V, int K>
+__host__ KernelFn full_kernel() {
+    if constexpr (reg_full_capped(OP, V * K, V * (int)sizeof(T)))
+        return reg_full_capped_kernel<OP, T, V, K>;
+    else
+        return reg_full_kernel<OP, T, V, K>;
+}
+
+template <int OP, typename T, int V, bool AL, bool CL, bool FU = false>
 __host__ KernelFn reg_kernel_for_chunks(int K) {
-    switch (K) {
-        case 1: return reg_kernel<OP, T, V, 1, AL, CL>;
-        case 2: return reg_kernel<OP, T, V, 2, AL, CL>;
-        case 4: return reg_kernel<OP, T, V, 4, AL, CL>;
-        case 8: return reg_kernel<OP, T, V, 8, AL, CL>;
-        case 16: return reg_kernel<OP, T, V, 16, AL, CL>;
-        default: return nullptr;
+    if constexpr (FU) {
+        switch (K) {
+            case 1: return full_kernel<OP, T, V, 1>();
+            case 2: return full_kernel<OP, T, V, 2>();
+            case 4: return full_kernel<OP, T, V, 4>();
+            case 8: return full_kernel<OP, T, V, 8>();
+            case 16: return full_kernel<OP, T, V, 16>();
+            default: return nullptr;
+        }
+    } else {
+        switch (K) {
+            case 1: return reg_kernel<OP, T, V, 1, AL, CL>;
+            case 2: return reg_kernel<OP, T, V, 2, AL, CL>;
+            case 4: return reg_kernel<OP, T, V, 4, AL, CL>;
+            case 8: return reg_kernel<OP, T, V, 8, AL, CL>;
+            case 16: return reg_kernel<OP, T, V, 16, AL, CL>;
+            default: return nullptr;
+        }
     }
 }
 
 // A pack of one FP32 value needs no alignment head, so it has only the
 // aligned kernels.  Cluster (split-row) kernels exist for 16-byte packs.
+// Whole-tile register kernels (KM_FULL) exist for one CTA per row group.
 template <int OP, typename T, int V, bool CL>
-__host__ KernelFn kernel_for_cl(const mt_plan_t &p, bool aligned) {
+__host__ KernelFn kernel_for_cl(const mt_plan_t &p, int mode) {
     constexpr bool kOnlyAligned = (V == 1 && sizeof(T) == 4);
+    const bool aligned = kOnlyAligned || mode != KM_UNALIGNED;
     if (p.path == MT_PATH_LOOP) {
-        if (kOnlyAligned || aligned) return loop_kernel<OP, T, V, true, CL>;
+        if (aligned) return loop_kernel<OP, T, V, true, CL>;
         return loop_kernel<OP, T, V, kOnlyAligned, CL>;
     }
-    if (kOnlyAligned || aligned)
-        return reg_kernel_for_chunks<OP, T, V, true, CL>(p.chunks);
+    if constexpr (!CL) {
+        if (mode == KM_FULL)
+            return reg_kernel_for_chunks<OP, T, V, true, false, true>(
+                p.chunks);
+    }
+    if (aligned) return reg_kernel_for_chunks<OP, T, V, true, CL>(p.chunks);
     return reg_kernel_for_chunks<OP, T, V, kOnlyAligned, CL>(p.chunks);
 }
 
 template <int OP, typename T, int V>
-__host__ KernelFn kernel_for(const mt_plan_t &p, bool aligned) {
+__host__ KernelFn kernel_for(const mt_plan_t &p, int mode) {
     if constexpr (V * sizeof(T) == 16) {
-        if (p.cluster > 1) return kernel_for_cl<OP, T, V, true>(p, aligned);
+        if (p.cluster > 1) return kernel_for_cl<OP, T, V, true>(p, mode);
     }
     if (p.cluster > 1) return nullptr;
-    return kernel_for_cl<OP, T, V, false>(p, aligned);
+    return kernel_for_cl<OP, T, V, false>(p, mode);
 }
 
 // Instantiated values per thread per chunk: FP32 V = 1, 2, 4 (4-, 8- and
 // 16-byte packs); FP16/BF16 V = 2, 4, 8 (4-, 8- and 16-byte packs).
 template <int OP, typename T>
-__host__ KernelFn select_kernel(const mt_plan_t &p, bool aligned) {
+__host__ KernelFn select_kernel(const mt_plan_t &p, int mode) {
     if constexpr (sizeof(T) == 4) {
         switch (p.values_per_thread) {
-            case 1: return kernel_for<OP, T, 1>(p, aligned);
-            case 2: return kernel_for<OP, T, 2>(p, aligned);
-            case 4: return kernel_for<OP, T, 4>(p, aligned);
+            case 1: return kernel_for<OP, T, 1>(p, mode);
+            case 2: return kernel_for<OP, T, 2>(p, mode);
+            case 4: return kernel_for<OP, T, 4>(p, mode);
         }
     } else {
         switch (p.values_per_thread) {
-            case 2: return kernel_for<OP, T, 2>(p, aligned);
-            case 4: return kernel_for<OP, T, 4>(p, aligned);
-            case 8: return kernel_for<OP, T, 8>(p, aligned);
+            case 2: return kernel_for<OP, T, 2>(p, mode);
+            case 4: return kernel_for<OP, T, 4>(p, mode);
+            case 8: return kernel_for<OP, T, 8>(p, mode);
         }
     }
     return nullptr;
@@ -1332,8 +1400,8 @@ __host__ KernelFn select_kernel(const mt_plan_t &p, bool aligned) {
 
 template <int OP, typename T>
 __host__ cudaError_t launch_op(const mt_plan_t &p, const KArgs &a,
-                               bool aligned, cudaStream_t stream) {
-    KernelFn k = select_kernel<OP, T>(p, aligned);
+                               int mode, cudaStream_t stream) {
+    KernelFn k = select_kernel<OP, T>(p, mode);
     if (k == nullptr) return cudaErrorInvalidValue;
     cudaLaunchAttribute attr[2];
     unsigned n = 0;
@@ -1366,9 +1434,9 @@ __host__ cudaError_t launch_op(const mt_plan_t &p, const KArgs &a,
 }
 
 template <int OP, typename T>
-__host__ cudaError_t occupancy_op(const mt_plan_t &p, bool aligned,
+__host__ cudaError_t occupancy_op(const mt_plan_t &p, int mode,
                                   int *blocks_per_sm) {
-    KernelFn k = select_kernel<OP, T>(p, aligned);
+    KernelFn k = select_kernel<OP, T>(p, mode);
     if (k == nullptr) return cudaErrorInvalidValue;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
         blocks_per_sm, k, p.threads_per_row * p.rows_per_block, 0);
@@ -1380,12 +1448,12 @@ __host__ cudaError_t occupancy_op(const mt_plan_t &p, bool aligned,
 // pair through this macro.
 #define MT_DEFINE_LAUNCHER(name, OPV, TYPE)                                  \
     namespace mt {                                                           \
-    cudaError_t name(const mt_plan_t &plan, const KArgs &a, bool aligned,    \
+    cudaError_t name(const mt_plan_t &plan, const KArgs &a, int mode,        \
                      cudaStream_t stream) {                                  \
-        return launch_op<OPV, TYPE>(plan, a, aligned, stream);               \
+        return launch_op<OPV, TYPE>(plan, a, mode, stream);                  \
     }                                                                        \
-    cudaError_t name##_occupancy(const mt_plan_t &plan, bool aligned,        \
+    cudaError_t name##_occupancy(const mt_plan_t &plan, int mode,            \
                                  int *blocks_per_sm) {                       \
-        return occupancy_op<OPV, TYPE>(plan, aligned, blocks_per_sm);        \
+        return occupancy_op<OPV, TYPE>(plan, mode, blocks_per_sm);           \
     }                                                                        \
     }

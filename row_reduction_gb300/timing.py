@@ -196,22 +196,53 @@ def _replay_for(graph, stream, seconds, until=None, max_seconds=5.0):
             return
 
 
+# Largest K timed as one graph (spacer, K steps and both timing events in a
+# single CUDA graph); longer runs replay graphs of whole pool cycles.
+MAX_ONE_GRAPH_STEPS = 4096
+
+
+def _graph_with_events(work, spacer, steps, stream, start, end, plan=None):
+    """One CUDA graph: `spacer` untimed steps, then `steps` timed steps,
+    with the timing events as graph nodes.  The start event hangs off a
+    side branch that depends on the last untimed step, so the chain of
+    programmatic dependent launches through the timed steps is never broken
+    by it: the window runs from the completion of the last untimed step to
+    the completion of the last timed step, which is `steps` steps of the
+    steady chain."""
+    import torch
+    side = torch.cuda.Stream()
+    fork = torch.cuda.Event()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        cur = torch.cuda.current_stream()
+        h = cur.cuda_stream
+        for i in range(spacer):
+            work.call_fn(i, h, plan)()
+        fork.record(cur)
+        side.wait_event(fork)
+        start.record(side)
+        for i in range(steps):
+            work.call_fn(spacer + i, h, plan)()
+        end.record(cur)
+        cur.wait_stream(side)
+    return g
+
+
 def time_graph_steps(work, steps, warmup, plan=None, per_graph=64,
                      barrier=None, sampler=None, load_s=0.3):
     """Device seconds for exactly `steps` steps (after at least `warmup`
     steps), replayed from CUDA graphs.
 
     The timed region is bracketed by a synchronize (and `barrier`, when
-    given) on both sides.  After the first synchronize one untimed replay is
-    enqueued ahead of the start event, so the GPU is busy while the host
-    enqueues the timed replays: the start event then marks the first timed
-    step, not the host's graph-launch latency.  The spacer is a graph of
-    its own, so the timed graph is not a relaunch of the one still
-    running.  With `sampler` (an object
-    with start(), stop() and has_samples(n)), the GPU also runs the same steps
-    for `load_s` seconds before and after the timed region (before: until
-    the sampler holds at least two samples), so clock samples are taken
-    under the timed load."""
+    given) on both sides.  Up to MAX_ONE_GRAPH_STEPS steps are timed inside
+    one graph that first runs a pool cycle of untimed steps
+    (_graph_with_events), so the timed steps follow a busy GPU and their
+    launch chain is unbroken.  Longer runs record the start event after an
+    untimed graph (a spacer) and replay graphs of whole pool cycles.  With
+    `sampler` (an object with start(), stop() and has_samples(n)), the GPU
+    also runs the same steps for `load_s` seconds before and after the
+    timed region (before: until the sampler holds at least two samples),
+    so clock samples are taken under the timed load."""
     import torch
     stream = torch.cuda.Stream()
     h = stream.cuda_stream
@@ -219,33 +250,44 @@ def time_graph_steps(work, steps, warmup, plan=None, per_graph=64,
         for i in range(3):              # fill the library's per-device caches
             work.call_fn(i, h, plan)()
     stream.synchronize()
+    start = torch.cuda.Event(enable_timing=True, external=True)
+    end = torch.cuda.Event(enable_timing=True, external=True)
     G = min(graph_size(work, per_graph), max(1, steps))
-    full = _graph_of(work, G, stream, plan)
-    rem = steps % G
-    tail = _graph_of(work, rem, stream, plan) if rem else None
     spacer = _graph_of(work, graph_size(work, per_graph), stream, plan)
+    one = None
+    full = tail = None
+    if steps <= MAX_ONE_GRAPH_STEPS:
+        one = _graph_with_events(work, graph_size(work, per_graph), steps,
+                                 stream, start, end, plan)
+    else:
+        full = _graph_of(work, G, stream, plan)
+        rem = steps % G
+        tail = _graph_of(work, rem, stream, plan) if rem else None
+    warm = full if full is not None else spacer
     with torch.cuda.stream(stream):
-        for _ in range(max(1, math.ceil(warmup / G))):
-            full.replay()
+        for _ in range(max(1, math.ceil(warmup / graph_size(work,
+                                                            per_graph)))):
+            warm.replay()
         spacer.replay()
     stream.synchronize()
     if sampler is not None:
         sampler.start()
         _replay_for(spacer, stream, load_s,
                     until=lambda: sampler.has_samples(2))
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     if barrier:
         barrier()
     with torch.cuda.stream(stream):
-        spacer.replay()                 # untimed
-        start.record(stream)
-        for _ in range(steps // G):
-            full.replay()
-        if tail is not None:
-            tail.replay()
-        end.record(stream)
+        if one is not None:
+            one.replay()
+        else:
+            spacer.replay()             # untimed
+            start.record(stream)
+            for _ in range(steps // G):
+                full.replay()
+            if tail is not None:
+                tail.replay()
+            end.record(stream)
     end.synchronize()
     torch.cuda.synchronize()
     if barrier:

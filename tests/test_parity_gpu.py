@@ -255,6 +255,44 @@ def test_mapping_matrix(op, cols):
                     f"{mt.mt_describe_plan(p)}")
 
 
+# ------------------------------------------------ whole-tile kernels
+# Plans whose packs tile every row exactly (cols = W*V*K) run, when rows is
+# a multiple of B and every parameter vector is present, the unguarded
+# whole-tile kernels; one more row (no longer a multiple of B) sends the
+# same plan to the guarded kernel.  (cols, W, V, K, B):
+WHOLE_TILES = [(128, 32, 4, 1, 4), (512, 128, 1, 4, 2), (1024, 64, 4, 4, 2),
+               (2048, 256, 2, 4, 2), (4096, 128, 4, 8, 2),
+               (4096, 256, 4, 4, 2), (4096, 64, 4, 16, 2),
+               (8192, 512, 4, 4, 2)]
+
+
+def _first_rows(d, n):
+    return {k: (v[:n] if isinstance(v, np.ndarray) and k in
+                ("x", "residual", "labels") else v) for k, v in d.items()}
+
+
+@pytest.mark.parametrize("op", OPS)
+def test_whole_tile_kernels(op):
+    """The whole-tile kernels agree with the oracle, and bit for bit with
+    the guarded kernel of the same plan on the same rows."""
+    rows = 6
+    for cols, W, V, K, B in WHOLE_TILES:
+        p = mt.make_plan(W, V, K, B)
+        assert mt.mt_plan_check(mt.OP_IDS[op], cols, p) == mt.MT_OK
+        d = inputs.make(op, rows + 1, cols, SEED + 7 * cols + W)
+        d6 = _first_rows(d, rows)
+        what = f"{op} {rows}x{cols} {mt.mt_describe_plan(p)}"
+        full = run_guarded(op, d6, rows, cols, plan=p)
+        compare(op, full, oracle.run(op, d6), what + " (whole tiles)")
+        guarded = run_guarded(op, d, rows + 1, cols, plan=p)
+        for k in full:
+            if k == "mean_loss":
+                continue
+            a, b = full[k], guarded[k][:rows]
+            assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), \
+                f"{what}: {k} differs from the guarded kernel"
+
+
 # --------------------------------------- alignment heads and guards
 @pytest.mark.parametrize("op", OPS)
 @pytest.mark.parametrize("cols", [3, 127, 257, 4096, 4103])
@@ -317,6 +355,35 @@ def test_row_sum_near_zero_rows():
     ref = oracle.row_sum(x)
     got = mt.row_sum(torch.from_numpy(x).cuda()).cpu().numpy()
     assert_close(got, ref, "near-zero sums")
+
+
+def test_row_sum_cancelling_pairs():
+    """Rows of large values whose exact negatives sit elsewhere in the row
+    (magnitudes up to ~4e4), plus a residue of 1e-3: the exact sum is the
+    residue, far below the rounding error of a plain FP32 sum of the row.
+    Every plan family (register path, loop path, whole tiles) must keep the
+    1e-5*(1+|ref|) tolerance."""
+    rng = np.random.default_rng(SEED + 99)
+    for rows, cols in ((32, 4096), (16, 4098), (4, 100003)):
+        x = np.zeros((rows, cols), np.float32)
+        for r in range(rows):
+            half = (cols - 1) // 2
+            big = (rng.standard_normal(half) * 1e4).astype(np.float32)
+            perm = rng.permutation(cols)
+            x[r, perm[:half]] = big
+            x[r, perm[half:2 * half]] = -big
+            x[r, perm[-1]] = np.float32(1e-3) * (r + 1)
+        ref = oracle.row_sum(x)
+        xt = torch.from_numpy(x).cuda()
+        plans = [None]
+        if cols == 4096:
+            plans += [mt.make_plan(128, 4, 8, 1), mt.make_plan(64, 4, 16, 2),
+                      mt.make_plan(256, 2, 8, 1), mt.make_plan(1024, 4, 1, 1),
+                      mt.make_plan(128, 4, 0, 2, mt.MT_PATH_LOOP)]
+        for p in plans:
+            got = mt.row_sum(xt, plan=p).cpu().numpy()
+            assert_close(got, ref, f"cancelling pairs {rows}x{cols} "
+                         f"{mt.mt_describe_plan(p) if p else 'default'}")
 
 
 def test_residual_h_out_bit_exact_and_aliasing():
