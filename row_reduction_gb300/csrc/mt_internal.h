@@ -81,9 +81,12 @@ constexpr int reg_max_threads(int vk) {
 // the operators that fit it without spilling (not the two-parameter
 // LayerNorms, nor residual RMSNorm).
 constexpr int kFullCapRegs = 72;
-constexpr bool reg_full_capped(int op, int vk, int pack_bytes) {
-    return vk == 32 && pack_bytes == 16 && op != MT_OP_LAYERNORM &&
-           op != MT_OP_RESIDUAL_LAYERNORM && op != MT_OP_RESIDUAL_RMSNORM;
+constexpr bool reg_full_capped(int op, int vk, int pack_bytes,
+                               int elem_bytes) {
+    return vk == 32 && pack_bytes == 16 &&
+           (elem_bytes == 2 || (op != MT_OP_LAYERNORM &&
+                                op != MT_OP_RESIDUAL_LAYERNORM &&
+                                op != MT_OP_RESIDUAL_RMSNORM));
 }
 constexpr int kLoopMaxThreads = 512;
 

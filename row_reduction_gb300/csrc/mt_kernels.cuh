@@ -849,6 +849,9 @@ __device__ __forceinline__ void reg_body(const KArgs &a) {
 #pragma unroll
                 for (int e = 0; e < V; ++e) {
                     const float d = v[k][e] - mean;
+                    // Whole tiles keep the deviation in place of the value
+                    // (the epilogue forms the same bits from it).
+                    if constexpr (FU) v[k][e] = d;
                     if (FU || (AL ? pack_in : (active && off + e < nb)))
                         acc[e] = fmaf(d, d, acc[e]);
                 }
@@ -873,7 +876,8 @@ __device__ __forceinline__ void reg_body(const KArgs &a) {
                                          0.f, bv);
 #pragma unroll
                 for (int e = 0; e < V; ++e)
-                    o[e] = fmaf((v[k][e] - mean) * rstd, gv[e], bv[e]);
+                    o[e] = fmaf((FU ? v[k][e] : v[k][e] - mean) * rstd,
+                                gv[e], bv[e]);
                 store_pack<T, V, AL, FU>(yb, off, nb, active, yvec, o);
             }
             if (head)
@@ -1320,7 +1324,8 @@ using KernelFn = void (*)(KArgs);
 
 template <int OP, typename T, int V, int K>
 __host__ KernelFn full_kernel() {
-    if constexpr (reg_full_capped(OP, V * K, V * (int)sizeof(T)))
+    if constexpr (reg_full_capped(OP, V * K, V * (int)sizeof(T),
+                                  (int)sizeof(T)))
         return reg_full_capped_kernel<OP, T, V, K>;
     else
         return reg_full_kernel<OP, T, V, K>;
