@@ -112,7 +112,20 @@ typedef enum mt_path {
     /* Rows too wide for registers: a strided loop computes the statistics
      * and a second (LayerNorm: third) loop re-reads x to write y.  Row sum
      * and cross-entropy need only the first loop. */
-    MT_PATH_LOOP = 1
+    MT_PATH_LOOP = 1,
+    /* Rows staged in shared memory: each CTA (of a cluster of
+     * `cluster` CTAs per row) copies its contiguous run of the row, at most
+     * 200 KiB, into shared memory with `chunks` bulk asynchronous copies
+     * (1, 2, 4 or 8 pieces), computes the statistics from shared memory and
+     * writes y from it, so x is read from global memory once.  Inside the
+     * run, 16-byte units go round robin to the W threads.  For RMSNorm,
+     * LayerNorm, softmax, log-softmax, cross-entropy and row sum; 16-byte
+     * units (V*element size = 16), rows_per_block = 1, W >= 32, and rows
+     * that start on 16-byte boundaries (cols a multiple of V, 16-byte
+     * aligned pointers): a forced staged plan on other rows returns
+     * MT_ERR_INVALID_ARGUMENT, and a staged plan from the table gives way
+     * to the loop path there. */
+    MT_PATH_STAGE = 2
 } mt_path;
 
 /* One launch configuration ("plan").  In the pages' notation W =
@@ -128,7 +141,9 @@ typedef struct mt_plan {
                                   access) */
     int32_t chunks;            /* register path: chunks held per thread, one
                                   of 1, 2, 4, 8, 16; W*V*chunks >= cols.
-                                  Loop path: ignored (set 0). */
+                                  Staged path: bulk copies per CTA run (1,
+                                  2, 4 or 8).  Loop path: ignored (set
+                                  0). */
     int32_t rows_per_block;    /* B >= 1 rows per CTA; W*B threads per CTA,
                                   a multiple of 32 and <= 1024 */
     int32_t path;              /* mt_path */
@@ -441,6 +456,14 @@ MT_API const char *mt_status_string(mt_status status);
 /* The cudaError_t behind the calling thread's last MT_ERR_CUDA (0 if
  * none). */
 MT_API int mt_last_cuda_error(void);
+
+/* Diagnostic of the staged path (no counterpart on the pages): *count =
+ * the number of waits for a bulk copy into shared memory that gave up
+ * (after about two seconds) on the current device since the library was
+ * loaded; 0 unless something else has gone wrong on the device.  A kernel
+ * that gives up leaves its outputs undefined but returns.  Synchronous (a
+ * device-to-host copy per kernel family); not for hot paths. */
+MT_API mt_status mt_stage_wait_timeouts(uint64_t *count);
 
 #ifdef __cplusplus
 }

@@ -13,7 +13,7 @@ from ._binding import (  # noqa: F401
     EXPORTS, LIB_PATH, MT_ERR_CUDA, MT_ERR_INVALID_ARGUMENT,
     MT_ERR_OUT_OF_RESOURCES, MT_ERR_UNSUPPORTED, MT_OK, MT_OP_CROSS_ENTROPY,
     MT_OP_LAYERNORM, MT_OP_RESIDUAL_LAYERNORM, MT_OP_RMSNORM, MT_OP_ROW_SUM,
-    MT_OP_SOFTMAX, MT_PATH_LOOP, MT_PATH_REGISTERS, MT_PLAN_PDL,
+    MT_OP_SOFTMAX, MT_PATH_LOOP, MT_PATH_REGISTERS, MT_PATH_STAGE, MT_PLAN_PDL,
     MT_PLAN_PREFETCH_NEXT, OP_IDS, DTYPE_IDS, MT_DTYPE_F32, MT_DTYPE_F16,
     MT_DTYPE_BF16, MTError, MtPlan, dtype_of, mt_row_reduce_with_plan,
     mt_plan_query_dtype, mt_plan_check_dtype, mt_rmsnorm_f16,
@@ -28,7 +28,8 @@ from ._binding import (  # noqa: F401
     mt_cross_entropy_ignore_f32, mt_cross_entropy_ignore_f16,
     mt_cross_entropy_ignore_bf16,
     lib, make_plan, mt_cross_entropy_f32, mt_cross_entropy_f32_with_plan,
-    mt_describe_plan, mt_last_cuda_error, mt_layernorm_f32,
+    mt_describe_plan, mt_last_cuda_error, mt_stage_wait_timeouts,
+    mt_layernorm_f32,
     mt_layernorm_f32_with_plan, mt_plan_check, mt_plan_query,
     mt_private_slot_bound, mt_residual_layernorm_f32,
     mt_residual_layernorm_f32_with_plan, mt_rmsnorm_f32,

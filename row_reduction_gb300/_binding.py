@@ -44,6 +44,7 @@ DTYPE_IDS = {"f32": 0, "f16": 1, "bf16": 2}
 
 MT_PATH_REGISTERS = 0
 MT_PATH_LOOP = 1
+MT_PATH_STAGE = 2
 
 MT_PLAN_PDL = 1
 MT_PLAN_PREFETCH_NEXT = 2
@@ -58,6 +59,7 @@ EXPORTS = (
     "mt_cross_entropy_f32", "mt_cross_entropy_f32_with_plan",
     "mt_plan_query", "mt_plan_check", "mt_private_slot_bound",
     "mt_describe_plan", "mt_status_string", "mt_last_cuda_error",
+    "mt_stage_wait_timeouts",
     "mt_rmsnorm_f16", "mt_rmsnorm_bf16", "mt_layernorm_f16",
     "mt_layernorm_bf16", "mt_residual_layernorm_f16",
     "mt_residual_layernorm_bf16", "mt_softmax_f16", "mt_softmax_bf16",
@@ -161,6 +163,7 @@ def lib() -> ctypes.CDLL:
                 "mt_probe_copy": [P, P, I64, I32, I32, I32, I32, P],
                 "mt_probe_read": [P, I64, P, I64, I32, I32, I32, I32, P],
                 "mt_probe_empty": [I32, I32, P],
+                "mt_stage_wait_timeouts": [ctypes.POINTER(ctypes.c_uint64)],
             }
             for dt in ("f16", "bf16"):
                 sig.update({
@@ -464,6 +467,15 @@ mt_status_string = status_string
 
 def mt_last_cuda_error() -> int:
     return lib().mt_last_cuda_error()
+
+
+def mt_stage_wait_timeouts() -> int:
+    """Waits of the staged path that gave up on the current device (a
+    diagnostic; synchronous)."""
+    n = ctypes.c_uint64(0)
+    _check(lib().mt_stage_wait_timeouts(ctypes.byref(n)),
+           "mt_stage_wait_timeouts")
+    return n.value
 
 
 def mt_probe_copy(src, dst, nbytes, threads=512, unroll=4, grid=0,

@@ -30,6 +30,24 @@ std::mutex g_nonportable_mu;
 std::unordered_set<uint64_t> g_nonportable;
 }  // namespace
 
+std::mutex g_stage_smem_mu;
+std::unordered_set<uint64_t> g_stage_smem;
+
+cudaError_t allow_stage_smem(const void *kernel) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t key = (reinterpret_cast<uintptr_t>(kernel) << 8) ^
+                         (uint64_t)(dev & 0xff);
+    std::lock_guard<std::mutex> lk(g_stage_smem_mu);
+    if (g_stage_smem.count(key)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kStageMaxRunBytes);
+    if (e == cudaSuccess) g_stage_smem.insert(key);
+    return e;
+}
+
 cudaError_t allow_nonportable_cluster(const void *kernel) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -76,7 +94,7 @@ cudaError_t sm_count(int dev, int *out) {
 
 typedef cudaError_t (*LaunchFn)(const mt_plan_t &, const KArgs &, int,
                                 cudaStream_t);
-typedef cudaError_t (*OccFn)(const mt_plan_t &, int, int *);
+typedef cudaError_t (*OccFn)(const mt_plan_t &, int, int64_t, int *);
 
 #define MT_ROW(op)                                                           \
     {launch_##op##_f32, launch_##op##_f16, launch_##op##_bf16}
@@ -93,21 +111,39 @@ const OccFn kOcc[OP_COUNT][DT_COUNT] = {
     MT_OCC_ROW(residual_layernorm), MT_OCC_ROW(softmax),
     MT_OCC_ROW(row_sum),       MT_OCC_ROW(cross_entropy),
     MT_OCC_ROW(residual_rmsnorm), MT_OCC_ROW(log_softmax)};
+typedef cudaError_t (*TimeoutFn)(unsigned long long *);
+#define MT_TO_ROW(op)                                                        \
+    {launch_##op##_f32_timeouts, launch_##op##_f16_timeouts,                 \
+     launch_##op##_bf16_timeouts}
+const TimeoutFn kTimeouts[OP_COUNT][DT_COUNT] = {
+    MT_TO_ROW(rmsnorm),       MT_TO_ROW(layernorm),
+    MT_TO_ROW(residual_layernorm), MT_TO_ROW(softmax),
+    MT_TO_ROW(row_sum),       MT_TO_ROW(cross_entropy),
+    MT_TO_ROW(residual_rmsnorm), MT_TO_ROW(log_softmax)};
 #undef MT_ROW
 #undef MT_OCC_ROW
+#undef MT_TO_ROW
 
 // Resident CTAs per SM for a (device, op, dtype, kernel variant, block).
 std::mutex g_occ_mu;
 std::unordered_map<uint64_t, int> g_occ;
 
 cudaError_t blocks_per_sm(int dev, int op, int dtype, const mt_plan_t &p,
-                          int mode, int *out) {
+                          int mode, int64_t cols, int *out) {
+    // Staged plans: the shared memory of a run (whole KiB) and the cluster
+    // size join the key.
+    uint64_t stage = 0;
+    if (p.path == MT_PATH_STAGE)
+        stage = ((uint64_t)(stage_run_bytes(cols, dtype_size(dtype),
+                                            p.cluster > 1 ? p.cluster : 1) /
+                            1024) << 11) |
+                (uint64_t)(p.cluster & 31) << 19;
     const uint64_t key =
         ((uint64_t)(dev & 0xff) << 56) | ((uint64_t)op << 50) |
         ((uint64_t)dtype << 46) | ((uint64_t)p.path << 44) |
         ((uint64_t)p.values_per_thread << 40) |
         ((uint64_t)(p.chunks & 0xff) << 32) | ((uint64_t)mode << 30) |
-        (uint64_t)(p.threads_per_row * p.rows_per_block);
+        (uint64_t)(p.threads_per_row * p.rows_per_block) | stage;
     {
         std::lock_guard<std::mutex> lk(g_occ_mu);
         auto it = g_occ.find(key);
@@ -117,7 +153,7 @@ cudaError_t blocks_per_sm(int dev, int op, int dtype, const mt_plan_t &p,
         }
     }
     int n = 0;
-    cudaError_t e = kOcc[op][dtype](p, mode, &n);
+    cudaError_t e = kOcc[op][dtype](p, mode, cols, &n);
     if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lk(g_occ_mu);
     g_occ[key] = n;
@@ -233,6 +269,17 @@ mt_status run(const Call &c, const mt_plan_t *forced, cudaStream_t stream) {
     const bool aligned = (V == 1 && es == 4) ||
                          (c.cols % V == 0 && al(c.x) && al(c.y) &&
                           al(c.res) && al(c.h) && al(c.w) && al(c.b));
+    // The staged path copies rows with 16-byte bulk copies, so it needs
+    // aligned rows.  A forced staged plan on other rows is refused; the
+    // table's staged plan gives way to the loop path with the same threads
+    // (at most the loop path's limit), cluster and flags.
+    if (p.path == MT_PATH_STAGE && !aligned) {
+        if (forced != nullptr) return MT_ERR_INVALID_ARGUMENT;
+        p.path = MT_PATH_LOOP;
+        p.chunks = 0;
+        if (p.threads_per_row > kLoopMaxThreads)
+            p.threads_per_row = kLoopMaxThreads;
+    }
     // Unaligned kernels: a pointer keeps x's phase when its distance from x
     // is a multiple of V elements; then its row bodies are aligned too.
     auto phase = [&](const void *q) -> int32_t {
@@ -264,6 +311,7 @@ mt_status run(const Call &c, const mt_plan_t *forced, cudaStream_t stream) {
     a.pdl = (p.flags & MT_PLAN_PDL) ? 1 : 0;
     a.prefetch_next = (p.flags & MT_PLAN_PREFETCH_NEXT) ? 1 : 0;
     a.csize = p.cluster > 1 ? p.cluster : 1;
+    a.pieces = p.path == MT_PATH_STAGE ? p.chunks : 0;
     const int64_t C = a.csize;
 
     // Row groups are processed by CTAs, or by clusters of C CTAs.
@@ -276,7 +324,7 @@ mt_status run(const Call &c, const mt_plan_t *forced, cudaStream_t stream) {
         int sms = 0, bps = 0;
         e = sm_count(dev, &sms);
         if (e != cudaSuccess) return cuda_status(e);
-        e = blocks_per_sm(dev, c.op, c.dtype, p, mode, &bps);
+        e = blocks_per_sm(dev, c.op, c.dtype, p, mode, c.cols, &bps);
         if (e != cudaSuccess) return cuda_status(e);
         if (bps < 1) return MT_ERR_OUT_OF_RESOURCES;
         grid = (int64_t)sms * bps / C;
@@ -595,5 +643,18 @@ const char *mt_status_string(mt_status s) {
 }
 
 int mt_last_cuda_error(void) { return g_last_cuda_error; }
+
+mt_status mt_stage_wait_timeouts(uint64_t *count) {
+    if (count == nullptr) return MT_ERR_INVALID_ARGUMENT;
+    uint64_t total = 0;
+    for (int op = 0; op < OP_COUNT; ++op)
+        for (int dt = 0; dt < DT_COUNT; ++dt) {
+            unsigned long long n = 0;
+            if (mt_status st = cuda_status(kTimeouts[op][dt](&n))) return st;
+            total += n;
+        }
+    *count = total;
+    return MT_OK;
+}
 
 }  // extern "C"

@@ -62,6 +62,8 @@ struct KArgs {
     int32_t prefetch_next;
     // CTAs per row (thread-block cluster size; 1 = no cluster).
     int32_t csize;
+    // Staged path: bulk copies (and barriers) per CTA's run of the row.
+    int32_t pieces;
 };
 
 // Instantiated register-path chunk counts.
@@ -89,6 +91,21 @@ constexpr bool reg_full_capped(int op, int vk, int pack_bytes,
                                 op != MT_OP_RESIDUAL_RMSNORM));
 }
 constexpr int kLoopMaxThreads = 512;
+// Staged path: largest run of a row one CTA stages in shared memory (bytes)
+// and the most bulk-copy pieces per run.
+constexpr int64_t kStageMaxRunBytes = 200 * 1024;
+constexpr int kStagePiecesMax = 8;
+// Bytes of shared memory a staged CTA needs for one run of a row of `cols`
+// elements of `elem` bytes split over `csize` CTAs.
+inline int64_t stage_run_bytes(int64_t cols, int elem, int64_t csize) {
+    const int64_t units = cols * elem / 16;
+    return (units + csize - 1) / csize * 16;
+}
+inline bool stage_op(int op) {
+    return op == MT_OP_RMSNORM || op == MT_OP_LAYERNORM ||
+           op == MT_OP_SOFTMAX || op == MT_OP_LOG_SOFTMAX ||
+           op == MT_OP_CROSS_ENTROPY || op == MT_OP_ROW_SUM;
+}
 
 // Kernel variants of one plan.  KM_ALIGNED: every access of the row body is
 // a V-wide vector access without a head.  KM_FULL (register path, no
@@ -103,7 +120,8 @@ enum KMode : int { KM_UNALIGNED = 0, KM_ALIGNED = 1, KM_FULL = 2 };
     cudaError_t name(const mt_plan_t &plan, const KArgs &a, int mode,        \
                      cudaStream_t stream);                                   \
     cudaError_t name##_occupancy(const mt_plan_t &plan, int mode,            \
-                                 int *blocks_per_sm);
+                                 int64_t cols, int *blocks_per_sm);          \
+    cudaError_t name##_timeouts(unsigned long long *n);
 #define MT_DECLARE_OP(op)                                                    \
     MT_DECLARE_LAUNCHER(launch_##op##_f32)                                   \
     MT_DECLARE_LAUNCHER(launch_##op##_f16)                                   \
@@ -134,6 +152,9 @@ mt_status status_from_cuda(cudaError_t e);
 // the current device.  The attribute is set on the first call for each
 // (device, kernel) and remembered, so later launches make no driver call.
 cudaError_t allow_nonportable_cluster(const void *kernel);
+// Lets a staged-path `kernel` take kStageMaxRunBytes of dynamic shared
+// memory on the current device (set once per device and kernel, likewise).
+cudaError_t allow_stage_smem(const void *kernel);
 
 // Planner (planner.cpp).
 mt_status plan_lookup(int op, int dtype, int64_t rows, int64_t cols,

@@ -1317,6 +1317,12 @@ __global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
     if (csize > 1) cluster_sync();
 }
 
+}  // namespace mt
+
+#include "mt_stage.cuh"
+
+namespace mt {
+
 // =========================================================================
 // Launch helpers
 // =========================================================================
@@ -1361,6 +1367,13 @@ template <int OP, typename T, int V, bool CL>
 __host__ KernelFn kernel_for_cl(const mt_plan_t &p, int mode) {
     constexpr bool kOnlyAligned = (V == 1 && sizeof(T) == 4);
     const bool aligned = kOnlyAligned || mode != KM_UNALIGNED;
+    if (p.path == MT_PATH_STAGE) {
+        // Staged runs: 16-byte units, aligned rows.
+        if constexpr (stage_supported<OP>() && V * sizeof(T) == 16) {
+            if (aligned) return stage_kernel<OP, T, CL>;
+        }
+        return nullptr;
+    }
     if (p.path == MT_PATH_LOOP) {
         if (aligned) return loop_kernel<OP, T, V, true, CL>;
         return loop_kernel<OP, T, V, kOnlyAligned, CL>;
@@ -1421,6 +1434,12 @@ __host__ cudaError_t launch_op(const mt_plan_t &p, const KArgs &a,
                 allow_nonportable_cluster(reinterpret_cast<const void *>(k)))
             return e;
     }
+    size_t smem = 0;
+    if (p.path == MT_PATH_STAGE) {
+        smem = (size_t)stage_run_bytes(a.cols, (int)sizeof(T), a.csize);
+        if (cudaError_t e = allow_stage_smem(reinterpret_cast<const void *>(k)))
+            return e;
+    }
     if (a.csize > 1) {
         attr[n].id = cudaLaunchAttributeClusterDimension;
         attr[n].val.clusterDim.x = (unsigned)a.csize;
@@ -1431,7 +1450,7 @@ __host__ cudaError_t launch_op(const mt_plan_t &p, const KArgs &a,
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.grid);
     cfg.blockDim = dim3((unsigned)(p.threads_per_row * p.rows_per_block));
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = n ? attr : nullptr;
     cfg.numAttrs = n;
@@ -1439,12 +1458,19 @@ __host__ cudaError_t launch_op(const mt_plan_t &p, const KArgs &a,
 }
 
 template <int OP, typename T>
-__host__ cudaError_t occupancy_op(const mt_plan_t &p, int mode,
+__host__ cudaError_t occupancy_op(const mt_plan_t &p, int mode, int64_t cols,
                                   int *blocks_per_sm) {
     KernelFn k = select_kernel<OP, T>(p, mode);
     if (k == nullptr) return cudaErrorInvalidValue;
+    size_t smem = 0;
+    if (p.path == MT_PATH_STAGE) {
+        smem = (size_t)stage_run_bytes(cols, (int)sizeof(T),
+                                       p.cluster > 1 ? p.cluster : 1);
+        if (cudaError_t e = allow_stage_smem(reinterpret_cast<const void *>(k)))
+            return e;
+    }
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        blocks_per_sm, k, p.threads_per_row * p.rows_per_block, 0);
+        blocks_per_sm, k, p.threads_per_row * p.rows_per_block, smem);
 }
 
 }  // namespace mt
@@ -1458,7 +1484,10 @@ __host__ cudaError_t occupancy_op(const mt_plan_t &p, int mode,
         return launch_op<OPV, TYPE>(plan, a, mode, stream);                  \
     }                                                                        \
     cudaError_t name##_occupancy(const mt_plan_t &plan, int mode,            \
-                                 int *blocks_per_sm) {                       \
-        return occupancy_op<OPV, TYPE>(plan, mode, blocks_per_sm);           \
+                                 int64_t cols, int *blocks_per_sm) {         \
+        return occupancy_op<OPV, TYPE>(plan, mode, cols, blocks_per_sm);     \
+    }                                                                        \
+    cudaError_t name##_timeouts(unsigned long long *n) {                     \
+        return cudaMemcpyFromSymbol(n, g_stage_timeouts, sizeof(*n));        \
     }                                                                        \
     }

@@ -330,6 +330,15 @@ mt_status plan_check_impl(int op, int dtype, int64_t cols, const mt_plan_t &p) {
             return MT_ERR_OUT_OF_RESOURCES;
     } else if (p.path == MT_PATH_LOOP) {
         if (threads > kLoopMaxThreads) return MT_ERR_OUT_OF_RESOURCES;
+    } else if (p.path == MT_PATH_STAGE) {
+        // One row per CTA (or cluster), 16-byte units, W >= 32, 1..8 bulk
+        // copies per run, a run that fits the shared-memory budget.
+        if (!stage_op(op) || B != 1 || W < 32 ||
+            V * dtype_size(dtype) != 16 || p.chunks < 1 ||
+            p.chunks > kStagePiecesMax || !is_pow2(p.chunks))
+            return MT_ERR_INVALID_ARGUMENT;
+        if (stage_run_bytes(cols, dtype_size(dtype), C) > kStageMaxRunBytes)
+            return MT_ERR_OUT_OF_RESOURCES;
     } else {
         return MT_ERR_INVALID_ARGUMENT;
     }
@@ -423,6 +432,7 @@ size_t mt_describe_plan(const mt_plan_t *p, char *buf, size_t n) {
             snprintf(grid, sizeof(grid), "%d", p->grid);
         const char *path = p->path == MT_PATH_REGISTERS ? "registers"
                            : p->path == MT_PATH_LOOP    ? "loop"
+                           : p->path == MT_PATH_STAGE   ? "staged"
                                                         : "invalid";
         char cl[32] = "";
         if (p->cluster > 1) snprintf(cl, sizeof(cl), " cluster=%d", p->cluster);

@@ -3,8 +3,9 @@
 For each (operator, storage type, rows, cols) the tuner enumerates the legal
 plans (V in {1, 2, 4} for FP32 and {2, 4, 8} for FP16/BF16; W a power of
 two; the smallest register chunk count that holds the row; rows per CTA B so
-that a CTA has 32..1024 threads; the loop path for wide rows; clusters of
-2, 4, 8 or 16 CTAs per row for few or very wide rows; the launch flags),
+that a CTA has 32..1024 threads; the loop path and the staged path for wide
+rows; clusters of 2, 4, 8 or 16 CTAs per row for few or very wide rows; the
+launch flags),
 then, in a second stage, the four fastest again on persistent grids of one
 to three CTAs per SM.  For each plan it:
 
@@ -41,6 +42,8 @@ from . import inputs
 from .timing import Workload, time_rounds
 
 CHUNKS = (1, 2, 4, 8, 16)
+STAGE_OPS = ("rmsnorm", "layernorm", "softmax", "log_softmax",
+             "cross_entropy", "row_sum")
 VALUES = {"f32": (4, 2, 1), "f16": (8, 4, 2), "bf16": (8, 4, 2)}
 FLAG_SETS = (B.MT_PLAN_PDL, B.MT_PLAN_PDL | B.MT_PLAN_PREFETCH_NEXT, 0)
 
@@ -91,6 +94,17 @@ def candidates(op, rows, cols, dtype="f32"):
                     if cols >= 8192:
                         out.append(B.make_plan(W, vmax, 0, 1, B.MT_PATH_LOOP,
                                                flags=fl, cluster=C))
+    # Staged rows (shared memory filled by bulk copies): wide rows, one row
+    # per CTA or per cluster.
+    if cols >= 8192 and op in STAGE_OPS:
+        for C in ((1, 2, 4, 8, 16) if rows <= 19 else (1, 2, 4, 8)):
+            for W in (256, 512, 1024):
+                for pieces in (2, 4):
+                    for fl in (B.MT_PLAN_PDL,
+                               B.MT_PLAN_PDL | B.MT_PLAN_PREFETCH_NEXT):
+                        out.append(B.make_plan(W, vmax, pieces, 1,
+                                               B.MT_PATH_STAGE, flags=fl,
+                                               cluster=C if C > 1 else 0))
     seen, legal = set(), []
     for p in out:
         key = tuple(p.as_dict().values())

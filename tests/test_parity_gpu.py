@@ -750,6 +750,61 @@ def test_cluster_split_rows(op, shape):
         compare(op, got, ref, f"{op} {shape} persistent clusters")
 
 
+# ------------------------------------------------------ staged rows
+STAGE_OPS = ["rmsnorm", "layernorm", "softmax", "log_softmax",
+             "cross_entropy", "row_sum"]
+
+
+def staged_plans(cols):
+    """Legal staged plans for FP32 rows of `cols`: threads, cluster sizes,
+    bulk-copy pieces and persistent grids."""
+    out = []
+    for W, C, pieces, grid in ((128, 1, 1, 0), (256, 1, 4, 0),
+                               (512, 2, 2, 0), (1024, 4, 8, 0),
+                               (256, 8, 4, 0), (64, 16, 2, 0),
+                               (256, 2, 4, 4), (128, 1, 2, 3)):
+        p = mt.make_plan(W, 4, pieces, 1, mt.MT_PATH_STAGE, grid=grid,
+                         cluster=C if C > 1 else 0, flags=mt.MT_PLAN_PDL)
+        if mt.mt_plan_check(0, cols, p) == mt.MT_OK:
+            out.append(p)
+    return out
+
+
+@pytest.mark.parametrize("op", STAGE_OPS)
+@pytest.mark.parametrize("shape", [(3, 8192), (5, 40004), (2, 131072),
+                                   (4, 1028)])
+def test_staged_rows(op, shape):
+    """Rows staged in shared memory by bulk copies (one CTA or a cluster of
+    CTAs per row, 1-8 copies per run, persistent grids), against the
+    oracle with guard regions; no staged wait gives up."""
+    rows, cols = shape
+    d = inputs.make(op, rows, cols, SEED + cols + 23)
+    ref = oracle.run(op, d)
+    plans = staged_plans(cols)
+    assert plans
+    for p in plans:
+        got = run_guarded(op, d, rows, cols, plan=p)
+        compare(op, got, ref, f"{op} {shape} {mt.mt_describe_plan(p)}")
+    assert mt.mt_stage_wait_timeouts() == 0
+
+
+def test_staged_plan_needs_aligned_rows():
+    """A forced staged plan on rows off the 16-byte grid is refused before
+    any launch."""
+    rows, cols = 3, 8192
+    p = mt.make_plan(256, 4, 2, 1, mt.MT_PATH_STAGE)
+    d = inputs.make("softmax", rows, cols, SEED)
+    bufs = {"x": Guarded(rows * cols, 1, float("nan"), data=d["x"]),
+            "y": Guarded(rows * cols, 0, Guarded.SENTINEL)}
+    with pytest.raises(mt.MTError) as e:
+        call("softmax", {k: b.ptr for k, b in bufs.items()}, rows, cols,
+             plan=p)
+    assert e.value.status == mt.MT_ERR_INVALID_ARGUMENT
+    torch.cuda.synchronize()
+    for b in bufs.values():
+        b.check()
+
+
 # ------------------------------------------------- masked (-inf) runs
 def masked_logits(rows, cols, seed):
     """Softmax inputs N(0, 2^2) with runs of -inf covering whole packs and
@@ -784,6 +839,8 @@ def test_masked_runs_of_minus_infinity(op, cols):
                       if cols <= 4103 or p.path == mt.MT_PATH_LOOP][::3]
     if cols >= 4103:
         plans += cluster_plans(cols)
+    if cols % 4 == 0:
+        plans += staged_plans(cols)
     for p in plans:
         if p is not None and mt.mt_plan_check(mt.OP_IDS[op], cols, p) != 0:
             continue

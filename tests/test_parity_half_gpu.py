@@ -304,6 +304,27 @@ def test_cross_entropy_ignore_index_half(dt):
 
 
 @pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("op", ["rmsnorm", "layernorm", "softmax",
+                                "log_softmax", "cross_entropy", "row_sum"])
+def test_staged_rows_half(dt, op):
+    """16-bit rows staged in shared memory (single CTAs, clusters, several
+    bulk copies per run), against the oracle."""
+    for rows, cols in ((3, 32768), (2, 131072), (5, 40008)):
+        st, wide = case(op, rows, cols, dt, SEED + 41 + cols)
+        for W, C, pieces in ((256, 1, 4), (512, 2, 2), (128, 4, 8),
+                             (1024, 8, 1), (256, 16, 4)):
+            p = mt.make_plan(W, 8, pieces, 1, mt.MT_PATH_STAGE,
+                             cluster=C if C > 1 else 0,
+                             flags=mt.MT_PLAN_PDL)
+            if mt.mt_plan_check_dtype(op, dt, cols, p) != mt.MT_OK:
+                continue
+            outs = run(op, st, dt, rows, cols, plan=p)
+            check(op, dt, outs, st, wide,
+                  f"{op} {dt} {rows}x{cols} {mt.mt_describe_plan(p)}")
+    assert mt.mt_stage_wait_timeouts() == 0
+
+
+@pytest.mark.parametrize("dt", DTYPES)
 @pytest.mark.parametrize("op", OPS)
 def test_cluster_split_rows_half(dt, op):
     rows, cols = 3, 50003
