@@ -85,6 +85,16 @@ int64_t wide_row_cluster(int64_t rows, int64_t cols, int64_t V) {
     return 0;
 }
 
+// Staged rows: the smallest cluster (1..16 CTAs) whose runs take at most
+// 128 KiB of shared memory each, so at least one CTA fits an SM beside
+// another's run (the measured staged winners: 32000 FP32 values on one CTA
+// or two, 131072 BF16 values on two); 0 when even 16 CTAs do not suffice.
+int64_t stage_cluster(int64_t cols, int es) {
+    for (int64_t C = 1; C <= 16; C *= 2)
+        if (stage_run_bytes(cols, es, C) <= 128 * 1024) return C;
+    return 0;
+}
+
 // Heuristic plan for shapes far from every measured one.  It follows what
 // the measured winners have in common:
 //  * 16-byte packs (V = 16 / element size) unless the row is tiny;
@@ -93,9 +103,13 @@ int64_t wide_row_cluster(int64_t rows, int64_t cols, int64_t V) {
 //    of FP32 data): one row per CTA of W = row/16 threads (at most 1024),
 //    two rows per CTA when that leaves fewer than 256 threads;
 //  * wider rows, fewer rows than SMs: a cluster of 8 CTAs per row;
-//  * wider rows, at least 512 of them, that one or two CTAs of 256 threads
-//    x 16 chunks hold: the register path on that cluster -- one read of
-//    the row instead of the loop path's two (wide_row_cluster);
+//  * wider rows of the staged operators (cols a multiple of the 16-byte
+//    unit): the staged path, 512 threads, two bulk copies per run, on the
+//    smallest cluster whose runs take at most 128 KiB (stage_cluster) --
+//    the row read once, as the measured wide-row winners do;
+//  * other wider rows, at least 512 of them, that one or two CTAs of 256
+//    threads x 16 chunks hold: the register path on that cluster -- one
+//    read of the row instead of the loop path's two (wide_row_cluster);
 //  * the other wide rows: the loop path with 256 threads per row and two
 //    rows per CTA, so several rows stream through each SM at once.
 // All launches use the programmatic-dependent prologue.  Register-path CTAs
@@ -103,7 +117,6 @@ int64_t wide_row_cluster(int64_t rows, int64_t cols, int64_t V) {
 // winners mostly do without it: their own second pass re-reads the row from
 // L2, and the prefetch competes with it).
 mt_plan_t heuristic_plan(int op, int dtype, int64_t rows, int64_t cols) {
-    (void)op;
     mt_plan_t p;
     memset(&p, 0, sizeof(p));
     const int es = dtype_size(dtype);
@@ -165,6 +178,17 @@ mt_plan_t heuristic_plan(int op, int dtype, int64_t rows, int64_t cols) {
         p.threads_per_row = 512;
         return p;
     }
+    if (V * es == 16 && stage_op(op) && cols % V == 0) {
+        const int64_t Cs = stage_cluster(cols, es);
+        if (Cs > 0) {
+            p.path = MT_PATH_STAGE;
+            p.cluster = Cs > 1 ? (int)Cs : 0;
+            p.threads_per_row = 512;
+            p.chunks = 2;
+            p.rows_per_block = 1;
+            return p;
+        }
+    }
     if (V * es == 16) {
         const int64_t Cw = wide_row_cluster(rows, cols, V);
         if (Cw > 0) {
@@ -216,6 +240,27 @@ mt_status plan_check_impl(int op, int dtype, int64_t cols, const mt_plan_t &p);
 bool refit(int op, int dtype, int64_t rows_src, int64_t rows, int64_t cols,
            mt_plan_t *p) {
     const int64_t V = p->values_per_thread;
+    if (p->path == MT_PATH_STAGE) {
+        // A staged winner stays staged where the row can be: same threads,
+        // copies and flags, the cluster that keeps runs within 128 KiB (or
+        // spreads few rows as cluster_for does), a resident grid.
+        const int64_t Cs = stage_cluster(cols, dtype_size(dtype));
+        int64_t C = cluster_for(rows);
+        if (Cs > C) C = Cs;
+        if (Cs > 0 && cols % V == 0 && C <= 16) {
+            mt_plan_t q = *p;
+            q.cluster = C > 1 ? (int32_t)C : 0;
+            q.grid = 0;
+            if (plan_check_impl(op, dtype, cols, q) == MT_OK) {
+                *p = q;
+                return true;
+            }
+        }
+        // Otherwise the loop path with the same team.
+        p->path = MT_PATH_LOOP;
+        p->chunks = 0;
+        p->cluster = 0;
+    }
     const int64_t cta = (int64_t)p->threads_per_row * p->rows_per_block;
     const int64_t c_src = p->cluster > 1 ? p->cluster : 1;
     // Split rows when there are few of them and they are wide, and on the
@@ -335,7 +380,8 @@ mt_status plan_check_impl(int op, int dtype, int64_t cols, const mt_plan_t &p) {
         // copies per run, a run that fits the shared-memory budget.
         if (!stage_op(op) || B != 1 || W < 32 ||
             V * dtype_size(dtype) != 16 || p.chunks < 1 ||
-            p.chunks > kStagePiecesMax || !is_pow2(p.chunks))
+            p.chunks > kStagePiecesMax || !is_pow2(p.chunks) ||
+            cols % V != 0)
             return MT_ERR_INVALID_ARGUMENT;
         if (stage_run_bytes(cols, dtype_size(dtype), C) > kStageMaxRunBytes)
             return MT_ERR_OUT_OF_RESOURCES;

@@ -40,16 +40,38 @@ def test_few_wide_rows_split_across_clusters():
         assert p.cluster == C, (rows, p.as_dict())
 
 
-def test_many_wide_rows_stay_in_registers_when_two_ctas_hold_them():
-    # 32000 FP32 values need two CTAs of 256 threads x 16 chunks; 32000
-    # BF16 values fit one
+def test_many_wide_rows_are_staged_or_held_in_registers():
+    # The staged operators read many wide rows once through shared memory,
+    # on the smallest cluster whose runs take at most 128 KiB.
     p = plan("layernorm", "f32", 8192, 32000)
-    assert (p.path, p.cluster) == (mt.MT_PATH_REGISTERS, 2)
+    assert p.path == mt.MT_PATH_STAGE and p.cluster <= 1
     p = plan("layernorm", "bf16", 8192, 32000)
-    assert p.path == mt.MT_PATH_REGISTERS and p.cluster <= 1
-    # wider than two CTAs, or too few rows: the loop path
-    assert plan("layernorm", "f32", 8192, 65536).path == mt.MT_PATH_LOOP
+    assert p.path == mt.MT_PATH_STAGE and p.cluster <= 1
+    p = plan("layernorm", "f32", 8192, 65536)
+    assert (p.path, p.cluster) == (mt.MT_PATH_STAGE, 2)
+    # The residual operators have no staged path: 32000 FP32 values need
+    # two CTAs of 256 threads x 16 chunks, wider rows the loop path.
+    p = plan("residual_layernorm", "f32", 8192, 32000)
+    assert (p.path, p.cluster) == (mt.MT_PATH_REGISTERS, 2)
+    assert plan("residual_layernorm", "f32", 8192,
+                65536).path == mt.MT_PATH_LOOP
+    # Rows that are not a whole number of 16-byte units: the loop path.
     assert plan("softmax", "bf16", 128, 50257).path == mt.MT_PATH_LOOP
+
+
+def test_staged_plans_need_whole_units():
+    p = mt.make_plan(256, 4, 2, 1, mt.MT_PATH_STAGE)
+    assert mt.mt_plan_check(mt.OP_IDS["softmax"], 8192, p) == mt.MT_OK
+    assert mt.mt_plan_check(mt.OP_IDS["softmax"], 8194,
+                            p) == mt.MT_ERR_INVALID_ARGUMENT
+    # no staged path for the residual operators
+    assert mt.mt_plan_check(mt.OP_IDS["residual_layernorm"], 8192,
+                            p) == mt.MT_ERR_INVALID_ARGUMENT
+    # a run beyond the shared-memory budget
+    assert mt.mt_plan_check(mt.OP_IDS["softmax"], 65536,
+                            p) == mt.MT_ERR_OUT_OF_RESOURCES
+    q = mt.make_plan(256, 4, 2, 1, mt.MT_PATH_STAGE, cluster=2, grid=0)
+    assert mt.mt_plan_check(mt.OP_IDS["softmax"], 65536, q) == mt.MT_OK
 
 
 def test_refit_avoids_the_spilling_fp32_instance():
