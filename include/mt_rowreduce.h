@@ -174,6 +174,14 @@ typedef struct mt_plan {
  * loop over row groups), each CTA asks L2 to prefetch its next row group
  * while it processes the current one. */
 #define MT_PLAN_PREFETCH_NEXT 2
+/* Plan flag (register path, no cluster): where the plan tiles every row
+ * exactly (cols = W*V*chunks), rows is a multiple of rows_per_block, the
+ * rows are aligned and every parameter vector the operator reads is
+ * present, run the variant of the kernel without bounds guards.  Elsewhere
+ * the flag has no effect.  The results are the same bits either way; the
+ * two variants differ in instructions and registers, so the tuner measures
+ * both. */
+#define MT_PLAN_WHOLE_TILES 4
 
 /* ---- operators ---------------------------------------------------------
  * Each takes its plan from the built-in, measured plan table

@@ -14,7 +14,8 @@ from ._binding import (  # noqa: F401
     MT_ERR_OUT_OF_RESOURCES, MT_ERR_UNSUPPORTED, MT_OK, MT_OP_CROSS_ENTROPY,
     MT_OP_LAYERNORM, MT_OP_RESIDUAL_LAYERNORM, MT_OP_RMSNORM, MT_OP_ROW_SUM,
     MT_OP_SOFTMAX, MT_PATH_LOOP, MT_PATH_REGISTERS, MT_PATH_STAGE, MT_PLAN_PDL,
-    MT_PLAN_PREFETCH_NEXT, OP_IDS, DTYPE_IDS, MT_DTYPE_F32, MT_DTYPE_F16,
+    MT_PLAN_PREFETCH_NEXT, MT_PLAN_WHOLE_TILES, OP_IDS, DTYPE_IDS,
+    MT_DTYPE_F32, MT_DTYPE_F16,
     MT_DTYPE_BF16, MTError, MtPlan, dtype_of, mt_row_reduce_with_plan,
     mt_plan_query_dtype, mt_plan_check_dtype, mt_rmsnorm_f16,
     mt_rmsnorm_bf16, mt_layernorm_f16, mt_layernorm_bf16,

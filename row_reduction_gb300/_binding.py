@@ -48,6 +48,7 @@ MT_PATH_STAGE = 2
 
 MT_PLAN_PDL = 1
 MT_PLAN_PREFETCH_NEXT = 2
+MT_PLAN_WHOLE_TILES = 4
 
 # Symbols declared in include/mt_rowreduce.h.
 EXPORTS = (

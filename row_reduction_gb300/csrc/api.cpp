@@ -298,8 +298,8 @@ mt_status run(const Call &c, const mt_plan_t *forced, cudaStream_t stream) {
             : (c.op == OP_LAYERNORM || c.op == OP_RESIDUAL_LAYERNORM)
                   ? (c.w != nullptr && c.b != nullptr)
                   : true;
-    const bool full = aligned && params && p.path == MT_PATH_REGISTERS &&
-                      p.cluster <= 1 &&
+    const bool full = (p.flags & MT_PLAN_WHOLE_TILES) && aligned && params &&
+                      p.path == MT_PATH_REGISTERS && p.cluster <= 1 &&
                       (int64_t)p.threads_per_row * V * p.chunks == c.cols &&
                       c.rows % p.rows_per_block == 0;
     const int mode = full ? KM_FULL : (aligned ? KM_ALIGNED : KM_UNALIGNED);

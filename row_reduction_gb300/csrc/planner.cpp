@@ -353,7 +353,7 @@ mt_status plan_check_impl(int op, int dtype, int64_t cols, const mt_plan_t &p) {
     if (V > 1 && W < V) return MT_ERR_INVALID_ARGUMENT;
     if (B < 1 || B > 1024) return MT_ERR_INVALID_ARGUMENT;
     if (p.grid < 0) return MT_ERR_INVALID_ARGUMENT;
-    if (p.flags & ~(MT_PLAN_PDL | MT_PLAN_PREFETCH_NEXT))
+    if (p.flags & ~(MT_PLAN_PDL | MT_PLAN_PREFETCH_NEXT | MT_PLAN_WHOLE_TILES))
         return MT_ERR_INVALID_ARGUMENT;
     const int64_t C = p.cluster <= 1 ? 1 : p.cluster;
     if (p.cluster < 0 || (C != 1 && C != 2 && C != 4 && C != 8 && C != 16))
@@ -484,13 +484,15 @@ size_t mt_describe_plan(const mt_plan_t *p, char *buf, size_t n) {
         if (p->cluster > 1) snprintf(cl, sizeof(cl), " cluster=%d", p->cluster);
         len = snprintf(tmp, sizeof(tmp),
                        "path=%s W=%d V=%d chunks=%d rows_per_block=%d "
-                       "threads=%d grid=%s%s%s%s",
+                       "threads=%d grid=%s%s%s%s%s",
                        path, p->threads_per_row, p->values_per_thread,
                        p->chunks, p->rows_per_block,
                        p->threads_per_row * p->rows_per_block, grid, cl,
                        (p->flags & MT_PLAN_PDL) ? " pdl" : "",
                        (p->flags & MT_PLAN_PREFETCH_NEXT) ? " prefetch_next"
-                                                          : "");
+                                                          : "",
+                       (p->flags & MT_PLAN_WHOLE_TILES) ? " whole_tiles"
+                                                        : "");
     }
     if (len < 0) len = 0;
     if (buf != nullptr && n > 0) {

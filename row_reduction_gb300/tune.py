@@ -73,6 +73,13 @@ def candidates(op, rows, cols, dtype="f32"):
                     for fl in FLAG_SETS:
                         if K is not None:
                             out.append(B.make_plan(W, V, K, Bk, flags=fl))
+                            # Exact tiling: the unguarded whole-tile kernel
+                            # too (with the dependent-launch prologue).
+                            if (fl and W * V * K == cols and rows % Bk == 0
+                                    and (V > 1 or dtype == "f32")):
+                                out.append(B.make_plan(
+                                    W, V, K, Bk,
+                                    flags=fl | B.MT_PLAN_WHOLE_TILES))
                         if cols >= 8192:
                             out.append(B.make_plan(W, V, 0, Bk,
                                                    B.MT_PATH_LOOP, flags=fl))
@@ -130,8 +137,9 @@ def grid_variants(rows, plans, sms):
             G = sms * mult
             if G % C or G // C >= ngroups:
                 continue
+            keep = d.get("flags", 0) & B.MT_PLAN_WHOLE_TILES
             for fl in flag_sets:
-                out.append(B.MtPlan(**dict(d, grid=G, flags=fl)))
+                out.append(B.MtPlan(**dict(d, grid=G, flags=fl | keep)))
     return out
 
 

@@ -174,15 +174,19 @@ def test_plan_query_errors_and_describe():
 
 
 def test_plan_flags():
-    both = mt.MT_PLAN_PDL | mt.MT_PLAN_PREFETCH_NEXT
-    for fl in range(both + 1):
+    every = (mt.MT_PLAN_PDL | mt.MT_PLAN_PREFETCH_NEXT |
+             mt.MT_PLAN_WHOLE_TILES)
+    for fl in range(every + 1):
         p = mt.make_plan(128, 4, 8, 2, grid=152, flags=fl)
         assert mt.mt_plan_check(0, 4096, p) == OK
-    for fl in (4, 8, -1, both | 4):
+    for fl in (8, 16, -1, every | 8):
         p = mt.make_plan(128, 4, 8, 2, flags=fl)
         assert mt.mt_plan_check(0, 4096, p) == INV
+    both = mt.MT_PLAN_PDL | mt.MT_PLAN_PREFETCH_NEXT
     s = mt.mt_describe_plan(mt.make_plan(128, 4, 8, 2, grid=152, flags=both))
     assert s.endswith("grid=152 pdl prefetch_next")
+    s = mt.mt_describe_plan(mt.make_plan(128, 4, 8, 2, flags=every))
+    assert s.endswith("pdl prefetch_next whole_tiles")
 
 
 # ------------------------------------------------------ argument validation

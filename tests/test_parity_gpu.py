@@ -256,10 +256,11 @@ def test_mapping_matrix(op, cols):
 
 
 # ------------------------------------------------ whole-tile kernels
-# Plans whose packs tile every row exactly (cols = W*V*K) run, when rows is
-# a multiple of B and every parameter vector is present, the unguarded
-# whole-tile kernels; one more row (no longer a multiple of B) sends the
-# same plan to the guarded kernel.  (cols, W, V, K, B):
+# Plans with the whole-tile flag whose packs tile every row exactly
+# (cols = W*V*K) run, when rows is a multiple of B and every parameter
+# vector is present, the unguarded whole-tile kernels; one more row (no
+# longer a multiple of B) sends the same plan to the guarded kernel.
+# (cols, W, V, K, B):
 WHOLE_TILES = [(128, 32, 4, 1, 4), (512, 128, 1, 4, 2), (1024, 64, 4, 4, 2),
                (2048, 256, 2, 4, 2), (4096, 128, 4, 8, 2),
                (4096, 256, 4, 4, 2), (4096, 64, 4, 16, 2),
@@ -277,7 +278,8 @@ def test_whole_tile_kernels(op):
     the guarded kernel of the same plan on the same rows."""
     rows = 6
     for cols, W, V, K, B in WHOLE_TILES:
-        p = mt.make_plan(W, V, K, B)
+        p = mt.make_plan(W, V, K, B, flags=mt.MT_PLAN_PDL |
+                         mt.MT_PLAN_WHOLE_TILES)
         assert mt.mt_plan_check(mt.OP_IDS[op], cols, p) == mt.MT_OK
         d = inputs.make(op, rows + 1, cols, SEED + 7 * cols + W)
         d6 = _first_rows(d, rows)
