@@ -120,8 +120,8 @@ def kernel_sources_sha(op="rmsnorm", plan=None, dtype="f32"):
     its plan."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "row_reduction_gb300", "csrc")
-    for name in ("mt_kernels.cuh", "mt_internal.h", "api.cpp",
-                 f"ops_{op}_{dtype}.cu"):
+    for name in ("mt_kernels.cuh", "mt_stage.cuh", "mt_internal.h",
+                 "api.cpp", f"ops_{op}_{dtype}.cu"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + b"\0" + f.read())
     h.update((plan or "").encode())
