@@ -5,10 +5,10 @@
 // grid, launch flags and the cluster size.  The operators take the plan from
 // a table of winners measured on the GPU (plan_table.inc, written by the
 // package's tuner), keyed by operator, storage type and a (cols, rows)
-// range.  A shape outside the table takes the measured winner of the
-// nearest tuned shape -- nearest in log2(cols), then log2(rows) -- with its
-// chunk count (and if need be its width, or its path) re-fitted to the new
-// row length; the heuristic below is the last resort.
+// range.  A shape outside the table takes a plan derived from the shape
+// (shape_plan: values per thread from the work per SM, active groups per
+// SM, live lanes, the staged path for wide rows); the heuristic below is the
+// last resort.
 //
 // The legality rules follow the fail-closed contract of the pages: a plan is
 // checked before dispatch and an illegal one is rejected, never remapped
@@ -93,6 +93,179 @@ int64_t stage_cluster(int64_t cols, int es) {
     for (int64_t C = 1; C <= 16; C *= 2)
         if (stage_run_bytes(cols, es, C) <= 128 * 1024) return C;
     return 0;
+}
+
+// ---- shape-derived plans --------------------------------------------------
+// The fallback for shapes outside the table prices the two features the
+// pages name for this choice ("Consecutive-worker reduction layout
+// checkpoint", §Evidence and what remains: the loss of active groups from
+// short-row packing, live lanes, shape-derived collaborating widths), with
+// constants read off the measured winners (the tuned table and the
+// held-out regret set):
+//  * values per thread vt = R*cols / (SMs * 512) rounded down to a power of
+//    two and clamped to [8, 32] (the residual operators, which hold two
+//    inputs, to 32 bytes of row per thread for LayerNorm and 64 for
+//    RMSNorm): the device's share of the work sets how long each thread
+//    stays busy, so that about a quarter of the SM's thread slots carry it;
+//  * the one-pass operators (row sum, cross-entropy) on rows of up to 16
+//    packs per lane: one warp per row, so no shared-memory combine;
+//  * the collaborating width W = the row's packs / (vt / V), a power of two,
+//    and the chunk count K the smallest that covers the row (the live lanes
+//    W*V*K >= cols); FP32 rows at 8 values per thread take 2-value packs
+//    (the 4-value, 2-chunk instance spills);
+//  * rows per CTA B: CTAs of about 128 threads, halved while that leaves
+//    fewer than four active groups per SM (ceil(R / B) < 4 * SMs);
+//  * rows of more than 16384 values (more than 32 register values per
+//    thread at 512 threads): the staged path for its operators (the
+//    one-pass ones from ten rows, the others from 39), on the smallest
+//    cluster whose runs take at most 160 KiB and that gives the rows 1.5
+//    CTAs per SM, 512 threads for runs of 96 KiB and more, else 256;
+//  * other few wide rows (at most 38, at least 8192 values): the register
+//    path on a cluster of 4, 8 or 16 CTAs per row (cluster_for);
+//  * one-pass rows on the loop path: 64-thread teams on many rows, a
+//    cluster of 512-thread CTAs for fewer rows than 1.5 per SM.
+// Plans that tile the rows exactly also take the whole-tile variant.
+constexpr int64_t kPlanSMs = 152;  // GB300
+
+mt_status plan_check_impl(int op, int dtype, int64_t cols, const mt_plan_t &p);
+
+bool has_residual_op(int op) {
+    return op == OP_RESIDUAL_LAYERNORM || op == OP_RESIDUAL_RMSNORM;
+}
+
+int64_t pow2_floor(int64_t v) {
+    int64_t p = 1;
+    while (p * 2 <= v) p <<= 1;
+    return p;
+}
+
+// Staged rows: the smallest cluster whose runs take at most `cap` bytes.
+int64_t stage_cluster_cap(int64_t cols, int es, int64_t cap) {
+    for (int64_t C = 1; C <= 16; C *= 2)
+        if (stage_run_bytes(cols, es, C) <= cap) return C;
+    return 0;
+}
+
+// One pass, one value out per row: row sum and cross-entropy.
+bool one_pass_op(int op) { return op == OP_ROW_SUM || op == OP_CROSS_ENTROPY; }
+
+// Smallest cluster (a power of two, at most 16) that gives `rows` rows at
+// least 1.5 CTAs per SM.
+int64_t cluster_for_rows(int64_t rows) {
+    int64_t C = 1;
+    while (C < 16 && rows * C * 2 < 3 * kPlanSMs) C *= 2;
+    return C;
+}
+
+bool shape_plan(int op, int dtype, int64_t rows, int64_t cols,
+                mt_plan_t *out) {
+    mt_plan_t p;
+    memset(&p, 0, sizeof(p));
+    const int es = dtype_size(dtype);
+    const int64_t vmax = 16 / es;
+    const int64_t R = rows < 1 ? 1 : rows;
+    p.flags = MT_PLAN_PDL | MT_PLAN_PREFETCH_NEXT;
+    // Wide rows of the staged operators: read once through shared memory.
+    // Rows that need more than 32 register values per thread at 512
+    // threads (16384 values) count as wide; the cluster is the smallest
+    // whose runs take at most 160 KiB and that gives the rows 1.5 CTAs per
+    // SM.  The one-pass operators stage from ten rows on, the others from
+    // 39 (fewer rows keep the register path on a cluster).
+    if (cols > 16384 && (one_pass_op(op) ? R > 9 : cluster_for(R) <= 2) &&
+        stage_op(op) && cols % vmax == 0) {
+        int64_t C = stage_cluster_cap(cols, es, 160 * 1024);
+        const int64_t Cr = cluster_for_rows(R);
+        if (C > 0 && Cr > C) C = Cr;
+        if (C > 0) {
+            p.path = MT_PATH_STAGE;
+            p.values_per_thread = (int32_t)vmax;
+            p.cluster = C > 1 ? (int32_t)C : 0;
+            p.threads_per_row =
+                stage_run_bytes(cols, es, C) >= 96 * 1024 ? 512 : 256;
+            p.chunks = 2;
+            p.rows_per_block = 1;
+            if (plan_check_impl(op, dtype, cols, p) == MT_OK) {
+                *out = p;
+                return true;
+            }
+        }
+    }
+    // Few wide rows (at most 38) split across a cluster; wider rows than a
+    // cluster's registers hold go to the caller's other rules.
+    const int64_t C = (cols >= 8192 && cluster_for(R) > 2) ? cluster_for(R) : 1;
+    if (cols > C * cta_register_values(vmax)) return false;
+    int64_t V, W;
+    if (one_pass_op(op) && C == 1 && cols <= 32 * vmax * 16) {
+        // One warp per row: no shared-memory combine at all (the measured
+        // one-pass winners on 300..4000 values); 16-bit rows in 16-byte
+        // packs, FP32 rows in 8-byte packs.
+        V = dtype == DT_F32 ? 2 : vmax;
+        // Short 16-bit rows (two 16-byte packs per thread or fewer): 8-byte
+        // packs, twice as many.
+        if (dtype != DT_F32 && cols <= 32 * vmax * 2) V = vmax / 2;
+        if (cols < 4 * V) V = dtype == DT_F32 ? 1 : 2;
+        W = 32;
+    } else {
+        // Values per thread from the work per SM.
+        // The residual operators hold two inputs: at most 32 bytes of row
+        // per thread for residual LayerNorm, 64 for residual RMSNorm.
+        int64_t vt = pow2_floor(R * cols / (kPlanSMs * 512));
+        const int64_t vt_max = op == OP_RESIDUAL_LAYERNORM ? 32 / es
+                               : op == OP_RESIDUAL_RMSNORM ? 64 / es
+                                                           : 32;
+        if (vt < 8) vt = 8;
+        if (vt > vt_max) vt = vt_max;
+        V = cols >= 4 * vmax ? vmax : (dtype == DT_F32 ? 1 : 2);
+        if (V > vt) V = vt;
+        if (dtype == DT_F32 && vt == 8 && V == 4 && !has_residual_op(op))
+            V = 2;
+        if (C > 1) V = vmax;  // clusters take 16-byte packs
+        const int64_t kt = vt / V < 1 ? 1 : vt / V;
+        const int64_t packs = (cols + V - 1) / V;
+        W = pow2_ceil((packs + C * kt - 1) / (C * kt));
+    }
+    const int64_t wmin = C > 1 ? 32 : (V > 1 ? V : 1);
+    if (W < wmin) W = wmin;
+    if (W > 1024) W = 1024;
+    // The chunk count that covers the row (the live lanes W*V*K >= cols); a
+    // wider team while the kernel's thread limit allows, if the row needs
+    // more than 16 chunks.
+    for (;; W *= 2) {
+        int64_t K = 0;
+        for (int i = 0; i < kNumChunkSet; ++i)
+            if (C * W * V * kChunkSet[i] >= cols) {
+                K = kChunkSet[i];
+                break;
+            }
+        if (K != 0 && W <= reg_max_threads((int)(V * K))) {
+            p.chunks = (int32_t)K;
+            break;
+        }
+        if (W >= 1024) return false;
+    }
+    // Rows per CTA: about 128 threads, but at least four active groups per
+    // SM while packing allows fewer rows per CTA.
+    int64_t B = 1;
+    if (C == 1) {
+        const int64_t bmin = W >= 32 ? 1 : 32 / W;
+        B = W >= 128 ? 1 : 128 / W;
+        while (B > bmin && (R + B - 1) / B < 4 * kPlanSMs) B /= 2;
+        while (B > bmin && W * B > reg_max_threads((int)(V * p.chunks)))
+            B /= 2;
+    }
+    p.path = MT_PATH_REGISTERS;
+    p.values_per_thread = (int32_t)V;
+    p.threads_per_row = (int32_t)W;
+    p.rows_per_block = (int32_t)B;
+    p.cluster = C > 1 ? (int32_t)C : 0;
+    // Exact tilings take the whole-tile variant, except for the residual
+    // operators, whose guarded kernels hold fewer registers.
+    if (C == 1 && W * V * p.chunks == cols && R % B == 0 &&
+        !has_residual_op(op))
+        p.flags |= MT_PLAN_WHOLE_TILES;
+    if (plan_check_impl(op, dtype, cols, p) != MT_OK) return false;
+    *out = p;
+    return true;
 }
 
 // Heuristic plan for shapes far from every measured one.  It follows what
@@ -209,130 +382,27 @@ mt_plan_t heuristic_plan(int op, int dtype, int64_t rows, int64_t cols) {
     p.path = MT_PATH_LOOP;
     p.chunks = 0;
     p.flags = MT_PLAN_PDL;
+    if (one_pass_op(op)) {
+        // One-pass loops: narrow teams on many rows (64 threads, no
+        // dependent-launch prologue, as measured on 2048 and 4096 rows of
+        // 32000-50257 values); fewer rows than 1.5 per SM split across a
+        // cluster of 512-thread CTAs.
+        const int64_t Cr = V * es == 16 ? cluster_for_rows(rows) : 1;
+        if (Cr > 1) {
+            p.cluster = (int32_t)Cr;
+            p.threads_per_row = 512;
+            p.rows_per_block = 1;
+            return p;
+        }
+        p.flags = 0;
+        p.threads_per_row = 64;
+        p.rows_per_block = 1;
+        return p;
+    }
     // Two rows per CTA once there are enough rows for two CTAs per SM.
     p.threads_per_row = rows >= 304 ? 256 : 512;
     p.rows_per_block = rows >= 304 ? 2 : 1;
     return p;
-}
-
-}  // namespace
-
-namespace {
-double log2d(double v) { return log2(v < 1.0 ? 1.0 : v); }
-
-mt_status plan_check_impl(int op, int dtype, int64_t cols, const mt_plan_t &p);
-
-// Re-fits the measured plan of shape (rows_src, cols_src) to (rows, cols).
-// The source plan says how many threads the device wanted in flight
-// (rows_src * W * cluster) and how they were grouped (threads per CTA,
-// flags, V); the re-fit keeps those and recomputes the rest:
-//  * cluster: cluster_for(rows) for wide rows (>= 8192) of 16-byte packs;
-//    on the register path, rows wider than those CTAs' registers take
-//    wide_row_cluster's cluster, or the loop path when it has none;
-//  * W = the source's threads in flight / rows / cluster (a power of two),
-//    raised until the row fits in at most 8 chunks, capped at 1024, then
-//    lowered while that breaks the kernel's thread limit for the chunk
-//    count the row needs;
-//  * chunks: the smallest instantiated count that holds the row, the loop
-//    path when none does;
-//  * rows per CTA: what keeps the source's CTA size.
-// Returns false when nothing legal is left.
-bool refit(int op, int dtype, int64_t rows_src, int64_t rows, int64_t cols,
-           mt_plan_t *p) {
-    const int64_t V = p->values_per_thread;
-    if (p->path == MT_PATH_STAGE) {
-        // A staged winner stays staged where the row can be: same threads,
-        // copies and flags, the cluster that keeps runs within 128 KiB (or
-        // spreads few rows as cluster_for does), a resident grid.
-        const int64_t Cs = stage_cluster(cols, dtype_size(dtype));
-        int64_t C = cluster_for(rows);
-        if (Cs > C) C = Cs;
-        if (Cs > 0 && cols % V == 0 && C <= 16) {
-            mt_plan_t q = *p;
-            q.cluster = C > 1 ? (int32_t)C : 0;
-            q.grid = 0;
-            if (plan_check_impl(op, dtype, cols, q) == MT_OK) {
-                *p = q;
-                return true;
-            }
-        }
-        // Otherwise the loop path with the same team.
-        p->path = MT_PATH_LOOP;
-        p->chunks = 0;
-        p->cluster = 0;
-    }
-    const int64_t cta = (int64_t)p->threads_per_row * p->rows_per_block;
-    const int64_t c_src = p->cluster > 1 ? p->cluster : 1;
-    // Split rows when there are few of them and they are wide, and on the
-    // register path whenever one CTA's registers cannot hold the row.
-    const bool packs16 = V * dtype_size(dtype) == 16;
-    const int64_t c_loop = (packs16 && cols >= 8192) ? cluster_for(rows) : 1;
-    int64_t C = c_loop;
-    if (packs16 && p->path == MT_PATH_REGISTERS &&
-        C * cta_register_values(V) < cols) {
-        const int64_t cw = wide_row_cluster(rows, cols, V);
-        if (cw == 0)
-            p->path = MT_PATH_LOOP;
-        else if (cw > C)
-            C = cw;
-    }
-    p->cluster = C > 1 ? (int32_t)C : 0;
-    p->grid = 0;
-    const double inflight = (double)(rows_src < 1 ? 1 : rows_src) *
-                            p->threads_per_row * c_src;
-    int64_t W = pow2_ceil((int64_t)(inflight / (double)(rows < 1 ? 1 : rows) /
-                                    (double)C / 1.414));
-    const int64_t wmin = C > 1 ? 32 : (V > 1 ? V : 1);
-    if (W < wmin) W = wmin;
-    while (W < 1024 && C * W * V * 8 < cols) W *= 2;
-    if (W > 1024) W = 1024;
-    if (p->path == MT_PATH_REGISTERS) {
-        // From W down: narrower teams hold more chunks each, and the
-        // kernel's thread limit falls as the chunks per thread rise.
-        for (int64_t w = W; w >= wmin; w /= 2) {
-            int64_t K = 0;
-            for (int i = 0; i < kNumChunkSet; ++i)
-                if (C * w * V * kChunkSet[i] >= cols) {
-                    K = kChunkSet[i];
-                    break;
-                }
-            if (K == 0) break;
-            int64_t B = C > 1 ? 1 : (cta / w < 1 ? 1 : cta / w);
-            while (B > 1 && w * B > reg_max_threads((int)(V * K))) B /= 2;
-            if ((w * B) % 32 == 0 && w * B <= reg_max_threads((int)(V * K))) {
-                p->threads_per_row = (int32_t)w;
-                p->chunks = (int32_t)K;
-                p->rows_per_block = (int32_t)B;
-                // ptxas holds the FP32 4-value, 2-chunk instance to 32
-                // registers (it spills); the same row in 2-value packs and
-                // 4 chunks does not.
-                if (dtype == DT_F32 && V == 4 && K == 2 && C == 1 &&
-                    w >= 2) {
-                    p->values_per_thread = 2;
-                    p->chunks = 4;
-                    if (plan_check_impl(op, dtype, cols, *p) == MT_OK)
-                        return true;
-                    p->values_per_thread = 4;
-                    p->chunks = 2;
-                }
-                if (plan_check_impl(op, dtype, cols, *p) == MT_OK)
-                    return true;
-            }
-        }
-        p->path = MT_PATH_LOOP;
-        // The loop path splits rows only when they are few.
-        C = c_loop;
-        p->cluster = C > 1 ? (int32_t)C : 0;
-        if (W < 32 && C > 1) W = 32;
-    }
-    p->chunks = 0;
-    if (W > kLoopMaxThreads) W = kLoopMaxThreads;
-    int64_t B = C > 1 ? 1 : (cta / W < 1 ? 1 : cta / W);
-    while (W * B > kLoopMaxThreads) B /= 2;
-    while ((W * B) % 32 != 0) B *= 2;
-    p->threads_per_row = (int32_t)W;
-    p->rows_per_block = (int32_t)(B < 1 ? 1 : B);
-    return plan_check_impl(op, dtype, cols, *p) == MT_OK;
 }
 
 }  // namespace
@@ -406,29 +476,11 @@ mt_status plan_lookup(int op, int dtype, int64_t rows, int64_t cols,
             return MT_OK;
         }
     }
-    // Nearest measured shape of the same operator and storage type.
-    const PlanEntry *best = nullptr;
-    double best_d = 0.0;
-    for (const PlanEntry &e : kPlanTable) {
-        if (e.op != op || e.dtype != dtype) continue;
-        const double d =
-            fabs(log2d((double)cols) - log2d((double)e.cols_min)) +
-            0.5 * fabs(log2d((double)rows) - log2d((double)e.rows_tuned));
-        if (best == nullptr || d < best_d) {
-            best = &e;
-            best_d = d;
-        }
-    }
-    // A measured plan transfers to rows within a factor 4 in length and 16
-    // in count; farther shapes take the heuristic.
-    if (best != nullptr &&
-        fabs(log2d((double)cols) - log2d((double)best->cols_min)) <= 2.0 &&
-        fabs(log2d((double)rows) - log2d((double)best->rows_tuned)) <= 4.0) {
-        mt_plan_t p = best->plan;
-        if (refit(op, dtype, best->rows_tuned, rows, cols, &p)) {
-            *out = p;
-            return MT_OK;
-        }
+    // Shapes outside the table: the shape-derived plan, else the heuristic.
+    mt_plan_t p;
+    if (shape_plan(op, dtype, rows, cols, &p)) {
+        *out = p;
+        return MT_OK;
     }
     *out = heuristic_plan(op, dtype, rows, cols);
     return MT_OK;

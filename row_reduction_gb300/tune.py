@@ -372,6 +372,19 @@ HELDOUT_CASES = (
 )
 
 
+# A second held-out set, for the shape-derived plans' out-of-sample check:
+# shapes that neither the table nor the constants of those rules saw.
+VALIDATION_CASES = (
+    "rmsnorm:f32:1536x2304", "rmsnorm:bf16:6000x1536",
+    "layernorm:f32:768x3072", "layernorm:bf16:12000x512",
+    "layernorm:f16:48x40000", "residual_layernorm:bf16:2500x4096",
+    "residual_rmsnorm:f32:5000x768", "softmax:f32:256x20000",
+    "softmax:bf16:9000x1000", "log_softmax:f16:3000x2500",
+    "row_sum:bf16:200x60000", "row_sum:f32:10000x640",
+    "cross_entropy:f32:512x32768", "cross_entropy:bf16:60x128000",
+)
+
+
 def parse_case(text):
     """'op:dtype:RxC' -> (dtype, op, rows, cols)."""
     op, dt, shape = text.split(":")
@@ -398,7 +411,8 @@ def main(argv=None):
                     help="explicit (operator, storage type, shape) cases "
                          "instead of --ops/--dtypes/--shapes, e.g. "
                          "rmsnorm:f32:512x2048,softmax:bf16:128x50257, "
-                         "or 'heldout' for HELDOUT_CASES")
+                         "or 'heldout' / 'validation' for HELDOUT_CASES / "
+                         "VALIDATION_CASES")
     args = ap.parse_args(argv)
     import torch
     from . import build
@@ -422,6 +436,7 @@ def main(argv=None):
             for op, r, c in shapes]
     if args.cases:
         cases = (HELDOUT_CASES if args.cases == "heldout"
+                 else VALIDATION_CASES if args.cases == "validation"
                  else args.cases.split(","))
         work = [parse_case(c) for c in cases if c]
     props = torch.cuda.get_device_properties(0)

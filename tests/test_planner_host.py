@@ -33,11 +33,21 @@ def test_every_table_winner_is_legal_and_served():
 
 
 def test_few_wide_rows_split_across_clusters():
-    # up to 9 rows: 16 CTAs per row; up to 19: 8; up to 38: 4; up to 76: 2
-    for rows, C in ((1, 16), (9, 16), (10, 8), (19, 8), (20, 4), (38, 4),
-                    (39, 2), (76, 2)):
+    # up to 9 rows: 16 CTAs per row; up to 19: 8; up to 38: 4; more rows
+    # of a staged operator: the staged path on the smallest cluster whose
+    # runs take at most 160 KiB (300000 FP32 values: 8 CTAs)
+    for rows, C in ((1, 16), (9, 16), (10, 8), (19, 8), (20, 4), (38, 4)):
         p = plan("layernorm", "f32", rows, 300000)
-        assert p.cluster == C, (rows, p.as_dict())
+        assert p.cluster == C and p.path != mt.MT_PATH_STAGE, (rows,
+                                                               p.as_dict())
+    for rows in (39, 76, 5000):
+        p = plan("layernorm", "f32", rows, 300000)
+        assert (p.path, p.cluster) == (mt.MT_PATH_STAGE, 8), (rows,
+                                                              p.as_dict())
+    # 20 rows of a one-pass operator are staged too: 8 CTAs per run fit
+    # 160 KiB, 16 give the rows 1.5 CTAs per SM
+    p = plan("row_sum", "f32", 20, 300000)
+    assert (p.path, p.cluster) == (mt.MT_PATH_STAGE, 16), p.as_dict()
 
 
 def test_many_wide_rows_are_staged_or_held_in_registers():
@@ -74,18 +84,40 @@ def test_staged_plans_need_whole_units():
     assert mt.mt_plan_check(mt.OP_IDS["softmax"], 65536, q) == mt.MT_OK
 
 
-def test_refit_avoids_the_spilling_fp32_instance():
-    for op in ("rmsnorm", "residual_layernorm"):
-        for rows, cols in ((512, 2048), (300, 3000)):
-            p = plan(op, "f32", rows, cols)
-            assert not (p.values_per_thread == 4 and p.chunks == 2 and
-                        p.path == mt.MT_PATH_REGISTERS), (op, rows, cols)
+def test_shape_plans_avoid_the_spilling_fp32_instance():
+    # ptxas holds RMSNorm's FP32 4-value, 2-chunk instance to 32 registers
+    # (it spills): rows that would take it use 2-value packs instead
+    for rows, cols in ((512, 2048), (300, 3000)):
+        p = plan("rmsnorm", "f32", rows, cols)
+        assert not (p.values_per_thread == 4 and p.chunks == 2 and
+                    p.path == mt.MT_PATH_REGISTERS), (rows, cols)
 
 
 def test_loop_heuristic_leaves_the_next_group_prefetch_off():
-    p = plan("row_sum", "f32", 2048, 131072)
+    # wide rows of an operator without a staged path
+    p = plan("residual_layernorm", "f32", 2048, 131072)
     assert p.path == mt.MT_PATH_LOOP
     assert not p.flags & mt.MT_PLAN_PREFETCH_NEXT
+
+
+def test_shape_derived_plans_price_active_groups_and_work_per_sm():
+    # Values per thread follow the work per SM (R*cols / (152*512), 8..32)
+    # and CTAs keep at least two active groups per SM.
+    p = plan("layernorm", "f16", 512, 768)         # little work: 8 values
+    assert p.values_per_thread * p.chunks == 8
+    assert -(-512 // p.rows_per_block) >= 2 * 152
+    p = plan("rmsnorm", "f16", 777, 5000)           # more work: 32 values
+    assert (p.threads_per_row, p.values_per_thread, p.chunks) == (256, 8, 4)
+    p = plan("rmsnorm", "f32", 300, 3000)           # FP32 at 8: 2-value packs
+    assert (p.threads_per_row, p.values_per_thread, p.chunks) == (512, 2, 4)
+    p = plan("residual_rmsnorm", "f32", 2048, 3072)  # residual: at most 16
+    assert p.values_per_thread * p.chunks <= 16
+    p = plan("row_sum", "f16", 700, 300)            # short rows packed, but
+    assert -(-700 // p.rows_per_block) >= 2 * 152   # >= 2 groups per SM
+    # an exact tiling takes the whole-tile variant
+    p = plan("layernorm", "f32", 2048, 1024)
+    assert p.threads_per_row * p.values_per_thread * p.chunks == 1024
+    assert p.flags & mt.MT_PLAN_WHOLE_TILES
 
 
 @pytest.mark.parametrize("seed", [1, 2, 3])
