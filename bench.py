@@ -45,8 +45,9 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 
 from row_reduction_gb300.timing import (  # noqa: E402
-    CopyProbe, EmptyProbe, ReadProbe, Workload, algorithmic_bytes, time_e2e,
-    time_graph_steps, time_link, time_plain_steps, time_rounds)
+    MAX_ONE_GRAPH_STEPS, CopyProbe, EmptyProbe, ReadProbe, Workload,
+    algorithmic_bytes, time_e2e, time_graph_steps, time_link,
+    time_plain_steps, time_rounds)
 
 METRIC = ("RMSNorm FP32 µs/op and HBM GB/s (% of GB300 peak), "
           "1×127 … 1024×4096")
@@ -400,11 +401,20 @@ def quick_us(work, rounds=3, min_round_s=0.01):
                                          min_round_s=min_round_s))
 
 
-def best_probe(cls, work):
+def steps_us(work, steps, reps=5):
+    """Median µs per step over `reps` windows of exactly `steps` steps timed
+    as the headline is (time_graph_steps: one graph, events on its side
+    branch)."""
+    return statistics.median(time_graph_steps(work, steps, 5) / steps * 1e6
+                             for _ in range(reps))
+
+
+def best_probe(cls, work, steps):
     """The fastest launch shape of a probe kernel on the workload's pool:
     one wave of resident CTAs or one CTA per row (as the operators'
-    one-row-per-CTA plans), with and without the L2 prefetch; then that
-    shape re-timed with longer rounds.  Returns (µs, shape text)."""
+    one-row-per-CTA plans), with and without the L2 prefetch, found with
+    short graph-replay rounds; then that shape timed like the headline
+    (windows of `steps` steps).  Returns (µs, shape text)."""
     best = None
     for grid in (0, work.rows):
         for threads in (128, 256, 512, 1024):
@@ -414,25 +424,27 @@ def best_probe(cls, work):
                     if best is None or us < best[0]:
                         best = (us, threads, unroll, grid, flags)
     us, threads, unroll, grid, flags = best
-    us = quick_us(cls(work, threads, unroll, grid, flags), rounds=5,
-                  min_round_s=0.03)
+    us = steps_us(cls(work, threads, unroll, grid, flags), steps)
     return us, (f"{threads} threads, {unroll} in flight, "
                 f"grid {grid or 'one wave'}, "
                 f"{'L2 prefetch' if flags else 'no prefetch'}")
 
 
-def measure_floor(work):
-    """The floor of one step, timed like the steps themselves (graph
-    replays of dependent launches over the same rotating pool): the
-    library's plain copy kernel moving the step's matrix bytes in and out,
-    or its read kernel reading them (best of a few launch shapes each), and
-    its empty kernel, alone and on a full wave."""
+def measure_floor(work, steps=20):
+    """The floor of one step, timed like the steps themselves (dependent
+    launches over the same rotating pool, windows of `steps` steps inside
+    one graph): the library's plain copy kernel moving the step's matrix
+    bytes in and out, or its read kernel reading them (best of a few launch
+    shapes each), and its empty kernel, alone and on a full wave."""
     out = {}
+    steps = max(1, min(steps, MAX_ONE_GRAPH_STEPS))
     if work.op in COPY_FLOOR_OPS:
-        out["copy_us"], out["copy_shape"] = best_probe(CopyProbe, work)
+        out["copy_us"], out["copy_shape"] = best_probe(CopyProbe, work,
+                                                       steps)
         out["copy_bytes"] = CopyProbe(work).bytes
     if work.op in READ_FLOOR_OPS:
-        out["read_us"], out["read_shape"] = best_probe(ReadProbe, work)
+        out["read_us"], out["read_shape"] = best_probe(ReadProbe, work,
+                                                       steps)
         out["read_bytes"] = ReadProbe(work).bytes
     out["empty_us"] = quick_us(EmptyProbe(32, 1), rounds=5, min_round_s=0.03)
     out["empty_wave_us"] = quick_us(EmptyProbe(512, 0), rounds=5,
@@ -551,7 +563,7 @@ def run_ours(args, rank, world, local_rank):
     key = f"{args.op}_{args.dtype}_{args.rows}x{args.cols}"
     plan = plan_text(args.op, args.rows, args.cols, args.dtype)
     rounds = time_rounds(work, rounds=5, min_round_s=0.03)
-    floor = measure_floor(work)
+    floor = measure_floor(work, args.steps)
     e2e_steps = max(3, min(args.steps, 200))
     e2e_el, bi, bo = time_e2e(work, e2e_steps, 3, depth=3)
     link_el = time_link(bi, bo, e2e_steps, 3, depth=3)

@@ -113,13 +113,15 @@ int64_t stage_cluster(int64_t cols, int es) {
 //    and the chunk count K the smallest that covers the row (the live lanes
 //    W*V*K >= cols); FP32 rows at 8 values per thread take 2-value packs
 //    (the 4-value, 2-chunk instance spills);
-//  * rows per CTA B: CTAs of about 128 threads, halved while that leaves
-//    fewer than four active groups per SM (ceil(R / B) < 4 * SMs);
+//  * rows per CTA B: CTAs of about 256 threads (128 for the residual
+//    operators), halved while that leaves fewer than three active groups
+//    per SM (ceil(R / B) < 3 * SMs);
 //  * rows of more than 16384 values (more than 32 register values per
 //    thread at 512 threads): the staged path for its operators (the
-//    one-pass ones from ten rows, the others from 39), on the smallest
-//    cluster whose runs take at most 160 KiB and that gives the rows 1.5
-//    CTAs per SM, 512 threads for runs of 96 KiB and more, else 256;
+//    one-pass ones from ten rows, the others from 39; FP32 one-pass rows
+//    on 304 rows or more keep the loop path), on the smallest cluster whose
+//    runs take at most 160 KiB (doubled once when there are fewer runs
+//    than 1.5 per SM), 512 threads for runs of 96 KiB and more, else 256;
 //  * other few wide rows (at most 38, at least 8192 values): the register
 //    path on a cluster of 4, 8 or 16 CTAs per row (cluster_for);
 //  * one-pass rows on the loop path: 64-thread teams on many rows, a
@@ -168,14 +170,21 @@ bool shape_plan(int op, int dtype, int64_t rows, int64_t cols,
     // Wide rows of the staged operators: read once through shared memory.
     // Rows that need more than 32 register values per thread at 512
     // threads (16384 values) count as wide; the cluster is the smallest
-    // whose runs take at most 160 KiB and that gives the rows 1.5 CTAs per
-    // SM.  The one-pass operators stage from ten rows on, the others from
-    // 39 (fewer rows keep the register path on a cluster).
+    // whose runs take at most 160 KiB, doubled once when that leaves fewer
+    // runs than 1.5 per SM.  The one-pass operators stage from ten rows on,
+    // the others from 39 (fewer rows keep the register path on a
+    // cluster).
+    // FP32 one-pass rows on many rows stay on the loop path, which reads
+    // them once too (measured: cross-entropy FP32 512x32768 and
+    // 4096x32000); their 16-bit rows, with twice the arithmetic per byte,
+    // are staged.
+    const bool fp32_one_pass_loop =
+        one_pass_op(op) && dtype == DT_F32 && R >= 2 * kPlanSMs;
     if (cols > 16384 && (one_pass_op(op) ? R > 9 : cluster_for(R) <= 2) &&
-        stage_op(op) && cols % vmax == 0) {
+        !fp32_one_pass_loop && stage_op(op) && cols % vmax == 0) {
         int64_t C = stage_cluster_cap(cols, es, 160 * 1024);
-        const int64_t Cr = cluster_for_rows(R);
-        if (C > 0 && Cr > C) C = Cr;
+        // Fewer runs than 1.5 per SM: split each row once more.
+        if (C > 0 && C < 16 && R * C * 2 < 3 * kPlanSMs) C *= 2;
         if (C > 0) {
             p.path = MT_PATH_STAGE;
             p.values_per_thread = (int32_t)vmax;
@@ -243,13 +252,16 @@ bool shape_plan(int op, int dtype, int64_t rows, int64_t cols,
         }
         if (W >= 1024) return false;
     }
-    // Rows per CTA: about 128 threads, but at least four active groups per
-    // SM while packing allows fewer rows per CTA.
+    // Rows per CTA: about 256 threads, halved while that leaves fewer than
+    // three active groups per SM (short rows: many rows per CTA when there
+    // are rows to spare, one row per CTA when there are not)
     int64_t B = 1;
     if (C == 1) {
         const int64_t bmin = W >= 32 ? 1 : 32 / W;
-        B = W >= 128 ? 1 : 128 / W;
-        while (B > bmin && (R + B - 1) / B < 4 * kPlanSMs) B /= 2;
+        // (the residual operators, heavier in registers: 128 threads)
+        const int64_t T = has_residual_op(op) ? 128 : 256;
+        B = W >= T ? 1 : T / W;
+        while (B > bmin && (R + B - 1) / B < 3 * kPlanSMs) B /= 2;
         while (B > bmin && W * B > reg_max_threads((int)(V * p.chunks)))
             B /= 2;
     }
@@ -351,7 +363,8 @@ mt_plan_t heuristic_plan(int op, int dtype, int64_t rows, int64_t cols) {
         p.threads_per_row = 512;
         return p;
     }
-    if (V * es == 16 && stage_op(op) && cols % V == 0) {
+    if (V * es == 16 && stage_op(op) && cols % V == 0 &&
+        !(one_pass_op(op) && dtype == DT_F32 && rows >= 2 * kPlanSMs)) {
         const int64_t Cs = stage_cluster(cols, es);
         if (Cs > 0) {
             p.path = MT_PATH_STAGE;
@@ -362,7 +375,9 @@ mt_plan_t heuristic_plan(int op, int dtype, int64_t rows, int64_t cols) {
             return p;
         }
     }
-    if (V * es == 16) {
+    if (one_pass_op(op) && dtype == DT_F32 && rows >= 2 * kPlanSMs) {
+        // FP32 one-pass rows on many rows: the loop path (below).
+    } else if (V * es == 16) {
         const int64_t Cw = wide_row_cluster(rows, cols, V);
         if (Cw > 0) {
             int64_t K = 16;
@@ -383,10 +398,10 @@ mt_plan_t heuristic_plan(int op, int dtype, int64_t rows, int64_t cols) {
     p.chunks = 0;
     p.flags = MT_PLAN_PDL;
     if (one_pass_op(op)) {
-        // One-pass loops: narrow teams on many rows (64 threads, no
-        // dependent-launch prologue, as measured on 2048 and 4096 rows of
-        // 32000-50257 values); fewer rows than 1.5 per SM split across a
-        // cluster of 512-thread CTAs.
+        // One-pass loops: no dependent-launch prologue, 64-thread teams on
+        // unaligned rows (2048x50257), 256 threads on aligned ones
+        // (512x32768); fewer rows than 1.5 per SM split across a cluster
+        // of 512-thread CTAs.
         const int64_t Cr = V * es == 16 ? cluster_for_rows(rows) : 1;
         if (Cr > 1) {
             p.cluster = (int32_t)Cr;
@@ -395,7 +410,7 @@ mt_plan_t heuristic_plan(int op, int dtype, int64_t rows, int64_t cols) {
             return p;
         }
         p.flags = 0;
-        p.threads_per_row = 64;
+        p.threads_per_row = cols % V == 0 ? 256 : 64;
         p.rows_per_block = 1;
         return p;
     }
