@@ -422,6 +422,49 @@ def test_in_place(op):
         assert torch.equal(x, ref)
 
 
+@pytest.mark.parametrize("op", ["layernorm", "residual_layernorm"])
+def test_layernorm_ill_conditioned_rows(op):
+    """Rows fifty standard deviations away from zero (mean 50, std 1) with
+    1% outliers of +-5: a one-pass E[x^2] - E[x]^2 in FP32 misses y by about
+    five times the tolerance here; the two-pass statistics (the mean removed
+    before the squares are summed) stay within about a third of it.  (Rows
+    much further off centre, say mean 1e3 and std 1e-2, are beyond FP32
+    itself: the FP32 inputs quantise the deviations to 0.6% of the spread,
+    and no FP32 y can match the double oracle to 1e-5.)  Every plan family:
+    default, register (guarded and whole tiles), loop, cluster and
+    staged."""
+    rng = np.random.default_rng(SEED + 1234)
+    for rows, cols in ((16, 4096), (6, 40000)):
+        x = (50.0 + rng.standard_normal((rows, cols))).astype(np.float32)
+        mask = rng.random((rows, cols)) < 0.01
+        x[mask] += np.where(rng.random(mask.sum()) < 0.5, -5.0,
+                            5.0).astype(np.float32)
+        d = inputs.make(op, rows, cols, SEED + cols)
+        d["x"] = x
+        if op == "residual_layernorm":
+            d["residual"] = rng.standard_normal((rows, cols)).astype(
+                np.float32) * np.float32(0.1)
+        ref = oracle.run(op, d)
+        plans = [None]
+        if cols == 4096:
+            plans += [mt.make_plan(256, 4, 4, 1),
+                      mt.make_plan(256, 4, 4, 2, flags=mt.MT_PLAN_PDL |
+                                   mt.MT_PLAN_WHOLE_TILES),
+                      mt.make_plan(128, 4, 0, 2, mt.MT_PATH_LOOP),
+                      mt.make_plan(128, 4, 4, 1, cluster=2)]
+        else:
+            plans += [mt.make_plan(256, 4, 0, 1, mt.MT_PATH_LOOP),
+                      mt.make_plan(256, 4, 16, 1, cluster=4)]
+            if op == "layernorm":
+                plans += [mt.make_plan(512, 4, 2, 1, mt.MT_PATH_STAGE)]
+        for p in plans:
+            if p is not None:
+                assert mt.mt_plan_check(mt.OP_IDS[op], cols, p) == mt.MT_OK
+            got = run_guarded(op, d, rows, cols, plan=p)
+            compare(op, got, ref, f"{op} ill-conditioned {rows}x{cols} " + (
+                "default" if p is None else mt.mt_describe_plan(p)))
+
+
 def test_softmax_special_rows():
     x = np.array([[1.0, np.nan, 2.0, 3.0], [1000.0, 1000.0, -1000.0, 0.0],
                   [5.0, 5.0, 5.0, 5.0], [-np.inf, 0.0, 0.0, -np.inf]],
