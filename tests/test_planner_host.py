@@ -197,3 +197,23 @@ def test_heldout_cases_cover_every_operator_and_type_outside_the_table():
             hit = (e_op == mt.OP_IDS[op] and e_dt == mt.DTYPE_IDS[dt] and
                    c0 <= cols <= c1 and r0 <= rows <= r1)
             assert not hit, (op, dt, rows, cols)
+
+
+def test_every_planned_shape_is_legal():
+    """The planner's choice (table, shape-derived fallback or heuristic)
+    passes the library's own legality check across row lengths from 1 to
+    2**21 (aligned and not), row counts from 1 to 2**20, every operator and
+    storage type."""
+    cols_list = sorted({1, 2, 3, 7, 31, 33, 127, 257, 300, 768, 1000, 1024,
+                        2500, 4096, 4103, 5000, 8192, 12288, 16385, 20000,
+                        32000, 32768, 50257, 65536, 100003, 131072, 300000,
+                        1 << 20, (1 << 21) + 8})
+    rows_list = (1, 2, 9, 10, 17, 38, 39, 76, 77, 128, 303, 304, 1000, 4096,
+                 65536, 1 << 20)
+    for op in mt.OP_IDS:
+        for dt in ("f32", "f16", "bf16"):
+            for cols in cols_list:
+                for rows in rows_list:
+                    p = plan(op, dt, rows, cols)
+                    st = mt.mt_plan_check_dtype(op, dt, cols, p)
+                    assert st == mt.MT_OK, (op, dt, rows, cols, p.as_dict())
