@@ -489,6 +489,62 @@ __device__ __forceinline__ float team_allreduce(float v, int W, int csize,
     return v;
 }
 
+// Row all-reduce of two sums at once (one shared-memory publication, one
+// barrier, one cluster barrier), in the same fixed order as team_allreduce.
+__device__ __forceinline__ void team_allreduce_sum2(float &a, float &b, int W,
+                                                    int csize,
+                                                    RedScratch &red,
+                                                    int &parity, int &cpar) {
+    if (W <= 32) {
+        for (int off = W >> 1; off > 0; off >>= 1) {
+            a += __shfl_xor_sync(kFull, a, off);
+            b += __shfl_xor_sync(kFull, b, off);
+        }
+    } else {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            a += __shfl_xor_sync(kFull, a, off);
+            b += __shfl_xor_sync(kFull, b, off);
+        }
+        const int lane = threadIdx.x & 31;
+        const int warp = threadIdx.x >> 5;
+        const int nw = W >> 5;
+        float(*buf)[32] = red.buf[parity];
+        parity ^= 1;
+        if (lane == 0) {
+            buf[0][warp] = a;
+            buf[1][warp] = b;
+        }
+        __syncthreads();
+        const int first = warp & ~(nw - 1);
+        float ta = lane < nw ? buf[0][first + lane] : 0.f;
+        float tb = lane < nw ? buf[1][first + lane] : 0.f;
+        for (int off = nw >> 1; off > 0; off >>= 1) {
+            ta += __shfl_xor_sync(kFull, ta, off);
+            tb += __shfl_xor_sync(kFull, tb, off);
+        }
+        a = __shfl_sync(kFull, ta, 0);
+        b = __shfl_sync(kFull, tb, 0);
+    }
+    if (csize > 1) {
+        if (threadIdx.x == 0) {
+            red.cl[cpar][0] = a;
+            red.cl[cpar][1] = b;
+        }
+        cluster_sync();
+        const int lane = threadIdx.x & 31;
+        float ta = lane < csize ? ld_cluster(&red.cl[cpar][0], lane) : 0.f;
+        float tb = lane < csize ? ld_cluster(&red.cl[cpar][1], lane) : 0.f;
+        for (int off = csize >> 1; off > 0; off >>= 1) {
+            ta += __shfl_xor_sync(kFull, ta, off);
+            tb += __shfl_xor_sync(kFull, tb, off);
+        }
+        a = __shfl_sync(kFull, ta, 0);
+        b = __shfl_sync(kFull, tb, 0);
+        cpar ^= 1;
+    }
+}
+
 __device__ __forceinline__ void team_allreduce_compensated(
     float &s, float &c, int W, int csize, RedScratch &red, int &parity,
     int &cpar) {
@@ -749,6 +805,16 @@ __device__ __forceinline__ void reg_body(const KArgs &a) {
         const int nb = geo.nb;
         const bool head = kHead && active && worker < geo.hd;
 
+        // LayerNorm's pivot, the row's first value: loaded ahead of the
+        // row so that its latency hides under the row's own.
+        float piv = 0.f;
+        if constexpr (OP == OP_LAYERNORM || OP == OP_RESIDUAL_LAYERNORM) {
+            piv = to_f(X[geo.base]);
+            if constexpr (has_residual<OP>())
+                piv = __fadd_rn(piv,
+                                to_f(static_cast<const T *>(a.res)[geo.base]));
+        }
+
         // ---- single read of the row into registers --------------------
         float v[K][V];
         float hv = fill;
@@ -827,20 +893,16 @@ __device__ __forceinline__ void reg_body(const KArgs &a) {
                     from_f<T>(hv * r * param_at(Wt, worker, 1.f));
         } else if constexpr (OP == OP_LAYERNORM ||
                              OP == OP_RESIDUAL_LAYERNORM) {
-            float acc[V];
+            // Shifted moments: the sums of d = x - x0 and d^2 about the
+            // row's first value x0 (every thread reads it: a cache hit)
+            // in one reduction of two values, then mean = x0 + mean(d) and
+            // var = mean(d^2) - mean(d)^2.  x0 lies in the row's spread, so
+            // the subtraction loses no more than a few units of the
+            // spread's own rounding.
+            const float x0 = piv;
+            float s1v[V], s2v[V];
 #pragma unroll
-            for (int e = 0; e < V; ++e) acc[e] = 0.f;
-#pragma unroll
-            for (int k = 0; k < K; ++k)
-#pragma unroll
-                for (int e = 0; e < V; ++e) acc[e] += v[k][e];
-            float s = hv;
-#pragma unroll
-            for (int e = 0; e < V; ++e) s += acc[e];
-            s = team_allreduce<SumOp>(s, W, csize, red, parity, cpar);
-            const float mean = s / (float)cols;
-#pragma unroll
-            for (int e = 0; e < V; ++e) acc[e] = 0.f;
+            for (int e = 0; e < V; ++e) s1v[e] = s2v[e] = 0.f;
 #pragma unroll
             for (int k = 0; k < K; ++k) {
                 const int off = (k * WT + worker) * V;
@@ -848,23 +910,29 @@ __device__ __forceinline__ void reg_body(const KArgs &a) {
                 const bool pack_in = active && off < nb;
 #pragma unroll
                 for (int e = 0; e < V; ++e) {
-                    const float d = v[k][e] - mean;
-                    // Whole tiles keep the deviation in place of the value
-                    // (the epilogue forms the same bits from it).
-                    if constexpr (FU) v[k][e] = d;
-                    if (FU || (AL ? pack_in : (active && off + e < nb)))
-                        acc[e] = fmaf(d, d, acc[e]);
+                    const float d = v[k][e] - x0;
+                    if (FU || (AL ? pack_in : (active && off + e < nb))) {
+                        s1v[e] += d;
+                        s2v[e] = fmaf(d, d, s2v[e]);
+                    }
                 }
             }
-            float q = 0.f;
+            float s1 = 0.f, s2 = 0.f;
             if (head) {
-                const float d = hv - mean;
-                q = d * d;
+                const float d = hv - x0;
+                s1 = d;
+                s2 = d * d;
             }
 #pragma unroll
-            for (int e = 0; e < V; ++e) q += acc[e];
-            q = team_allreduce<SumOp>(q, W, csize, red, parity, cpar);
-            const float rstd = rsqrtf(q / (float)cols + a.eps);
+            for (int e = 0; e < V; ++e) {
+                s1 += s1v[e];
+                s2 += s2v[e];
+            }
+            team_allreduce_sum2(s1, s2, W, csize, red, parity, cpar);
+            const float md = s1 / (float)cols;
+            const float var = fmaxf(fmaf(-md, md, s2 / (float)cols), 0.f);
+            const float mean = x0 + md;
+            const float rstd = rsqrtf(var + a.eps);
             T *yb = Y + geo.base + geo.hd;
 #pragma unroll
             for (int k = 0; k < K; ++k) {
@@ -876,8 +944,7 @@ __device__ __forceinline__ void reg_body(const KArgs &a) {
                                          0.f, bv);
 #pragma unroll
                 for (int e = 0; e < V; ++e)
-                    o[e] = fmaf((FU ? v[k][e] : v[k][e] - mean) * rstd,
-                                gv[e], bv[e]);
+                    o[e] = fmaf((v[k][e] - mean) * rstd, gv[e], bv[e]);
                 store_pack<T, V, AL, FU>(yb, off, nb, active, yvec, o);
             }
             if (head)
