@@ -110,8 +110,8 @@ typedef enum mt_path {
      * thread) and written from them. */
     MT_PATH_REGISTERS = 0,
     /* Rows too wide for registers: a strided loop computes the statistics
-     * and a second (LayerNorm: third) loop re-reads x to write y.  Row sum
-     * and cross-entropy need only the first loop. */
+     * and a second loop re-reads x to write y.  Row sum and cross-entropy
+     * need only the first loop. */
     MT_PATH_LOOP = 1,
     /* Rows staged in shared memory: each CTA (of a cluster of
      * `cluster` CTAs per row) copies its contiguous run of the row, at most

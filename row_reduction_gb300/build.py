@@ -26,7 +26,7 @@ OPS = ("rmsnorm", "layernorm", "residual_layernorm", "softmax", "row_sum",
 DTYPES = ("f32", "f16", "bf16")
 SOURCES = (["api.cpp", "planner.cpp", "mean.cu", "probe.cu"] +
            [f"ops_{op}_{dt}.cu" for op in OPS for dt in DTYPES])
-DEPENDS = ["mt_internal.h", "mt_kernels.cuh", "plan_table.inc"]
+DEPENDS = ["mt_internal.h", "mt_kernels.cuh", "mt_stage.cuh", "plan_table.inc"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler",

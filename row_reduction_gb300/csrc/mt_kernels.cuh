@@ -1248,27 +1248,27 @@ __global__ void __launch_bounds__(kLoopMaxThreads) loop_kernel(const KArgs a) {
                 });
         } else if constexpr (OP == OP_LAYERNORM ||
                              OP == OP_RESIDUAL_LAYERNORM) {
-            float s = 0.f;
-            stream_row<V, AL, U>(worker, WT, hd, nb, active, load_x,
-                                 [&](const float *t, int nv, int) {
-#pragma unroll
-                                     for (int e = 0; e < V; ++e)
-                                         if (e < nv) s += t[e];
-                                 });
-            s = team_allreduce<SumOp>(s, W, csize, red, parity, cpar);
-            const float mean = s / (float)cols;
-            float q = 0.f;
+            // Shifted moments about the row's first value (as on the
+            // register path): one pass and one reduction for the
+            // statistics, then the output pass.
+            float x0 = 0.f;
+            load_x(-1, 1, &x0);  // column 0 of the row
+            float s1 = 0.f, s2 = 0.f;
             stream_row<V, AL, U>(worker, WT, hd, nb, active, load_x,
                                  [&](const float *t, int nv, int) {
 #pragma unroll
                                      for (int e = 0; e < V; ++e)
                                          if (e < nv) {
-                                             const float d = t[e] - mean;
-                                             q = fmaf(d, d, q);
+                                             const float d = t[e] - x0;
+                                             s1 += d;
+                                             s2 = fmaf(d, d, s2);
                                          }
                                  });
-            q = team_allreduce<SumOp>(q, W, csize, red, parity, cpar);
-            const float rstd = rsqrtf(q / (float)cols + a.eps);
+            team_allreduce_sum2(s1, s2, W, csize, red, parity, cpar);
+            const float md = s1 / (float)cols;
+            const float mean = x0 + md;
+            const float rstd = rsqrtf(
+                fmaxf(fmaf(-md, md, s2 / (float)cols), 0.f) + a.eps);
             T *yb = Y + base + hd;
             T *H = static_cast<T *>(a.h);
             T *hb = H ? H + base + hd : nullptr;
