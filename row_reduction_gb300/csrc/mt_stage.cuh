@@ -19,9 +19,10 @@
 // from the staged values, the cross-warp and cross-CTA combines of
 // team_allreduce*, one rounding at the store ("Thread Ownership and
 // Software Staging", §Register-tiled reductions).  Passes over the staged
-// run: RMSNorm 2, LayerNorm 2 (shifted moments, then the output), softmax
-// and log-softmax 2 (a running max/sum, then the output), cross-entropy and
-// row sum 1.
+// run: RMSNorm 2, LayerNorm 2 (shifted moments, then the output; 16-bit
+// rows on a lone CTA 3: the mean, the deviations, the output), softmax and
+// log-softmax 2 (a running max/sum, then the output), cross-entropy and row
+// sum 1.
 //
 // The path needs every row to start on a 16-byte boundary (aligned mode:
 // cols a multiple of V and 16-byte aligned pointers).
@@ -253,38 +254,66 @@ __global__ void __launch_bounds__(kStageMaxThreads)
                 st_vec<T, V>(Y + ybase + (int64_t)u * V, o);
             });
         } else if constexpr (OP == OP_LAYERNORM) {
-            // Shifted moments about the row's first value x0 (every CTA of
-            // the cluster reads it from global memory): one pass and one
-            // reduction for the statistics.
-            // One accumulator pair per value of a unit keeps the addition
-            // chains short.
-            const float x0 = to_f(xrow[0]);
-            float s1v[V], s2v[V];
+            float mean, rstd;
+            if constexpr (sizeof(T) == 2 && !CL) {
+                // 16-bit rows on a lone CTA: the mean, then the squared
+                // deviations about it, both from the staged run (measured
+                // faster here than the one-pass form below).
+                float s = 0.f;
+                for (int j = 0; j < npieces; ++j) {
+                    wait_piece(j);
+                    for_units<T, U>(sbuf, piece_lo(j), piece_hi(j), W,
+                                    [&](const float *t, int) {
 #pragma unroll
-            for (int e = 0; e < V; ++e) s1v[e] = s2v[e] = 0.f;
-            for (int j = 0; j < npieces; ++j) {
-                wait_piece(j);
-                for_units<T, U>(sbuf, piece_lo(j), piece_hi(j), W,
-                                [&](const float *t, int) {
+                                        for (int e = 0; e < V; ++e) s += t[e];
+                                    });
+                }
+                s = team_allreduce<SumOp>(s, W, csize, red, parity, cpar);
+                mean = s / (float)cols;
+                float q = 0.f;
+                for_units<T, U>(sbuf, 0, ucnt, W, [&](const float *t, int) {
 #pragma unroll
-                                    for (int e = 0; e < V; ++e) {
-                                        const float d = t[e] - x0;
-                                        s1v[e] += d;
-                                        s2v[e] = fmaf(d, d, s2v[e]);
-                                    }
-                                });
+                    for (int e = 0; e < V; ++e) {
+                        const float d = t[e] - mean;
+                        q = fmaf(d, d, q);
+                    }
+                });
+                q = team_allreduce<SumOp>(q, W, csize, red, parity, cpar);
+                rstd = rsqrtf(q / (float)cols + a.eps);
+            } else {
+                // Shifted moments about the row's first value x0 (every CTA
+                // of a cluster reads it from global memory; only rank 0
+                // stages column 0): one pass and one reduction.  One
+                // accumulator pair per value of a unit keeps the addition
+                // chains short.
+                const float x0 = to_f(xrow[0]);
+                float s1v[V], s2v[V];
+#pragma unroll
+                for (int e = 0; e < V; ++e) s1v[e] = s2v[e] = 0.f;
+                for (int j = 0; j < npieces; ++j) {
+                    wait_piece(j);
+                    for_units<T, U>(sbuf, piece_lo(j), piece_hi(j), W,
+                                    [&](const float *t, int) {
+#pragma unroll
+                                        for (int e = 0; e < V; ++e) {
+                                            const float d = t[e] - x0;
+                                            s1v[e] += d;
+                                            s2v[e] = fmaf(d, d, s2v[e]);
+                                        }
+                                    });
+                }
+                float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+                for (int e = 0; e < V; ++e) {
+                    s1 += s1v[e];
+                    s2 += s2v[e];
+                }
+                team_allreduce_sum2(s1, s2, W, csize, red, parity, cpar);
+                const float md = s1 / (float)cols;
+                mean = x0 + md;
+                rstd = rsqrtf(fmaxf(fmaf(-md, md, s2 / (float)cols), 0.f) +
+                              a.eps);
             }
-            float s1 = 0.f, s2 = 0.f;
-#pragma unroll
-            for (int e = 0; e < V; ++e) {
-                s1 += s1v[e];
-                s2 += s2v[e];
-            }
-            team_allreduce_sum2(s1, s2, W, csize, red, parity, cpar);
-            const float md = s1 / (float)cols;
-            const float mean = x0 + md;
-            const float rstd = rsqrtf(
-                fmaxf(fmaf(-md, md, s2 / (float)cols), 0.f) + a.eps);
             for_units<T, U>(sbuf, 0, ucnt, W, [&](const float *t, int u) {
                 const int col = (u0 + u) * V;
                 float gv[V], bv[V], o[V];
