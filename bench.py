@@ -53,7 +53,13 @@ METRIC = ("RMSNorm FP32 µs/op and HBM GB/s (% of GB300 peak), "
           "1×127 … 1024×4096")
 FALLBACK_HBM_GBS = 6800.0
 DATASHEET_HBM_GBS = 7900.0   # GB300 HBM3e nominal, for context only
-HEADLINE_MAX_BYTES = 1536
+HEADLINE_MAX_BYTES = 2048
+# Fields the headline gives up, in this order, if it would exceed
+# HEADLINE_MAX_BYTES (long plan strings, every throttle reason): all of them
+# stay in the --details file.
+HEADLINE_OPTIONAL = (("cpu_baseline", "cpu"), ("config", "l2"),
+                     ("roofline", "peak_source"), ("rounds_us",),
+                     ("floor",), ("e2e", "us_per_step"))
 H_OUT_OPS = ("residual_layernorm", "residual_rmsnorm")
 # Operators with one input matrix x and one output matrix y of its shape:
 # the copy floor moves exactly their matrix bytes.  Operators that read x
@@ -323,10 +329,21 @@ def cpu_baseline(op, d, rows, cols, budget_s=10.0, dtype="f32"):
 
 
 def headline_json(line):
-    """The headline as one compact JSON line; raises if it would exceed
-    HEADLINE_MAX_BYTES (a reader that keeps only the tail of stdout must
-    still see all of it)."""
+    """The headline as one compact JSON line of at most HEADLINE_MAX_BYTES
+    (a reader that keeps only the tail of stdout must still see all of it):
+    the HEADLINE_OPTIONAL fields go first, one at a time, while it is too
+    long; raises if the line without them is still too long."""
+    line = json.loads(json.dumps(line))      # private copy
     text = json.dumps(line, separators=(",", ":"))
+    for path in HEADLINE_OPTIONAL:
+        if len(text.encode()) <= HEADLINE_MAX_BYTES:
+            break
+        node = line
+        for key in path[:-1]:
+            node = node.get(key) if isinstance(node, dict) else None
+        if isinstance(node, dict):
+            node.pop(path[-1], None)
+        text = json.dumps(line, separators=(",", ":"))
     n = len(text.encode())
     if n > HEADLINE_MAX_BYTES:
         raise ValueError(f"headline is {n} bytes, over {HEADLINE_MAX_BYTES}")

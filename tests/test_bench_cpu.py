@@ -141,6 +141,40 @@ def test_headline_over_the_cap_is_refused():
         bench.headline_json(line)
 
 
+def test_headline_gives_up_optional_fields_before_failing(monkeypatch):
+    import bench
+    f = _figures(plan="path=staged W=512 V=4 chunks=8 rows_per_block=1 "
+                      "threads=512 grid=auto cluster=16 pdl prefetch_next "
+                      "whole_tiles")
+    f["clocks"]["reasons"] = list(bench.ClockSampler.NAMES)
+    line = bench.build_headline(f)
+    full = bench.headline_json(line)
+    assert json.loads(full) == json.loads(json.dumps(line))
+    # A cap between the line with and without the first optional fields:
+    # those go, in order, and the rest stays.
+    n = len(full.encode())
+    monkeypatch.setattr(bench, "HEADLINE_MAX_BYTES", n - 60)
+    back = json.loads(bench.headline_json(line))
+    assert "cpu" not in back["cpu_baseline"]
+    assert "l2" not in back["config"]
+    assert "rounds_us" in back and "floor" in back
+    # The smallest cap the line can meet: every optional field gone, every
+    # key the metric needs kept.
+    monkeypatch.setattr(bench, "HEADLINE_MAX_BYTES", 1170)
+    back = json.loads(bench.headline_json(line))
+    for path in bench.HEADLINE_OPTIONAL:
+        node = back
+        for key in path[:-1]:
+            node = node[key]
+        assert path[-1] not in node, path
+    for key in ("value", "roofline", "cpu_baseline", "e2e", "clocks",
+                "gpu_launches", "config"):
+        assert key in back, key
+    assert back["roofline"]["traffic"] == f["traffic"]
+    assert back["e2e"]["h2d_bytes_per_step"] == f["h2d"]
+    assert line["config"]["l2"]            # the caller's line is untouched
+
+
 def test_headline_is_the_last_stdout_line(capsys):
     import bench
     print('{"op": "rmsnorm", "a sweep row": 1}')
