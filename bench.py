@@ -53,7 +53,7 @@ METRIC = ("RMSNorm FP32 µs/op and HBM GB/s (% of GB300 peak), "
           "1×127 … 1024×4096")
 FALLBACK_HBM_GBS = 6800.0
 DATASHEET_HBM_GBS = 7900.0   # GB300 HBM3e nominal, for context only
-HEADLINE_MAX_BYTES = 2048
+HEADLINE_MAX_BYTES = 1536
 # Fields the headline gives up, in this order, if it would exceed
 # HEADLINE_MAX_BYTES (long plan strings, every throttle reason): all of them
 # stay in the --details file.
